@@ -1,0 +1,444 @@
+"""Benchmark of the fused pattern out = alpha * X^T (v * (X y)) + beta * z on GB300.
+
+Default workload: dense fp32 X 16,000,000 x 32 row-major, X, y, z ~ N(0, 1),
+v ~ U[0.1, 2], alpha = 2, beta = -1 (the full pattern with every step of the path).
+A step is one fused call over that input. Inputs (2.1 GB) exceed L2 (129 MB), so no
+flush is needed between steps.
+
+Prints one JSON line. ``value`` is effective GB/s: the algorithmic bytes of a call
+(X once, y, v, z, out) over its device time, inputs resident in HBM. ``e2e`` is the
+same metric with the host-to-device copy of the inputs (pinned memory) and the
+device-to-host copy of out inside the timed region. ``roofline`` relates the fused
+kernel to the measured HBM copy bandwidth; ``cpu_baseline`` is the C oracle timed on
+this host's cores; ``unfused_library`` is the three-call cuBLAS sequence
+(gemv, scale, transposed gemv) on the same GPU.
+
+--impl reference times the oracle (the CPU reference of this pattern) instead, on a
+bounded sample of the same workload, and prints the same line with "impl": "reference".
+--workload picks another configuration; --all prints one line per configuration.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "fused aX^T(v.*Xy)+bz: effective GB/s and % of GB300 HBM peak"
+FALLBACK_HBM_GBS = 6800.0
+
+WORKLOADS = {
+    "dense_small": ("dense f64 1000 x 64, U[-1,1], alpha=1.5, beta=0.5", lambda g: g.dense_small()),
+    "dense_tall_a": ("dense f32 16,000,000 x 32, N(0,1) X/y, v U[0.1,2], alpha=1, beta=0, no z",
+                     lambda g: g.dense_tall(variant="a")),
+    "dense_tall_b": ("dense f32 16,000,000 x 32, N(0,1) X/y/z, v U[0.1,2], alpha=2, beta=-1",
+                     lambda g: g.dense_tall(variant="b")),
+    "dense_tall_c": ("dense f32 16,000,000 x 32, N(0,1) X/y, v=1 (X^T X y), alpha=1, beta=0",
+                     lambda g: g.dense_tall(variant="c")),
+    "dense_wide": ("dense f64 20,000 x 20,000, U[-1,1], alpha=0.7, beta=0.3", lambda g: g.dense_wide()),
+    "csr_uniform": ("CSR f64 4,000,000 x 10,000, Poisson(50) uniform distinct columns, U[-1,1], alpha=beta=1",
+                    lambda g: g.csr_uniform()),
+    "csr_powerlaw": ("CSR f32 2,000,000 x 1,000,000, Zipf(1.5) row lengths (mean 100, cap 50,000), Zipf(1.1) "
+                     "columns, N(0,1) vals/y, v U[0,1], alpha=1, beta=0", lambda g: g.csr_powerlaw()),
+}
+PROFILED_KERNEL = {"dense": "dense_narrow_kernel", "dense_wide": "dense_wide_kernel", "csr": "csr_rows_kernel"}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            for k in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs"):
+                if k in d:
+                    return float(d[k]), "measured", d
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback", {}
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dense_linear_algebra_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, fn), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(key: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        d = json.load(open(path)).get(key)
+    except Exception:
+        return None
+    if not d or d.get("source_sha") != source_sha():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def cpu_oracle_time(p, budget_s: float, min_reps: int = 1, max_reps: int = 5):
+    """Times the oracle's double-accumulator pass (one thread) on problem p."""
+    import oracle
+
+    times = []
+    t_all = time.perf_counter()
+    while len(times) < max_reps:
+        t0 = time.perf_counter()
+        oracle.solve(p, acc="d")
+        times.append(time.perf_counter() - t0)
+        if len(times) >= min_reps and time.perf_counter() - t_all > budget_s:
+            break
+    return statistics.median(times), len(times)
+
+
+def sample_problem(p, rows: int):
+    """The first `rows` rows of a problem (same recipe, bounded CPU work)."""
+    import inputgen
+
+    if p.kind == "dense" or rows >= p.m:
+        if rows >= p.m:
+            return p
+        return inputgen.Problem(p.name + f"_first{rows}", p.kind, p.dtype, rows, p.n, p.alpha, p.beta, y=p.y,
+                                v=None if p.v is None else p.v[:rows], z=p.z, X=p.X[:rows], ld=p.ld)
+    rp = p.row_ptr[: rows + 1].copy()
+    nnz = int(rp[-1])
+    return inputgen.Problem(p.name + f"_first{rows}", p.kind, p.dtype, rows, p.n, p.alpha, p.beta, y=p.y,
+                            v=None if p.v is None else p.v[:rows], z=p.z, row_ptr=rp, col_idx=p.col_idx[:nnz],
+                            vals=p.vals[:nnz])
+
+
+def run_reference(args, name, desc, p):
+    """--impl reference: the oracle on the host cores, a bounded sample per step."""
+    rows = max(1, p.m // 4)
+    sp = sample_problem(p, rows)
+    for _ in range(args.warmup):
+        cpu_oracle_time(sp, 0.0, 1, 1)
+    ts = [cpu_oracle_time(sp, 0.0, 1, 1)[0] for _ in range(args.steps)]
+    t = statistics.median(ts)
+    val = sp.ideal_bytes() / t / 1e9
+    sample = f"first {rows} of {p.m} rows of the workload ({sp.ideal_bytes()} algorithmic bytes) per step"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype_name(p), "data": "synthetic",
+        "config": {"workload": desc, "name": name},
+        "cpu_baseline": {"value": round(val, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(val, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def dtype_name(p):
+    return "f32" if np.dtype(p.dtype) == np.float32 else "f64"
+
+
+def run_fused(args, name, desc, p, rank, world, dist):
+    import torch
+
+    import dense_linear_algebra_gb300 as fx
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream(dev)
+
+    def pin(a):
+        return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+
+    host = {}
+    if p.kind == "dense":
+        host["X"] = pin(p.X)
+    else:
+        host["row_ptr"], host["col_idx"], host["vals"] = pin(p.row_ptr), pin(p.col_idx), pin(p.vals)
+    host["y"], host["v"], host["z"] = pin(p.y), pin(p.v), pin(p.z)
+    d = {k: (None if t is None else t.to(dev, non_blocking=False)) for k, t in host.items()}
+    out = torch.empty(p.n, dtype=d["y"].dtype, device=dev)
+    out_host = torch.empty(p.n, dtype=d["y"].dtype).pin_memory()
+
+    if p.kind == "dense":
+        X = d["X"][:, : p.n]
+
+        def call(o=out):
+            return fx.dense(X, d["y"], d["v"], p.alpha, p.beta, d["z"], out=o, stream=stream)
+        launches = 1 if p.n * p.itemsize <= 2048 else 2
+    else:
+        def call(o=out):
+            return fx.csr(d["row_ptr"], d["col_idx"], d["vals"], d["y"], p.n, d["v"], p.alpha, p.beta, d["z"],
+                          out=o, stream=stream)
+        launches = 3
+
+    ideal = p.ideal_bytes()
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize()
+
+    # device-timed steps, inputs resident
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    smi_index = vis.split(",")[dev.index] if vis else str(dev.index)
+    with ClockSampler(smi_index) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for a, b in ev:
+            a.record(stream)
+            call()
+            b.record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    per = [a.elapsed_time(b) for a, b in ev]  # ms per call
+    total_ms = t_start.elapsed_time(t_end)
+    ms_step = total_ms / args.steps
+    if dist:
+        tt = torch.tensor([ms_step], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_step = float(tt.item())
+    value = world * ideal / (ms_step * 1e-3) / 1e9
+    kernel_ms = statistics.mean(per)
+
+    # end to end: H2D of the step's inputs, the call, D2H of out
+    h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
+    d2h = out_host.numel() * out_host.element_size()
+    e_steps = max(3, min(args.steps, 10))
+    for _ in range(2):
+        for k, t in host.items():
+            if t is not None:
+                d[k].copy_(t, non_blocking=True)
+        call()
+        out_host.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        for k, t in host.items():
+            if t is not None:
+                d[k].copy_(t, non_blocking=True)
+        call()
+        out_host.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e_steps
+    e2e_val = ideal / (e2e_ms * 1e-3) / 1e9
+
+    # the unfused library sequence on the same GPU (dense: cuBLAS gemv, scale, transposed gemv)
+    unfused = None
+    if p.kind == "dense":
+        try:
+            Xt = X
+            tz = d["z"] if (d["z"] is not None and p.beta != 0) else torch.zeros(p.n, dtype=out.dtype, device=dev)
+
+            def lib_seq():
+                u = torch.mv(Xt, d["y"])
+                t = u * d["v"] if d["v"] is not None else u
+                return torch.addmv(tz, Xt.t(), t, beta=p.beta, alpha=p.alpha)
+            for _ in range(3):
+                lib_seq()
+            torch.cuda.synchronize()
+            u0 = torch.cuda.Event(enable_timing=True)
+            u1 = torch.cuda.Event(enable_timing=True)
+            u0.record(stream)
+            for _ in range(args.steps):
+                lib_seq()
+            u1.record(stream)
+            torch.cuda.synchronize()
+            ums = u0.elapsed_time(u1) / args.steps
+            unfused = {"what": "torch.mv (cuBLAS gemv N), v scale, torch.addmv on X^T (cuBLAS gemv T)",
+                       "ms_per_step": round(ums, 4), "value": round(ideal / (ums * 1e-3) / 1e9, 2), "unit": "GB/s",
+                       "fused_speedup": round(ums / ms_step, 3)}
+        except Exception as e:  # report, do not fail the bench
+            unfused = {"error": str(e)[:200]}
+    else:
+        try:
+            Xs = torch.sparse_csr_tensor(d["row_ptr"], d["col_idx"], d["vals"], size=(p.m, p.n))
+            XsT = Xs.t().to_sparse_csr()
+            tz = d["z"] if (d["z"] is not None and p.beta != 0) else torch.zeros(p.n, dtype=out.dtype, device=dev)
+
+            def lib_seq():
+                u = torch.mv(Xs, d["y"])
+                t = u * d["v"] if d["v"] is not None else u
+                return torch.addmv(tz, XsT, t, beta=p.beta, alpha=p.alpha)
+            for _ in range(3):
+                lib_seq()
+            torch.cuda.synchronize()
+            u0 = torch.cuda.Event(enable_timing=True)
+            u1 = torch.cuda.Event(enable_timing=True)
+            u0.record(stream)
+            for _ in range(args.steps):
+                lib_seq()
+            u1.record(stream)
+            torch.cuda.synchronize()
+            ums = u0.elapsed_time(u1) / args.steps
+            unfused = {"what": "torch CSR mv (cuSPARSE SpMV), v scale, addmv on a pre-transposed CSR copy of X",
+                       "ms_per_step": round(ums, 4), "value": round(ideal / (ums * 1e-3) / 1e9, 2), "unit": "GB/s",
+                       "fused_speedup": round(ums / ms_step, 3)}
+            del Xs, XsT
+        except Exception as e:
+            unfused = {"error": str(e)[:200]}
+
+    peak, peak_kind, _ = measured_peaks()
+    key = f"{PROFILED_KERNEL['dense_wide' if (p.kind == 'dense' and launches == 2) else p.kind]} {name}"
+    traffic = profiled_traffic(key)
+    achieved = ideal / (kernel_ms * 1e-3) / 1e9
+    rec = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype_name(p), "data": "synthetic",
+        "config": {"workload": desc, "name": name, "algorithmic_bytes_per_step": ideal,
+                   "l2": "inputs larger than L2 (129 MB); no flush" if ideal > 256e6 else
+                         "inputs fit in L2: hot-L2 figure",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "us_per_call": round(kernel_ms * 1e3, 2),
+        "hbm_pct_of_peak": round(100 * value / world / peak, 2),
+        "hbm_pct_of_nominal_7900": round(100 * value / world / 7900.0, 2),
+        "clocks": clk.summary(),
+        "e2e": {"value": round(e2e_val, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": launches * args.steps,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": f"{peak_kind} HBM copy bandwidth",
+                     "kernel": PROFILED_KERNEL['dense_wide' if (p.kind == 'dense' and launches == 2) else p.kind]},
+        "unfused_library": unfused,
+    }
+    if p.kind == "csr":
+        rec["config"]["nnz"] = p.nnz
+    return rec
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="fused", choices=["fused", "reference"])
+    ap.add_argument("--workload", default="dense_tall_b", choices=sorted(WORKLOADS))
+    ap.add_argument("--all", action="store_true", help="one line per workload")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    import inputgen
+
+    rank, world, local = dist_env()
+    names = sorted(WORKLOADS) if args.all else [args.workload]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        for name in names:
+            desc, mk = WORKLOADS[name]
+            print(json.dumps(run_reference(args, name, desc, mk(inputgen))), flush=True)
+        return
+
+    import torch
+
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl")
+        dist = tdist
+    else:
+        torch.cuda.set_device(0)
+
+    for name in names:
+        desc, mk = WORKLOADS[name]
+        p = mk(inputgen)
+        rec = run_fused(args, name, desc, p, rank, world, dist)
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            t, reps = cpu_oracle_time(p, budget_s=10.0, min_reps=1, max_reps=3)
+            rec["cpu_baseline"] = {"value": round(p.ideal_bytes() / t / 1e9, 4), "unit": "GB/s", "cores": 1,
+                                   "kind": "oracle",
+                                   "sample": f"the whole workload ({p.ideal_bytes()} algorithmic bytes), double "
+                                             f"accumulator, single thread, median of {reps} runs of {t:.2f} s",
+                                   "host_cores": os.cpu_count()}
+        if rank == 0:
+            print(json.dumps(rec), flush=True)
+        del p
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

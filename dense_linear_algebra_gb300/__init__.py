@@ -1,0 +1,37 @@
+"""libfusedxtx for GB300: ``out = alpha * X^T (v * (X y)) + beta * z`` in one pass over X.
+
+The pattern and its instantiations come from "On optimizing machine learning
+workloads via kernel fusion" (abstract). Every step of the computation runs in the
+CUDA kernels of ``libfusedxtx.so`` (sources in ``csrc/``, C ABI in
+``include/fxtx.h``); this package only marshals arguments. There is no CPU
+fallback: if the library cannot be loaded, importing the binding fails.
+
+Raw C-ABI calls (pointers as ints, stream as a cudaStream_t int) carry the C names:
+``fxtx_dense_f32``, ``fxtx_dense_f64``, ``fxtx_csr_f32``, ``fxtx_csr_f64``,
+``fxtx_csr_validate``, ``fxtx_device_error``, ``fxtx_status_string``,
+``fxtx_plan_describe``. ``dense`` and ``csr`` take torch CUDA tensors.
+"""
+from ._lib import (  # noqa: F401
+    FXTX_ERR_ALLOC,
+    FXTX_ERR_BAD_CSR,
+    FXTX_ERR_CUDA,
+    FXTX_ERR_INVALID_ARG,
+    FXTX_ERR_TIMEOUT,
+    FXTX_ERR_UNSUPPORTED,
+    FXTX_OK,
+    FxtxError,
+    csr,
+    csr_validate,
+    dense,
+    device_error,
+    fxtx_csr_f32,
+    fxtx_csr_f64,
+    fxtx_csr_validate,
+    fxtx_dense_f32,
+    fxtx_dense_f64,
+    fxtx_device_error,
+    fxtx_plan_describe,
+    fxtx_status_string,
+    library_path,
+    plan_describe,
+)

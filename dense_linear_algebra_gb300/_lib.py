@@ -1,0 +1,175 @@
+"""ctypes binding over libfusedxtx's C ABI (argument marshalling only)."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+FXTX_OK = 0
+FXTX_ERR_INVALID_ARG = 1
+FXTX_ERR_UNSUPPORTED = 2
+FXTX_ERR_CUDA = 3
+FXTX_ERR_ALLOC = 4
+FXTX_ERR_BAD_CSR = 5
+FXTX_ERR_TIMEOUT = 6
+
+
+def _load() -> ctypes.CDLL:
+    path = _build.LIB
+    if not os.path.exists(path) or _build._stale():
+        try:
+            _build.build()
+        except Exception as e:  # no silent fallback: the library is the product
+            raise ImportError(f"libfusedxtx could not be built or loaded from {path}: {e}") from e
+    lib = ctypes.CDLL(path)
+    i32, i64, f32, f64, vp = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_double, ctypes.c_void_p
+    lib.fxtx_dense_f32.argtypes = [i64, i64, vp, i64, vp, vp, f32, f32, vp, vp, vp]
+    lib.fxtx_dense_f64.argtypes = [i64, i64, vp, i64, vp, vp, f64, f64, vp, vp, vp]
+    lib.fxtx_csr_f32.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, f32, f32, vp, vp, vp]
+    lib.fxtx_csr_f64.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, f64, f64, vp, vp, vp]
+    lib.fxtx_csr_validate.argtypes = [i64, i64, i64, vp, vp, vp]
+    lib.fxtx_device_error.argtypes = [vp]
+    lib.fxtx_status_string.argtypes = [i32]
+    lib.fxtx_status_string.restype = ctypes.c_char_p
+    lib.fxtx_plan_describe.argtypes = [i32, i32, i64, i64, i64, i64, ctypes.c_char_p, i64]
+    for name in ("fxtx_dense_f32", "fxtx_dense_f64", "fxtx_csr_f32", "fxtx_csr_f64", "fxtx_csr_validate",
+                 "fxtx_device_error", "fxtx_plan_describe"):
+        getattr(lib, name).restype = i32
+    return lib
+
+
+_lib = _load()
+library_path = _build.LIB
+
+fxtx_dense_f32 = _lib.fxtx_dense_f32
+fxtx_dense_f64 = _lib.fxtx_dense_f64
+fxtx_csr_f32 = _lib.fxtx_csr_f32
+fxtx_csr_f64 = _lib.fxtx_csr_f64
+fxtx_csr_validate = _lib.fxtx_csr_validate
+fxtx_device_error = _lib.fxtx_device_error
+fxtx_plan_describe = _lib.fxtx_plan_describe
+
+
+def fxtx_status_string(status: int) -> str:
+    return _lib.fxtx_status_string(int(status)).decode()
+
+
+class FxtxError(RuntimeError):
+    def __init__(self, status: int, where: str = ""):
+        self.status = status
+        super().__init__(f"{where}: {fxtx_status_string(status)}" if where else fxtx_status_string(status))
+
+
+def _check(status: int, where: str) -> None:
+    if status != FXTX_OK:
+        raise FxtxError(status, where)
+
+
+def plan_describe(kind: str, dtype: str, m: int, n: int, nnz: int = 0, ld: int | None = None) -> str:
+    """The launch plan the analytical model picks (host only)."""
+    buf = ctypes.create_string_buffer(512)
+    _check(fxtx_plan_describe(1 if kind == "csr" else 0, 1 if dtype in ("f64", "float64") else 0, m, n, nnz,
+                              n if ld is None else ld, buf, 512), "fxtx_plan_describe")
+    return buf.value.decode()
+
+
+# ---------------------------------------------------------------------------- torch tensors
+def _torch():
+    import torch
+
+    return torch
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream, device):
+    torch = _torch()
+    if stream is None:
+        return torch.cuda.current_stream(device).cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _vec(t, dtype, length, name, device):
+    if t is None:
+        return None
+    if t.dtype != dtype or t.device != device or t.dim() != 1 or t.shape[0] != length or t.stride(0) != 1:
+        raise ValueError(f"{name}: expected a contiguous {dtype} vector of length {length} on {device}")
+    return t
+
+
+def dense(X, y, v=None, alpha: float = 1.0, beta: float = 0.0, z=None, out=None, stream=None):
+    """out = alpha * X^T (v * (X y)) + beta * z for a row-major CUDA tensor X (m, n), X.stride(1) == 1.
+
+    ``v=None`` means v = 1; ``z=None`` (or beta = 0) drops the beta z term. A column slice of a
+    wider matrix is accepted: its row stride is passed as the leading dimension.
+    """
+    torch = _torch()
+    if X.dim() != 2 or (X.shape[0] > 1 and X.shape[1] > 1 and X.stride(1) != 1) or not X.is_cuda:
+        raise ValueError("X: expected a 2-D CUDA tensor with unit column stride")
+    m, n = X.shape
+    ld = X.stride(0) if m > 1 else max(n, 1)
+    dt, dev = X.dtype, X.device
+    y = _vec(y, dt, n, "y", dev)
+    v = _vec(v, dt, m, "v", dev)
+    z = _vec(z, dt, n, "z", dev)
+    if out is None:
+        out = torch.empty(n, dtype=dt, device=dev)
+    _vec(out, dt, n, "out", dev)
+    st = _stream(stream, dev)
+    if dt == torch.float32:
+        rc = fxtx_dense_f32(m, n, _ptr(X), ld, _ptr(y), _ptr(v), alpha, beta, _ptr(z), _ptr(out), st)
+    elif dt == torch.float64:
+        rc = fxtx_dense_f64(m, n, _ptr(X), ld, _ptr(y), _ptr(v), alpha, beta, _ptr(z), _ptr(out), st)
+    else:
+        raise TypeError(f"unsupported dtype {dt}")
+    _check(rc, "fxtx_dense")
+    return out
+
+
+def csr(row_ptr, col_idx, vals, y, n: int, v=None, alpha: float = 1.0, beta: float = 0.0, z=None, out=None,
+        stream=None):
+    """The same pattern for CSR X: int64 row_ptr (m + 1), int32 col_idx and vals (nnz), n columns."""
+    torch = _torch()
+    if row_ptr.dtype != torch.int64 or col_idx.dtype != torch.int32:
+        raise ValueError("row_ptr must be int64 and col_idx int32")
+    m = row_ptr.shape[0] - 1
+    nnz = vals.shape[0]
+    dt, dev = vals.dtype, vals.device
+    y = _vec(y, dt, n, "y", dev)
+    v = _vec(v, dt, m, "v", dev)
+    z = _vec(z, dt, n, "z", dev)
+    if out is None:
+        out = torch.empty(n, dtype=dt, device=dev)
+    _vec(out, dt, n, "out", dev)
+    st = _stream(stream, dev)
+    args = (m, n, nnz, _ptr(row_ptr), _ptr(col_idx), _ptr(vals), _ptr(y), _ptr(v), alpha, beta, _ptr(z), _ptr(out), st)
+    if dt == torch.float32:
+        rc = fxtx_csr_f32(*args)
+    elif dt == torch.float64:
+        rc = fxtx_csr_f64(*args)
+    else:
+        raise TypeError(f"unsupported dtype {dt}")
+    _check(rc, "fxtx_csr")
+    return out
+
+
+def csr_validate(row_ptr, col_idx, n: int, stream=None) -> bool:
+    """True if the CSR structure is well formed (synchronous device check)."""
+    m = row_ptr.shape[0] - 1
+    rc = fxtx_csr_validate(m, n, col_idx.shape[0], _ptr(row_ptr), _ptr(col_idx), _stream(stream, row_ptr.device))
+    if rc == FXTX_ERR_BAD_CSR:
+        return False
+    _check(rc, "fxtx_csr_validate")
+    return True
+
+
+def device_error(stream=None) -> int:
+    """Reads and clears the device-side error word (FXTX_OK or FXTX_ERR_TIMEOUT)."""
+    torch = _torch()
+    st = _stream(stream, torch.device("cuda", torch.cuda.current_device()))
+    return fxtx_device_error(st)

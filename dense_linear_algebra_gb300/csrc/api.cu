@@ -1,0 +1,272 @@
+// api.cu — the C ABI of libfusedxtx (declared in include/fxtx.h): argument
+// checks, the launch plan, transient workspace and the launches, all enqueued
+// on the caller's stream.
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "fxtx.h"
+#include "kernels.h"
+#include "plan.h"
+
+namespace fxtx {
+namespace {
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::once_flag g_dev_once[kMaxDevices];
+
+// Properties of the current device, queried once per device.
+fxtx_status_t current_device(const DeviceInfo** out) {
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) {
+    cudaGetLastError();
+    return FXTX_ERR_UNSUPPORTED;
+  }
+  std::call_once(g_dev_once[d], [d] {
+    DeviceInfo& di = g_dev[d];
+    di.device = d;
+    cudaDeviceGetAttribute(&di.sm_count, cudaDevAttrMultiProcessorCount, d);
+    cudaDeviceGetAttribute(&di.cc_major, cudaDevAttrComputeCapabilityMajor, d);
+    cudaDeviceGetAttribute(&di.cc_minor, cudaDevAttrComputeCapabilityMinor, d);
+    cudaDeviceGetAttribute(&di.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d);
+    cudaDeviceGetAttribute(&di.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, d);
+    cudaGetLastError();
+  });
+  const DeviceInfo& di = g_dev[d];
+  if (di.cc_major != 10 || di.cc_minor != 3 || di.sm_count <= 0) return FXTX_ERR_UNSUPPORTED;
+  *out = &di;
+  return FXTX_OK;
+}
+
+bool log_enabled() {
+  static const bool on = [] {
+    const char* s = getenv("FXTX_LOG");
+    return s && s[0] && s[0] != '0';
+  }();
+  return on;
+}
+
+// Test hook: FXTX_FAIL_ALLOC=1 makes every workspace allocation fail (host side).
+bool fail_alloc() {
+  const char* s = getenv("FXTX_FAIL_ALLOC");
+  return s && s[0] == '1';
+}
+
+fxtx_status_t alloc_ws(void** p, size_t bytes, cudaStream_t st) {
+  *p = nullptr;
+  if (bytes == 0) return FXTX_OK;
+  if (fail_alloc()) return FXTX_ERR_ALLOC;
+  if (cudaMallocAsync(p, bytes, st) != cudaSuccess) {
+    cudaGetLastError();
+    *p = nullptr;
+    return FXTX_ERR_ALLOC;
+  }
+  return FXTX_OK;
+}
+
+template <typename T>
+bool aligned16(const T* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+template <typename T>
+fxtx_status_t dense_impl(int64_t m, int64_t n, const T* X, int64_t ld, const T* y, const T* v, T alpha, T beta,
+                         const T* z, T* out, void* stream) {
+  if (m < 0 || n < 0) return FXTX_ERR_INVALID_ARG;
+  if (n == 0) return FXTX_OK;
+  if (ld < n || y == nullptr || out == nullptr) return FXTX_ERR_INVALID_ARG;
+  if (m > 0 && X == nullptr) return FXTX_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  fxtx_status_t s = current_device(&dev);
+  if (s != FXTX_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  const int elem = (int)sizeof(T);
+  const bool tma_ok = aligned16(X) && (ld * elem) % 16 == 0 && (n * elem) % 16 == 0;
+  const DensePlan plan = plan_dense(*dev, m, n, ld, elem, tma_ok);
+  if (log_enabled()) {
+    char buf[256];
+    describe(plan, buf, sizeof buf);
+    fprintf(stderr, "[fxtx] m=%lld n=%lld ld=%lld %s\n", (long long)m, (long long)n, (long long)ld, buf);
+  }
+
+  DenseArgs<T> a;
+  a.m = m; a.n = n; a.ld = ld;
+  a.X = X; a.y = y; a.v = v; a.z = z; a.out = out;
+  a.alpha = (double)alpha; a.beta = (double)beta;
+  a.use_z = (z != nullptr && beta != T(0));
+  a.tiles = plan.rows_per_tile > 0 ? (m + plan.rows_per_tile - 1) / plan.rows_per_tile : 0;
+
+  void* ws = nullptr;
+  s = alloc_ws(&ws, plan.ws_bytes, st);
+  if (s != FXTX_OK) return s;
+  if (ws) {
+    a.ws = static_cast<double*>(ws);
+    a.ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + plan.ws_bytes - 128);
+    if (cudaMemsetAsync(a.ticket, 0, sizeof(unsigned), st) != cudaSuccess) {
+      cudaGetLastError();
+      cudaFreeAsync(ws, st);
+      return FXTX_ERR_CUDA;
+    }
+  }
+  cudaError_t e = launch_dense<T>(plan, a, st);
+  if (ws) cudaFreeAsync(ws, st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FXTX_ERR_CUDA;
+  }
+  return FXTX_OK;
+}
+
+template <typename T>
+fxtx_status_t csr_impl(int64_t m, int64_t n, int64_t nnz, const int64_t* row_ptr, const int32_t* col_idx,
+                       const T* vals, const T* y, const T* v, T alpha, T beta, const T* z, T* out, void* stream) {
+  if (m < 0 || n < 0 || nnz < 0) return FXTX_ERR_INVALID_ARG;
+  if (n == 0) return FXTX_OK;
+  if (n > INT32_MAX || y == nullptr || out == nullptr) return FXTX_ERR_INVALID_ARG;
+  if (m > 0 && row_ptr == nullptr) return FXTX_ERR_INVALID_ARG;
+  if (nnz > 0 && (col_idx == nullptr || vals == nullptr)) return FXTX_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  fxtx_status_t s = current_device(&dev);
+  if (s != FXTX_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  const CsrPlan plan = plan_csr(*dev, m, n, nnz, (int)sizeof(T));
+  if (log_enabled()) {
+    char buf[256];
+    describe(plan, buf, sizeof buf);
+    fprintf(stderr, "[fxtx] m=%lld n=%lld nnz=%lld %s\n", (long long)m, (long long)n, (long long)nnz, buf);
+  }
+
+  CsrArgs<T> a;
+  a.m = m; a.n = n; a.nnz = nnz;
+  a.row_ptr = row_ptr; a.col_idx = col_idx; a.vals = vals;
+  a.y = y; a.v = v; a.z = z; a.out = out;
+  a.alpha = (double)alpha; a.beta = (double)beta;
+  a.use_z = (z != nullptr && beta != T(0));
+
+  void* ws = nullptr;
+  s = alloc_ws(&ws, plan.ws_bytes, st);
+  if (s != FXTX_OK) return s;
+  char* w = static_cast<char*>(ws);
+  const size_t part_bytes = ((size_t)(plan.ctas + 1) * 8 + 127) / 128 * 128;
+  a.part = reinterpret_cast<int64_t*>(w);
+  a.queue = reinterpret_cast<int64_t*>(w + part_bytes);
+  a.counters = reinterpret_cast<unsigned long long*>(w + plan.ws_bytes - 128);
+  cudaError_t e = launch_csr<T>(plan, a, st);
+  cudaFreeAsync(ws, st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FXTX_ERR_CUDA;
+  }
+  return FXTX_OK;
+}
+
+}  // namespace
+}  // namespace fxtx
+
+using namespace fxtx;
+
+extern "C" {
+
+fxtx_status_t fxtx_dense_f32(int64_t m, int64_t n, const float* X, int64_t ld, const float* y, const float* v,
+                             float alpha, float beta, const float* z, float* out, void* stream) {
+  return dense_impl<float>(m, n, X, ld, y, v, alpha, beta, z, out, stream);
+}
+
+fxtx_status_t fxtx_dense_f64(int64_t m, int64_t n, const double* X, int64_t ld, const double* y, const double* v,
+                             double alpha, double beta, const double* z, double* out, void* stream) {
+  return dense_impl<double>(m, n, X, ld, y, v, alpha, beta, z, out, stream);
+}
+
+fxtx_status_t fxtx_csr_f32(int64_t m, int64_t n, int64_t nnz, const int64_t* row_ptr, const int32_t* col_idx,
+                           const float* vals, const float* y, const float* v, float alpha, float beta, const float* z,
+                           float* out, void* stream) {
+  return csr_impl<float>(m, n, nnz, row_ptr, col_idx, vals, y, v, alpha, beta, z, out, stream);
+}
+
+fxtx_status_t fxtx_csr_f64(int64_t m, int64_t n, int64_t nnz, const int64_t* row_ptr, const int32_t* col_idx,
+                           const double* vals, const double* y, const double* v, double alpha, double beta,
+                           const double* z, double* out, void* stream) {
+  return csr_impl<double>(m, n, nnz, row_ptr, col_idx, vals, y, v, alpha, beta, z, out, stream);
+}
+
+fxtx_status_t fxtx_csr_validate(int64_t m, int64_t n, int64_t nnz, const int64_t* row_ptr, const int32_t* col_idx,
+                                void* stream) {
+  if (m < 0 || n < 0 || nnz < 0) return FXTX_ERR_INVALID_ARG;
+  if (m == 0 && row_ptr == nullptr) return nnz == 0 ? FXTX_OK : FXTX_ERR_BAD_CSR;
+  if (row_ptr == nullptr || (nnz > 0 && col_idx == nullptr)) return FXTX_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  fxtx_status_t s = current_device(&dev);
+  if (s != FXTX_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  void* flag = nullptr;
+  s = alloc_ws(&flag, sizeof(int), st);
+  if (s != FXTX_OK) return s;
+  int host = 0;
+  cudaError_t e = cudaMemsetAsync(flag, 0, sizeof(int), st);
+  if (e == cudaSuccess) e = launch_csr_validate(m, n, nnz, row_ptr, col_idx, static_cast<int*>(flag), st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&host, flag, sizeof(int), cudaMemcpyDeviceToHost, st);
+  cudaFreeAsync(flag, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FXTX_ERR_CUDA;
+  }
+  return host ? FXTX_ERR_BAD_CSR : FXTX_OK;
+}
+
+fxtx_status_t fxtx_device_error(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return FXTX_ERR_CUDA;
+  }
+  const int a = take_dense_device_error();
+  const int b = take_csr_device_error();
+  if (a < 0 || b < 0) {
+    cudaGetLastError();
+    return FXTX_ERR_CUDA;
+  }
+  return (a || b) ? FXTX_ERR_TIMEOUT : FXTX_OK;
+}
+
+const char* fxtx_status_string(fxtx_status_t status) {
+  switch (status) {
+    case FXTX_OK: return "FXTX_OK";
+    case FXTX_ERR_INVALID_ARG: return "FXTX_ERR_INVALID_ARG: invalid argument";
+    case FXTX_ERR_UNSUPPORTED: return "FXTX_ERR_UNSUPPORTED: no compute capability 10.3 device is current";
+    case FXTX_ERR_CUDA: return "FXTX_ERR_CUDA: a CUDA call failed while enqueueing";
+    case FXTX_ERR_ALLOC: return "FXTX_ERR_ALLOC: workspace allocation failed";
+    case FXTX_ERR_BAD_CSR: return "FXTX_ERR_BAD_CSR: malformed CSR structure";
+    case FXTX_ERR_TIMEOUT: return "FXTX_ERR_TIMEOUT: a kernel abandoned a bounded wait";
+  }
+  return "FXTX: unknown status";
+}
+
+fxtx_status_t fxtx_plan_describe(int is_csr, int is_f64, int64_t m, int64_t n, int64_t nnz, int64_t ld, char* buf,
+                                 int64_t cap) {
+  if (buf == nullptr || cap <= 0 || m < 0 || n < 0 || nnz < 0) return FXTX_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  DeviceInfo fallback;
+  if (current_device(&dev) != FXTX_OK) {
+    // no GB300 current: describe the plan for a 152-SM device with 227 KB shared memory
+    fallback.sm_count = 152;
+    fallback.cc_major = 10;
+    fallback.cc_minor = 3;
+    fallback.smem_optin = 232448;
+    fallback.smem_per_sm = 233472;
+    dev = &fallback;
+  }
+  const int elem = is_f64 ? 8 : 4;
+  if (is_csr) {
+    describe(plan_csr(*dev, m, n, nnz, elem), buf, (size_t)cap);
+  } else {
+    const bool tma_ok = (ld * elem) % 16 == 0 && (n * elem) % 16 == 0;
+    describe(plan_dense(*dev, m, n, ld < n ? n : ld, elem, tma_ok), buf, (size_t)cap);
+  }
+  return FXTX_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,414 @@
+// dense.cu — fused kernels for dense row-major X:
+//     out = alpha * X^T (v .* (X y)) + beta * z
+// ("On optimizing machine learning workloads via kernel fusion", abstract: one
+// fused kernel that reads X once, with coarsening and hierarchical aggregation
+// of partial results).
+//
+// Narrow rows (at most 128 sixteen-byte chunks, i.e. n <= 512 fp32 / 256 fp64):
+//   every warp owns a contiguous range of row tiles and runs its own pipeline of
+//   bulk asynchronous copies (cp.async.bulk + mbarrier) into shared memory. A
+//   group of LPR lanes holds one row: each lane takes VPL chunks, forms its part
+//   of the dot x_i . y against y cached in registers, the group sums it with
+//   shuffles, scales it by v_i, and adds t_i x_ij into register accumulators for
+//   the same chunks — so each element of X is loaded from HBM once and used
+//   twice. Column partials are then reduced lane -> warp (shuffles) -> CTA
+//   (shared memory) -> grid (fixed-order sum by the last CTA to finish).
+// Wide rows: a CTA takes rows in groups of WIDE_R, forms their dots in one pass,
+//   reduces them through shared memory, and accumulates t_i x_ij into a
+//   per-CTA column accumulator (shared memory when it fits); the second touch of
+//   the row is served by L1/L2, not HBM. A second kernel sums the per-CTA
+//   accumulators in fixed order and applies the epilogue.
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace fxtx {
+
+int take_dense_device_error() { return take_device_error(); }
+
+__host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------------------------------------
+// Narrow kernel
+// ---------------------------------------------------------------------------------------------
+template <typename T, int LPR, int VPL, bool TMA>
+__global__ void __launch_bounds__(512) dense_narrow_kernel(const DenseArgs<T> a, const int R, const int S) {
+  using VT = typename Vec16<T>::type;
+  constexpr int NV = Vec16<T>::N;  // elements per 16-byte chunk
+  constexpr int G = 32 / LPR;      // rows per warp pass
+  constexpr int C = VPL * NV;      // columns per lane
+  extern __shared__ __align__(128) unsigned char smem[];
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int g = lane / LPR, q = lane % LPR;
+  const int64_t n = a.n;
+  const int64_t pitch = TMA ? n : a.ld;  // elements between consecutive rows of a tile
+  const size_t stage_bytes = TMA ? align_up((size_t)R * n * sizeof(T), 128) : 0;
+
+  // y restricted to this lane's columns: chunk c = q + LPR * k covers columns c*NV .. c*NV+NV-1
+  T yr[C];
+#pragma unroll
+  for (int k = 0; k < VPL; ++k)
+#pragma unroll
+    for (int e = 0; e < NV; ++e) {
+      const int64_t col = (int64_t)(q + LPR * k) * NV + e;
+      yr[k * NV + e] = col < n ? ldg(a.y + col) : T(0);
+    }
+
+  // this warp's tiles
+  const int64_t gw = (int64_t)blockIdx.x * nw + warp, W = (int64_t)gridDim.x * nw;
+  const int64_t t0 = a.tiles * gw / W, t1 = a.tiles * (gw + 1) / W, nt = t1 - t0;
+
+  unsigned char* stages = smem + (size_t)warp * S * stage_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)nw * S * stage_bytes) + warp * S;
+  uint64_t pol = 0;
+
+  auto issue = [&](int64_t tile, int s) {
+    const int64_t row0 = tile * R;
+    const int rows = (int)tmin<int64_t>(R, a.m - row0);
+    unsigned char* dst = stages + (size_t)s * stage_bytes;
+    const uint32_t row_bytes = (uint32_t)(n * sizeof(T));
+    if (a.ld == n) {  // the tile is one contiguous span
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bars[s], rows * row_bytes);
+        bulk_g2s(dst, a.X + row0 * n, rows * row_bytes, &bars[s], pol);
+      }
+    } else {  // one copy per row, issued by as many lanes
+      if (lane == 0) mbar_arrive_expect_tx(&bars[s], rows * row_bytes);
+      __syncwarp();
+      for (int r = lane; r < rows; r += 32)
+        bulk_g2s(dst + (size_t)r * row_bytes, a.X + (row0 + r) * a.ld, row_bytes, &bars[s], pol);
+    }
+  };
+
+  auto load_v = [&](int64_t tile) -> T {
+    if (a.v == nullptr || tile >= t1) return T(0);
+    const int64_t r = tile * R + lane;
+    return (lane < R && r < a.m) ? ldg(a.v + r) : T(0);
+  };
+
+  if constexpr (TMA) {
+    pol = policy_evict_first();
+    if (lane == 0) {
+      for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+      fence_mbar_init();
+    }
+    __syncwarp();
+    for (int s = 0; s < S && s < nt; ++s) issue(t0 + s, s);
+  }
+
+  typename OuterAcc<T>::type acc[C];
+  T vnext = load_v(t0);
+  for (int64_t k = 0; k < nt; ++k) {
+    const int64_t tile = t0 + k, row0 = tile * R;
+    const int rows = (int)tmin<int64_t>(R, a.m - row0);
+    const T vcur = vnext;
+    if (k + 1 < nt) vnext = load_v(tile + 1);
+    const int s = (int)(k % S);
+    const T* tx;
+    if constexpr (TMA) {
+      const bool ok = mbar_wait_bounded(&bars[s], (uint32_t)((k / S) & 1));
+      if (__any_sync(FULL_MASK, !ok)) {
+        // give the copies still in flight a bounded chance to land, then stop
+        if (lane == 0)
+          for (int64_t j = k + 1; j < nt && j < k + S; ++j) mbar_wait_bounded(&bars[j % S], (uint32_t)((j / S) & 1));
+        break;
+      }
+      tx = reinterpret_cast<const T*>(stages + (size_t)s * stage_bytes);
+    } else {
+      tx = a.X + row0 * a.ld;
+    }
+
+    T tacc[C];
+#pragma unroll
+    for (int c = 0; c < C; ++c) tacc[c] = T(0);
+#pragma unroll 2
+    for (int r0 = 0; r0 < rows; r0 += G) {
+      const int r = r0 + g;
+      const bool valid = r < rows;
+      const T* rowp = tx + (int64_t)r * pitch;
+      T x[C];
+#pragma unroll
+      for (int k2 = 0; k2 < VPL; ++k2) {
+        const int64_t c0 = (int64_t)(q + LPR * k2) * NV;
+        if constexpr (TMA) {
+          if (valid && c0 < n) {
+            const VT vv = *reinterpret_cast<const VT*>(rowp + c0);
+            unpack<T>(vv, &x[k2 * NV]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < NV; ++e) x[k2 * NV + e] = T(0);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < NV; ++e) x[k2 * NV + e] = (valid && c0 + e < n) ? ldg(rowp + c0 + e) : T(0);
+        }
+      }
+      T d = T(0);
+#pragma unroll
+      for (int c = 0; c < C; ++c) d = fma(x[c], yr[c], d);
+      d = group_sum<LPR>(d);
+      const T vi = a.v ? __shfl_sync(FULL_MASK, vcur, r & 31) : T(1);
+      const T t = valid ? vi * d : T(0);
+#pragma unroll
+      for (int c = 0; c < C; ++c) tacc[c] = fma(t, x[c], tacc[c]);
+    }
+#pragma unroll
+    for (int c = 0; c < C; ++c) acc[c].add(tacc[c]);
+    if constexpr (TMA) {
+      __syncwarp();
+      if (k + S < nt) {
+        fence_proxy_async_smem();
+        issue(t0 + k + S, s);
+      }
+    }
+  }
+
+  // lane -> warp: lanes with the same q hold the same columns
+  double part[C];
+#pragma unroll
+  for (int c = 0; c < C; ++c) part[c] = acc[c].value();
+#pragma unroll
+  for (int o = LPR; o < 32; o <<= 1)
+#pragma unroll
+    for (int c = 0; c < C; ++c) part[c] += shfl_xor(part[c], o);
+
+  // warp -> CTA
+  __syncthreads();
+  double* red = reinterpret_cast<double*>(smem);  // [nw][n]
+  if (g == 0) {
+#pragma unroll
+    for (int k2 = 0; k2 < VPL; ++k2)
+#pragma unroll
+      for (int e = 0; e < NV; ++e) {
+        const int64_t col = (int64_t)(q + LPR * k2) * NV + e;
+        if (col < n) red[warp * n + col] = part[k2 * NV + e];
+      }
+  }
+  __syncthreads();
+  for (int64_t j = threadIdx.x; j < n; j += blockDim.x) {
+    double s = 0.0;
+    for (int w = 0; w < nw; ++w) s += red[w * n + j];
+    a.ws[blockIdx.x * n + j] = s;
+  }
+
+  // CTA -> grid: the last CTA to arrive sums every CTA's partial in a fixed order
+  __threadfence();
+  __syncthreads();
+  __shared__ unsigned s_last;
+  if (threadIdx.x == 0) s_last = (atomicAdd(a.ticket, 1u) == gridDim.x - 1) ? 1u : 0u;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int nc = gridDim.x;
+  const int cb = nc * warp / nw, ce = nc * (warp + 1) / nw;
+  for (int64_t j = lane; j < n; j += 32) {
+    double s = 0.0;
+    for (int c = cb; c < ce; ++c) s += __ldcg(a.ws + (int64_t)c * n + j);
+    red[warp * n + j] = s;
+  }
+  __syncthreads();
+  for (int64_t j = threadIdx.x; j < n; j += blockDim.x) {
+    double s = 0.0;
+    for (int w = 0; w < nw; ++w) s += red[w * n + j];
+    double o = a.alpha * s;
+    if (a.use_z) o += a.beta * (double)a.z[j];
+    a.out[j] = (T)o;
+  }
+  if (threadIdx.x == 0) *a.ticket = 0u;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Wide kernel
+// ---------------------------------------------------------------------------------------------
+constexpr int WIDE_R = 4;        // rows coarsened per step
+constexpr int WIDE_THREADS = 512;
+
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(WIDE_THREADS) dense_wide_kernel(const DenseArgs<T> a, const bool smem_acc) {
+  using VT = typename Vec16<T>::type;
+  constexpr int NV = Vec16<T>::N;
+  constexpr int NWARP = WIDE_THREADS / 32;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ double s_dot[WIDE_R][NWARP];
+  __shared__ double s_t[WIDE_R];
+
+  const int64_t n = a.n, ld = a.ld;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  double* acc = smem_acc ? reinterpret_cast<double*>(smem) : a.ws + (int64_t)blockIdx.x * n;
+  for (int64_t j = threadIdx.x; j < n; j += blockDim.x) acc[j] = 0.0;
+  __syncthreads();
+
+  const int64_t r_begin = a.m * blockIdx.x / gridDim.x, r_end = a.m * (blockIdx.x + 1) / gridDim.x;
+  const int64_t nvec = VEC ? n / NV : 0;  // whole chunks per row (VEC: rows start 16-byte aligned)
+
+  for (int64_t i0 = r_begin; i0 < r_end; i0 += WIDE_R) {
+    const int rows = (int)tmin<int64_t>(WIDE_R, r_end - i0);
+    // pass 1: WIDE_R dots at once
+    T d[WIDE_R];
+#pragma unroll
+    for (int r = 0; r < WIDE_R; ++r) d[r] = T(0);
+    for (int64_t c = threadIdx.x; c < nvec; c += blockDim.x) {
+      T yv[NV];
+      unpack<T>(*reinterpret_cast<const VT*>(a.y + c * NV), yv);
+#pragma unroll
+      for (int r = 0; r < WIDE_R; ++r) {
+        if (r < rows) {
+          T xv[NV];
+          unpack<T>(*reinterpret_cast<const VT*>(a.X + (i0 + r) * ld + c * NV), xv);
+#pragma unroll
+          for (int e = 0; e < NV; ++e) d[r] = fma(xv[e], yv[e], d[r]);
+        }
+      }
+    }
+    for (int64_t j = nvec * NV + threadIdx.x; j < n; j += blockDim.x) {
+      const T yj = a.y[j];
+#pragma unroll
+      for (int r = 0; r < WIDE_R; ++r)
+        if (r < rows) d[r] = fma(a.X[(i0 + r) * ld + j], yj, d[r]);
+    }
+#pragma unroll
+    for (int r = 0; r < WIDE_R; ++r) {
+      const T w = group_sum<32>(d[r]);
+      if (lane == 0) s_dot[r][warp] = (double)w;
+    }
+    __syncthreads();
+    if (threadIdx.x < WIDE_R) {
+      const int r = threadIdx.x;
+      double u = 0.0;
+      for (int w = 0; w < NWARP; ++w) u += s_dot[r][w];
+      const double vi = (r < rows && a.v) ? (double)a.v[i0 + r] : 1.0;
+      s_t[r] = r < rows ? (double)(T)(vi * (T)u) : 0.0;
+    }
+    __syncthreads();
+    T t[WIDE_R];
+#pragma unroll
+    for (int r = 0; r < WIDE_R; ++r) t[r] = (T)s_t[r];
+    // pass 2: the same rows again (served from L1/L2), scattered into the column accumulator
+    for (int64_t c = threadIdx.x; c < nvec; c += blockDim.x) {
+      T s[NV];
+#pragma unroll
+      for (int e = 0; e < NV; ++e) s[e] = T(0);
+#pragma unroll
+      for (int r = 0; r < WIDE_R; ++r) {
+        if (r < rows) {
+          T xv[NV];
+          unpack<T>(*reinterpret_cast<const VT*>(a.X + (i0 + r) * ld + c * NV), xv);
+#pragma unroll
+          for (int e = 0; e < NV; ++e) s[e] = fma(t[r], xv[e], s[e]);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < NV; ++e) acc[c * NV + e] += (double)s[e];
+    }
+    for (int64_t j = nvec * NV + threadIdx.x; j < n; j += blockDim.x) {
+      T s = T(0);
+#pragma unroll
+      for (int r = 0; r < WIDE_R; ++r)
+        if (r < rows) s = fma(t[r], a.X[(i0 + r) * ld + j], s);
+      acc[j] += (double)s;
+    }
+    __syncthreads();  // s_dot / s_t reuse
+  }
+  if (smem_acc)
+    for (int64_t j = threadIdx.x; j < n; j += blockDim.x) a.ws[(int64_t)blockIdx.x * n + j] = acc[j];
+}
+
+// Fixed-order sum of per-CTA column partials [nc][n], then out = alpha * w + beta * z.
+template <typename T>
+__global__ void __launch_bounds__(256) reduce_partials_kernel(const DenseArgs<T> a, const int nc) {
+  __shared__ double s[8][33];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t j = (int64_t)blockIdx.x * 32 + lane;
+  const int cb = nc * warp / 8, ce = nc * (warp + 1) / 8;
+  double acc = 0.0;
+  if (j < a.n)
+    for (int c = cb; c < ce; ++c) acc += __ldcg(a.ws + (int64_t)c * a.n + j);
+  s[warp][lane] = acc;
+  __syncthreads();
+  if (warp == 0 && j < a.n) {
+    double w = 0.0;
+    for (int k = 0; k < 8; ++k) w += s[k][lane];
+    double o = a.alpha * w;
+    if (a.use_z) o += a.beta * (double)a.z[j];
+    a.out[j] = (T)o;
+  }
+}
+
+// m == 0: out = beta z (or 0).
+template <typename T>
+__global__ void empty_rows_kernel(const DenseArgs<T> a) {
+  for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < a.n; j += (int64_t)gridDim.x * blockDim.x)
+    a.out[j] = a.use_z ? (T)(a.beta * (double)a.z[j]) : T(0);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Host launchers
+// ---------------------------------------------------------------------------------------------
+cudaError_t ensure_smem(const void* kernel, size_t bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+template <typename T, int LPR, int VPL>
+static cudaError_t launch_narrow(const DensePlan& p, const DenseArgs<T>& a, cudaStream_t st) {
+  const void* k = p.kind == DENSE_NARROW_TMA ? (const void*)dense_narrow_kernel<T, LPR, VPL, true>
+                                             : (const void*)dense_narrow_kernel<T, LPR, VPL, false>;
+  cudaError_t e = ensure_smem(k, p.smem);
+  if (e != cudaSuccess) return e;
+  if (p.kind == DENSE_NARROW_TMA)
+    dense_narrow_kernel<T, LPR, VPL, true><<<p.ctas, p.warps * 32, p.smem, st>>>(a, p.rows_per_tile, p.stages);
+  else
+    dense_narrow_kernel<T, LPR, VPL, false><<<p.ctas, p.warps * 32, p.smem, st>>>(a, p.rows_per_tile, 1);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_dense(const DensePlan& p, const DenseArgs<T>& a, cudaStream_t st) {
+  switch (p.kind) {
+    case DENSE_NOOP:
+      return cudaSuccess;
+    case DENSE_EMPTY_ROWS: {
+      const int blocks = (int)std::min<int64_t>((a.n + 255) / 256, 4096);
+      empty_rows_kernel<T><<<blocks, 256, 0, st>>>(a);
+      return cudaGetLastError();
+    }
+    case DENSE_NARROW_TMA:
+    case DENSE_NARROW_DIRECT: {
+      const int key = p.lpr * 8 + p.vpl;
+      switch (key) {
+        case 1 * 8 + 1: return launch_narrow<T, 1, 1>(p, a, st);
+        case 2 * 8 + 1: return launch_narrow<T, 2, 1>(p, a, st);
+        case 4 * 8 + 1: return launch_narrow<T, 4, 1>(p, a, st);
+        case 8 * 8 + 1: return launch_narrow<T, 8, 1>(p, a, st);
+        case 8 * 8 + 2: return launch_narrow<T, 8, 2>(p, a, st);
+        case 8 * 8 + 4: return launch_narrow<T, 8, 4>(p, a, st);
+        case 16 * 8 + 4: return launch_narrow<T, 16, 4>(p, a, st);
+        case 32 * 8 + 4: return launch_narrow<T, 32, 4>(p, a, st);
+        default: return cudaErrorInvalidConfiguration;
+      }
+    }
+    case DENSE_WIDE: {
+      const bool vec = (reinterpret_cast<uintptr_t>(a.X) % 16 == 0) && (reinterpret_cast<uintptr_t>(a.y) % 16 == 0) &&
+                       ((a.ld * (int64_t)sizeof(T)) % 16 == 0);
+      const void* k = vec ? (const void*)dense_wide_kernel<T, true> : (const void*)dense_wide_kernel<T, false>;
+      cudaError_t e = ensure_smem(k, p.smem);
+      if (e != cudaSuccess) return e;
+      if (vec)
+        dense_wide_kernel<T, true><<<p.ctas, WIDE_THREADS, p.smem, st>>>(a, p.smem_acc);
+      else
+        dense_wide_kernel<T, false><<<p.ctas, WIDE_THREADS, p.smem, st>>>(a, p.smem_acc);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+      reduce_partials_kernel<T><<<(unsigned)((a.n + 31) / 32), 256, 0, st>>>(a, p.ctas);
+      return cudaGetLastError();
+    }
+  }
+  return cudaErrorInvalidConfiguration;
+}
+
+template cudaError_t launch_dense<float>(const DensePlan&, const DenseArgs<float>&, cudaStream_t);
+template cudaError_t launch_dense<double>(const DensePlan&, const DenseArgs<double>&, cudaStream_t);
+
+}  // namespace fxtx

@@ -1,0 +1,63 @@
+// kernels.h — argument blocks and launchers of the fused kernels (host-visible).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "plan.h"
+
+namespace fxtx {
+
+// One dense call. alpha and beta are carried in double (exact for float).
+template <typename T>
+struct DenseArgs {
+  int64_t m = 0, n = 0, ld = 0;
+  const T* X = nullptr;
+  const T* y = nullptr;
+  const T* v = nullptr;  // NULL: v_i = 1
+  const T* z = nullptr;  // read only when use_z
+  T* out = nullptr;
+  double alpha = 1.0, beta = 0.0;
+  bool use_z = false;
+  double* ws = nullptr;         // [ctas][n] column partials of each CTA
+  unsigned* ticket = nullptr;   // arrival counter of the last-CTA reduction, zero at launch
+  int64_t tiles = 0;            // ceil(m / rows_per_tile)
+};
+
+template <typename T>
+cudaError_t launch_dense(const DensePlan& p, const DenseArgs<T>& a, cudaStream_t st);
+
+// One CSR call. alpha is folded into t_i; out is pre-set to beta z (or 0) by the
+// prologue and then receives atomic additions.
+template <typename T>
+struct CsrArgs {
+  int64_t m = 0, n = 0, nnz = 0;
+  const int64_t* row_ptr = nullptr;
+  const int32_t* col_idx = nullptr;
+  const T* vals = nullptr;
+  const T* y = nullptr;
+  const T* v = nullptr;
+  const T* z = nullptr;
+  T* out = nullptr;
+  double alpha = 1.0, beta = 0.0;
+  bool use_z = false;
+  int64_t* part = nullptr;       // [ctas + 1] row partition of the row-group kernel
+  int64_t* queue = nullptr;      // rows deferred to the long-row kernel
+  unsigned long long* counters = nullptr;  // [0] queue length, [1] long-row work counter
+};
+
+template <typename T>
+cudaError_t launch_csr(const CsrPlan& p, const CsrArgs<T>& a, cudaStream_t st);
+
+cudaError_t launch_csr_validate(int64_t m, int64_t n, int64_t nnz, const int64_t* row_ptr,
+                                const int32_t* col_idx, int* flag, cudaStream_t st);
+
+// Read and clear the device-side error word of each kernel file (synchronous;
+// -1 if the read itself failed).
+int take_dense_device_error();
+int take_csr_device_error();
+
+// Ensures a kernel may use `bytes` of dynamic shared memory on the current device.
+cudaError_t ensure_smem(const void* kernel, size_t bytes);
+
+}  // namespace fxtx

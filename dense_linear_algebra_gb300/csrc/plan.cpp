@@ -1,0 +1,144 @@
+// plan.cpp — the analytical launch-parameter model (see plan.h).
+#include "plan.h"
+
+#include <algorithm>
+#include <cstdio>
+
+namespace fxtx {
+
+namespace {
+
+constexpr int64_t kTileTarget = 8 * 1024;      // bytes a warp takes per pipeline step
+constexpr int64_t kSmemBudget = 200 * 1024;    // dynamic shared memory a CTA may claim
+constexpr int kCsrThreads = 512;
+
+int64_t pow2_ceil(int64_t x) {
+  int64_t p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+size_t align128(size_t x) { return (x + 127) / 128 * 128; }
+
+}  // namespace
+
+bool narrow_shape(int64_t chunks, int* lpr, int* vpl) {
+  if (chunks <= 0) return false;
+  if (chunks <= 8) {
+    *lpr = (int)pow2_ceil(chunks);
+    *vpl = 1;
+  } else if (chunks <= 16) {
+    *lpr = 8; *vpl = 2;
+  } else if (chunks <= 32) {
+    *lpr = 8; *vpl = 4;
+  } else if (chunks <= 64) {
+    *lpr = 16; *vpl = 4;
+  } else if (chunks <= 128) {
+    *lpr = 32; *vpl = 4;
+  } else {
+    return false;
+  }
+  return true;
+}
+
+DensePlan plan_dense(const DeviceInfo& dev, int64_t m, int64_t n, int64_t ld, int elem, bool tma_ok) {
+  DensePlan p;
+  if (n == 0) return p;  // nothing to write
+  if (m == 0) {
+    p.kind = DENSE_EMPTY_ROWS;
+    return p;
+  }
+  const int64_t budget = std::min<int64_t>(kSmemBudget, dev.smem_optin > 0 ? dev.smem_optin : 48 * 1024);
+  const int64_t chunks = cdiv(n * elem, 16);
+  int lpr = 0, vpl = 0;
+  if (narrow_shape(chunks, &lpr, &vpl)) {
+    p.lpr = lpr;
+    p.vpl = vpl;
+    const int G = 32 / lpr;
+    const int64_t row_bytes = n * elem;
+    if (tma_ok) {
+      // coarsening: the largest power-of-two row count (G..32) whose tile fits the target
+      int R = 32;
+      while (R > G && R * row_bytes > kTileTarget) R >>= 1;
+      const size_t stage = align128((size_t)(R * row_bytes));
+      int warps = stage <= 4096 ? 16 : 8;
+      int S = 0;
+      for (;;) {
+        S = (int)std::min<int64_t>(8, budget / (int64_t)(warps * (stage + 8)));
+        if (S >= 2 || warps <= 1) break;
+        warps >>= 1;
+      }
+      if (S < 1) S = 1;
+      p.kind = DENSE_NARROW_TMA;
+      p.rows_per_tile = R;
+      p.stages = S;
+      p.warps = warps;
+      p.smem = std::max<size_t>((size_t)warps * S * (stage + 8), (size_t)warps * n * sizeof(double));
+    } else {
+      p.kind = DENSE_NARROW_DIRECT;
+      p.rows_per_tile = 32;
+      p.stages = 1;
+      p.warps = 8;
+      p.smem = (size_t)p.warps * n * sizeof(double);
+    }
+    const int64_t tiles = cdiv(m, p.rows_per_tile);
+    const int per_sm = p.kind == DENSE_NARROW_DIRECT ? 4 : 1;
+    p.ctas = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)dev.sm_count * per_sm, cdiv(tiles, p.warps)));
+    p.ws_bytes = align128((size_t)p.ctas * n * sizeof(double)) + 128;
+    return p;
+  }
+  // wide rows
+  p.kind = DENSE_WIDE;
+  p.warps = 16;
+  p.rows_per_tile = 4;
+  p.ctas = (int)std::max<int64_t>(1, std::min<int64_t>(dev.sm_count, cdiv(m, 8)));
+  p.smem_acc = (int64_t)(n * sizeof(double)) <= budget;
+  p.smem = p.smem_acc ? (size_t)n * sizeof(double) : 0;
+  p.ws_bytes = align128((size_t)p.ctas * n * sizeof(double)) + 128;
+  return p;
+}
+
+CsrPlan plan_csr(const DeviceInfo& dev, int64_t m, int64_t n, int64_t nnz, int elem) {
+  CsrPlan p;
+  const double avg = m > 0 ? (double)nnz / (double)m : 0.0;
+  // short rows: the smallest power-of-two group whose registers (4 per lane) hold an average row
+  int64_t lpr = pow2_ceil((int64_t)(avg / 4.0 + 0.999));
+  p.lpr = (int)std::min<int64_t>(16, std::max<int64_t>(2, lpr));
+  p.group_cap = p.lpr * 4;
+  p.warp_cap = 32 * 8;
+  p.threads = kCsrThreads;
+  p.long_threads = kCsrThreads;
+  const int per_sm = 2;
+  const int64_t budget = std::min<int64_t>(kSmemBudget / per_sm, dev.smem_optin > 0 ? dev.smem_optin : 48 * 1024);
+  p.ctas = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)dev.sm_count * per_sm, cdiv(std::max<int64_t>(m, 1), 64)));
+  p.long_ctas = dev.sm_count * per_sm;
+  p.win_c0 = 0;
+  p.win_len = std::min<int64_t>(n, budget / elem);
+  p.smem = (size_t)p.win_len * elem;
+  p.long_smem = p.smem;
+  p.row_cost = 8;
+  p.queue_cap = std::min<int64_t>(m, nnz / (p.warp_cap + 1) + 1);
+  p.ws_bytes = align128((size_t)(p.ctas + 1) * 8) + align128((size_t)std::max<int64_t>(p.queue_cap, 1) * 8) + 128;
+  return p;
+}
+
+int describe(const DensePlan& p, char* buf, size_t cap) {
+  static const char* names[] = {"noop", "empty_rows", "narrow_tma", "narrow_direct", "wide"};
+  return snprintf(buf, cap,
+                  "dense kind=%s lanes_per_row=%d chunks_per_lane=%d rows_per_tile=%d stages=%d warps=%d ctas=%d "
+                  "smem=%zu smem_acc=%d ws=%zu",
+                  names[p.kind], p.lpr, p.vpl, p.rows_per_tile, p.stages, p.warps, p.ctas, p.smem, (int)p.smem_acc,
+                  p.ws_bytes);
+}
+
+int describe(const CsrPlan& p, char* buf, size_t cap) {
+  return snprintf(buf, cap,
+                  "csr lanes_per_row=%d group_cap=%d warp_cap=%d ctas=%d threads=%d long_ctas=%d window=[%lld,+%lld) "
+                  "smem=%zu queue_cap=%lld ws=%zu",
+                  p.lpr, p.group_cap, p.warp_cap, p.ctas, p.threads, p.long_ctas, (long long)p.win_c0,
+                  (long long)p.win_len, p.smem, (long long)p.queue_cap, p.ws_bytes);
+}
+
+}  // namespace fxtx

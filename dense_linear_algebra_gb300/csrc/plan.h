@@ -1,0 +1,66 @@
+// plan.h — the analytical launch-parameter model (host side).
+//
+// "On optimizing machine learning workloads via kernel fusion" (abstract) pairs
+// the fused kernel with a model that picks launch parameters from the input's
+// characteristics and the GPU's resources. This is that model rebuilt for
+// GB300: it reads m, n, ld, nnz, the element size, pointer alignment, the SM
+// count and the shared-memory limit, and returns the kernel variant together
+// with its coarsening (rows per tile, lanes per row, columns per lane), its
+// pipeline depth, grid size and reduction mode. It costs a few hundred
+// nanoseconds and touches no device memory.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+namespace fxtx {
+
+struct DeviceInfo {
+  int device = -1;
+  int sm_count = 0;
+  int cc_major = 0, cc_minor = 0;
+  int smem_optin = 0;  // max dynamic shared memory per block (bytes)
+  int smem_per_sm = 0;
+};
+
+enum DenseKind { DENSE_NOOP = 0, DENSE_EMPTY_ROWS, DENSE_NARROW_TMA, DENSE_NARROW_DIRECT, DENSE_WIDE };
+
+struct DensePlan {
+  DenseKind kind = DENSE_NOOP;
+  int lpr = 0;            // lanes cooperating on one row (narrow)
+  int vpl = 0;            // 16-byte chunks of a row held per lane (narrow)
+  int rows_per_tile = 0;  // coarsening: rows a warp takes per pipeline step
+  int stages = 0;         // pipeline depth per warp (narrow TMA)
+  int warps = 0;          // warps per CTA
+  int ctas = 0;           // grid size
+  size_t smem = 0;        // dynamic shared memory per CTA
+  bool smem_acc = false;  // wide: column accumulator kept in shared memory
+  size_t ws_bytes = 0;    // device workspace
+};
+
+// lanes-per-row / chunks-per-lane table of the narrow kernel, keyed by the
+// number of 16-byte chunks in a row (1..128). Returns false when the row is
+// too long for the narrow kernel.
+bool narrow_shape(int64_t chunks, int* lpr, int* vpl);
+
+DensePlan plan_dense(const DeviceInfo& dev, int64_t m, int64_t n, int64_t ld, int elem, bool tma_ok);
+
+struct CsrPlan {
+  int lpr = 0;              // lanes per short row in the row-group kernel
+  int group_cap = 0;        // longest row a lane group keeps in registers (lpr * 4)
+  int warp_cap = 0;         // longest row a whole warp keeps in registers
+  int ctas = 0, threads = 0;       // row-group kernel
+  int long_ctas = 0, long_threads = 0;  // long-row kernel
+  int64_t win_c0 = 0, win_len = 0;  // columns accumulated in shared memory
+  size_t smem = 0, long_smem = 0;
+  int row_cost = 0;         // nnz-equivalent cost of one row, for the partition
+  size_t ws_bytes = 0;
+  int64_t queue_cap = 0;    // capacity of the long-row queue
+};
+
+CsrPlan plan_csr(const DeviceInfo& dev, int64_t m, int64_t n, int64_t nnz, int elem);
+
+int describe(const DensePlan& p, char* buf, size_t cap);
+int describe(const CsrPlan& p, char* buf, size_t cap);
+
+}  // namespace fxtx

@@ -1,0 +1,125 @@
+/*
+ * fxtx.h — libfusedxtx: the fused pattern
+ *
+ *     out = alpha * X^T (v .* (X y)) + beta * z
+ *
+ * and its instantiations, from "On optimizing machine learning workloads via
+ * kernel fusion", abstract (the generic pattern; a fused GPU kernel for sparse
+ * and dense X that reads X once; coarsening and hierarchical aggregation of
+ * partial results; an analytical model choosing launch parameters).
+ *
+ * Shapes: X is m x n, y, z and out have n entries, v has m entries and scales
+ * element-wise. The instantiations are selected by NULL arguments:
+ *   v == NULL                 v_i = 1            (X^T X y when alpha = 1, beta = 0)
+ *   z == NULL or beta == 0    no beta z term, and z is not read
+ *
+ * Memory: every pointer argument is a DEVICE pointer owned by the caller, and
+ * `stream` is a cudaStream_t (NULL for the legacy default stream). Calls are
+ * asynchronous with respect to the host, like cuBLAS: they return after the
+ * work is enqueued on `stream`, and errors of execution surface at the caller's
+ * next synchronisation (and through fxtx_device_error). The library allocates
+ * only transient workspace, with cudaMallocAsync on `stream` and freed with
+ * cudaFreeAsync on the same stream; it keeps no global cache, so concurrent
+ * calls on different streams are safe.
+ *
+ * Aliasing: out may equal z (in place). Any other overlap of out with an input
+ * is undefined.
+ *
+ * Arithmetic: fp32 entry points compute in fp32 with compensated accumulation of
+ * column partials and an fp64 final reduction; fp64 entry points compute in
+ * fp64. The result matches the exact value within
+ *     |out_j - exact_j| <= c * S_j,  S_j = |alpha| sum_i |t_i| |X_ij| + |beta z_j|,
+ * t_i = v_i (x_i . y), with c = 2e-5 (fp32) or 1e-12 (fp64).
+ */
+#ifndef FXTX_H
+#define FXTX_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FXTX_OK = 0,
+  FXTX_ERR_INVALID_ARG = 1, /* a size is negative, ld < n, or a required pointer is NULL */
+  FXTX_ERR_UNSUPPORTED = 2, /* no CUDA device of compute capability 10.3 is current */
+  FXTX_ERR_CUDA = 3,        /* a CUDA runtime call failed while enqueueing (launch, allocation) */
+  FXTX_ERR_ALLOC = 4,       /* workspace allocation failed */
+  FXTX_ERR_BAD_CSR = 5,     /* fxtx_csr_validate found a malformed structure */
+  FXTX_ERR_TIMEOUT = 6      /* a kernel gave up a bounded wait (reported by fxtx_device_error) */
+} fxtx_status_t;
+
+/*
+ * Dense X, row-major: entry (i, j) at X[i * ld + j], ld >= max(1, n).
+ *
+ * m, n >= 0. X may be NULL only when m == 0 or n == 0; y and out must be non-NULL
+ * when n > 0. When m == 0, out = beta * z (or 0). When n == 0 the call does
+ * nothing and returns FXTX_OK.
+ *
+ * Any alignment and any ld are accepted. When X is 16-byte aligned and
+ * ld * sizeof(T) and n * sizeof(T) are multiples of 16, X is staged through
+ * shared memory by bulk asynchronous copies; otherwise a direct-load variant
+ * runs. The result is the same within the bound above.
+ *
+ * The column reduction of the dense kernels is deterministic: repeated calls
+ * with the same arguments give bitwise-identical out.
+ */
+fxtx_status_t fxtx_dense_f32(int64_t m, int64_t n, const float* X, int64_t ld, const float* y,
+                             const float* v, float alpha, float beta, const float* z, float* out,
+                             void* stream);
+fxtx_status_t fxtx_dense_f64(int64_t m, int64_t n, const double* X, int64_t ld, const double* y,
+                             const double* v, double alpha, double beta, const double* z, double* out,
+                             void* stream);
+
+/*
+ * CSR X: row_ptr (int64, m + 1 entries), col_idx (int32, nnz entries), vals
+ * (nnz entries). The structure must satisfy row_ptr[0] = 0, row_ptr
+ * non-decreasing, row_ptr[m] = nnz and 0 <= col_idx[k] < n; it is NOT checked
+ * on this path (see fxtx_csr_validate). Column order inside a row is free and
+ * repeated (i, j) entries add. row_ptr, col_idx and vals may be NULL only when
+ * m == 0 (row_ptr) or nnz == 0 (col_idx, vals).
+ *
+ * The scatter into out uses atomic additions, so the order of the column sums,
+ * and with it the last bits of out, may differ between calls.
+ */
+fxtx_status_t fxtx_csr_f32(int64_t m, int64_t n, int64_t nnz, const int64_t* row_ptr,
+                           const int32_t* col_idx, const float* vals, const float* y, const float* v,
+                           float alpha, float beta, const float* z, float* out, void* stream);
+fxtx_status_t fxtx_csr_f64(int64_t m, int64_t n, int64_t nnz, const int64_t* row_ptr,
+                           const int32_t* col_idx, const double* vals, const double* y,
+                           const double* v, double alpha, double beta, const double* z, double* out,
+                           void* stream);
+
+/*
+ * Checks a CSR structure on the device (row_ptr[0] == 0, non-decreasing,
+ * row_ptr[m] == nnz, 0 <= col_idx < n). Synchronous: it waits for `stream`.
+ * Returns FXTX_OK or FXTX_ERR_BAD_CSR (or an argument/CUDA error).
+ */
+fxtx_status_t fxtx_csr_validate(int64_t m, int64_t n, int64_t nnz, const int64_t* row_ptr,
+                                const int32_t* col_idx, void* stream);
+
+/*
+ * Reads and clears the device-side error word of the current device: FXTX_OK,
+ * or FXTX_ERR_TIMEOUT when a kernel abandoned a bounded wait since the last
+ * read (its output is then invalid). Synchronous on `stream`.
+ */
+fxtx_status_t fxtx_device_error(void* stream);
+
+/* A static string naming a status code. */
+const char* fxtx_status_string(fxtx_status_t status);
+
+/*
+ * The launch plan the analytical model picks for a dense or CSR call, for
+ * logging and tests. Host only; nothing is launched. For CSR, row_ptr is not
+ * read (the plan uses m, n and nnz only). Writes a NUL-terminated description
+ * of at most `cap` bytes into `buf` and returns FXTX_OK.
+ */
+fxtx_status_t fxtx_plan_describe(int is_csr, int is_f64, int64_t m, int64_t n, int64_t nnz,
+                                  int64_t ld, char* buf, int64_t cap);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FXTX_H */
