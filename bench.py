@@ -37,19 +37,26 @@ import numpy as np  # noqa: E402
 METRIC = "fused aX^T(v.*Xy)+bz: effective GB/s and % of GB300 HBM peak"
 FALLBACK_HBM_GBS = 6800.0
 
+def _m(kw, m):
+    return dict(kw, m=m) if m else kw
+
+
 WORKLOADS = {
-    "dense_small": ("dense f64 1000 x 64, U[-1,1], alpha=1.5, beta=0.5", lambda g: g.dense_small()),
+    "dense_small": ("dense f64 1000 x 64, U[-1,1], alpha=1.5, beta=0.5",
+                    lambda g, m=None: g.dense_small(**_m({}, m))),
     "dense_tall_a": ("dense f32 16,000,000 x 32, N(0,1) X/y, v U[0.1,2], alpha=1, beta=0, no z",
-                     lambda g: g.dense_tall(variant="a")),
+                     lambda g, m=None: g.dense_tall(**_m({"variant": "a"}, m))),
     "dense_tall_b": ("dense f32 16,000,000 x 32, N(0,1) X/y/z, v U[0.1,2], alpha=2, beta=-1",
-                     lambda g: g.dense_tall(variant="b")),
+                     lambda g, m=None: g.dense_tall(**_m({"variant": "b"}, m))),
     "dense_tall_c": ("dense f32 16,000,000 x 32, N(0,1) X/y, v=1 (X^T X y), alpha=1, beta=0",
-                     lambda g: g.dense_tall(variant="c")),
-    "dense_wide": ("dense f64 20,000 x 20,000, U[-1,1], alpha=0.7, beta=0.3", lambda g: g.dense_wide()),
+                     lambda g, m=None: g.dense_tall(**_m({"variant": "c"}, m))),
+    "dense_wide": ("dense f64 20,000 x 20,000, U[-1,1], alpha=0.7, beta=0.3",
+                   lambda g, m=None: g.dense_wide(**_m({}, m))),
     "csr_uniform": ("CSR f64 4,000,000 x 10,000, Poisson(50) uniform distinct columns, U[-1,1], alpha=beta=1",
-                    lambda g: g.csr_uniform()),
+                    lambda g, m=None: g.csr_uniform(**_m({}, m))),
     "csr_powerlaw": ("CSR f32 2,000,000 x 1,000,000, Zipf(1.5) row lengths (mean 100, cap 50,000), Zipf(1.1) "
-                     "columns, N(0,1) vals/y, v U[0,1], alpha=1, beta=0", lambda g: g.csr_powerlaw()),
+                     "columns, N(0,1) vals/y, v U[0,1], alpha=1, beta=0",
+                     lambda g, m=None: g.csr_powerlaw(**_m({}, m))),
 }
 PROFILED_KERNEL = {"dense": "dense_narrow_kernel", "dense_wide": "dense_wide_kernel", "csr": "csr_rows_kernel"}
 
@@ -82,7 +89,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -93,6 +100,11 @@ class ClockSampler:
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
+
+    def wait_first(self, timeout: float):
+        t0 = time.time()
+        while self.proc and not self.lines and time.time() - t0 < timeout:
+            time.sleep(0.02)
 
     def __exit__(self, *exc):
         if self.proc:
@@ -208,6 +220,97 @@ def dtype_name(p):
     return "f32" if np.dtype(p.dtype) == np.float32 else "f64"
 
 
+def time_e2e(args, host, d, call, out, out_host, stream, ideal):
+    """End to end: H2D of the step's inputs from pinned memory, the call, D2H of out."""
+    import torch
+
+    e_steps = max(3, min(args.steps, 10))
+    for _ in range(2):
+        for k, t in host.items():
+            if t is not None:
+                d[k].copy_(t, non_blocking=True)
+        call()
+        out_host.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        for k, t in host.items():
+            if t is not None:
+                d[k].copy_(t, non_blocking=True)
+        call()
+        out_host.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e_steps
+    e2e_val = ideal / (e2e_ms * 1e-3) / 1e9
+
+    return e2e_ms, e2e_val
+
+
+def time_unfused(args, p, d, X, out, dev, stream, ideal, ms_step):
+    """The unfused library sequence on the same GPU."""
+    import torch
+
+    # the unfused library sequence on the same GPU (dense: cuBLAS gemv, scale, transposed gemv)
+    if p.kind == "dense":
+        try:
+            Xt = X
+            tz = d["z"] if (d["z"] is not None and p.beta != 0) else torch.zeros(p.n, dtype=out.dtype, device=dev)
+
+            def lib_seq():
+                u = torch.mv(Xt, d["y"])
+                t = u * d["v"] if d["v"] is not None else u
+                return torch.addmv(tz, Xt.t(), t, beta=p.beta, alpha=p.alpha)
+            for _ in range(3):
+                lib_seq()
+            torch.cuda.synchronize()
+            u0 = torch.cuda.Event(enable_timing=True)
+            u1 = torch.cuda.Event(enable_timing=True)
+            u0.record(stream)
+            for _ in range(args.steps):
+                lib_seq()
+            u1.record(stream)
+            torch.cuda.synchronize()
+            ums = u0.elapsed_time(u1) / args.steps
+            unfused = {"what": "torch.mv (cuBLAS gemv N), v scale, torch.addmv on X^T (cuBLAS gemv T)",
+                       "ms_per_step": round(ums, 4), "value": round(ideal / (ums * 1e-3) / 1e9, 2), "unit": "GB/s",
+                       "fused_speedup": round(ums / ms_step, 3)}
+        except Exception as e:  # report, do not fail the bench
+            unfused = {"error": str(e)[:200]}
+    else:
+        try:
+            # cuSPARSE takes one index type for both arrays: widen col_idx to int64 to match row_ptr
+            Xs = torch.sparse_csr_tensor(d["row_ptr"], d["col_idx"].to(torch.int64), d["vals"], size=(p.m, p.n))
+            XsT = Xs.t().to_sparse_csr()
+            tz = d["z"] if (d["z"] is not None and p.beta != 0) else torch.zeros(p.n, dtype=out.dtype, device=dev)
+
+            def lib_seq():
+                u = torch.mv(Xs, d["y"])
+                t = u * d["v"] if d["v"] is not None else u
+                return torch.addmv(tz, XsT, t, beta=p.beta, alpha=p.alpha)
+            for _ in range(3):
+                lib_seq()
+            torch.cuda.synchronize()
+            u0 = torch.cuda.Event(enable_timing=True)
+            u1 = torch.cuda.Event(enable_timing=True)
+            u0.record(stream)
+            for _ in range(args.steps):
+                lib_seq()
+            u1.record(stream)
+            torch.cuda.synchronize()
+            ums = u0.elapsed_time(u1) / args.steps
+            unfused = {"what": "torch CSR mv (cuSPARSE SpMV), v scale, addmv on a pre-transposed CSR copy of X",
+                       "ms_per_step": round(ums, 4), "value": round(ideal / (ums * 1e-3) / 1e9, 2), "unit": "GB/s",
+                       "fused_speedup": round(ums / ms_step, 3)}
+            del Xs, XsT
+        except Exception as e:
+            unfused = {"error": str(e)[:200]}
+
+    return unfused
+
+
 def run_fused(args, name, desc, p, rank, world, dist):
     import torch
 
@@ -242,18 +345,19 @@ def run_fused(args, name, desc, p, rank, world, dist):
         launches = 3
 
     ideal = p.ideal_bytes()
-    for _ in range(max(args.warmup, 3)):
-        call()
-    torch.cuda.synchronize()
-
-    # device-timed steps, inputs resident
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
     smi_index = vis.split(",")[dev.index] if vis else str(dev.index)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     with ClockSampler(smi_index) as clk:
+        clk.wait_first(3.0)
+        for _ in range(max(args.warmup, 3)):
+            call()
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        # device-timed steps, inputs resident
+        wall0 = time.time()
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
@@ -263,6 +367,13 @@ def run_fused(args, name, desc, p, rank, world, dist):
             b.record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
+        # the same step keeps running until the clock window spans a second
+        extra = 0
+        while time.time() - wall0 < 1.0:
+            for _ in range(20):
+                call()
+            extra += 20
+            torch.cuda.synchronize()
     if dist:
         dist.barrier()
     per = [a.elapsed_time(b) for a, b in ev]  # ms per call
@@ -275,85 +386,13 @@ def run_fused(args, name, desc, p, rank, world, dist):
     value = world * ideal / (ms_step * 1e-3) / 1e9
     kernel_ms = statistics.mean(per)
 
-    # end to end: H2D of the step's inputs, the call, D2H of out
     h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
     d2h = out_host.numel() * out_host.element_size()
-    e_steps = max(3, min(args.steps, 10))
-    for _ in range(2):
-        for k, t in host.items():
-            if t is not None:
-                d[k].copy_(t, non_blocking=True)
-        call()
-        out_host.copy_(out, non_blocking=True)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e_steps):
-        for k, t in host.items():
-            if t is not None:
-                d[k].copy_(t, non_blocking=True)
-        call()
-        out_host.copy_(out, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e_steps
-    e2e_val = ideal / (e2e_ms * 1e-3) / 1e9
-
-    # the unfused library sequence on the same GPU (dense: cuBLAS gemv, scale, transposed gemv)
+    e2e_ms = e2e_val = None
     unfused = None
-    if p.kind == "dense":
-        try:
-            Xt = X
-            tz = d["z"] if (d["z"] is not None and p.beta != 0) else torch.zeros(p.n, dtype=out.dtype, device=dev)
-
-            def lib_seq():
-                u = torch.mv(Xt, d["y"])
-                t = u * d["v"] if d["v"] is not None else u
-                return torch.addmv(tz, Xt.t(), t, beta=p.beta, alpha=p.alpha)
-            for _ in range(3):
-                lib_seq()
-            torch.cuda.synchronize()
-            u0 = torch.cuda.Event(enable_timing=True)
-            u1 = torch.cuda.Event(enable_timing=True)
-            u0.record(stream)
-            for _ in range(args.steps):
-                lib_seq()
-            u1.record(stream)
-            torch.cuda.synchronize()
-            ums = u0.elapsed_time(u1) / args.steps
-            unfused = {"what": "torch.mv (cuBLAS gemv N), v scale, torch.addmv on X^T (cuBLAS gemv T)",
-                       "ms_per_step": round(ums, 4), "value": round(ideal / (ums * 1e-3) / 1e9, 2), "unit": "GB/s",
-                       "fused_speedup": round(ums / ms_step, 3)}
-        except Exception as e:  # report, do not fail the bench
-            unfused = {"error": str(e)[:200]}
-    else:
-        try:
-            Xs = torch.sparse_csr_tensor(d["row_ptr"], d["col_idx"], d["vals"], size=(p.m, p.n))
-            XsT = Xs.t().to_sparse_csr()
-            tz = d["z"] if (d["z"] is not None and p.beta != 0) else torch.zeros(p.n, dtype=out.dtype, device=dev)
-
-            def lib_seq():
-                u = torch.mv(Xs, d["y"])
-                t = u * d["v"] if d["v"] is not None else u
-                return torch.addmv(tz, XsT, t, beta=p.beta, alpha=p.alpha)
-            for _ in range(3):
-                lib_seq()
-            torch.cuda.synchronize()
-            u0 = torch.cuda.Event(enable_timing=True)
-            u1 = torch.cuda.Event(enable_timing=True)
-            u0.record(stream)
-            for _ in range(args.steps):
-                lib_seq()
-            u1.record(stream)
-            torch.cuda.synchronize()
-            ums = u0.elapsed_time(u1) / args.steps
-            unfused = {"what": "torch CSR mv (cuSPARSE SpMV), v scale, addmv on a pre-transposed CSR copy of X",
-                       "ms_per_step": round(ums, 4), "value": round(ideal / (ums * 1e-3) / 1e9, 2), "unit": "GB/s",
-                       "fused_speedup": round(ums / ms_step, 3)}
-            del Xs, XsT
-        except Exception as e:
-            unfused = {"error": str(e)[:200]}
+    if not args.no_extras:
+        e2e_ms, e2e_val = time_e2e(args, host, d, call, out, out_host, stream, ideal)
+        unfused = time_unfused(args, p, d, X if p.kind == "dense" else None, out, dev, stream, ideal, ms_step)
 
     peak, peak_kind, _ = measured_peaks()
     key = f"{PROFILED_KERNEL['dense_wide' if (p.kind == 'dense' and launches == 2) else p.kind]} {name}"
@@ -370,9 +409,9 @@ def run_fused(args, name, desc, p, rank, world, dist):
         "us_per_call": round(kernel_ms * 1e3, 2),
         "hbm_pct_of_peak": round(100 * value / world / peak, 2),
         "hbm_pct_of_nominal_7900": round(100 * value / world / 7900.0, 2),
-        "clocks": clk.summary(),
-        "e2e": {"value": round(e2e_val, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_ms, 4)},
+        "clocks": dict(clk.summary(), window=f"{args.steps} timed steps + {extra} identical steps (>= 1 s)"),
+        "e2e": None if e2e_val is None else {"value": round(e2e_val, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                                             "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
         "gpu_launches": launches * args.steps,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -394,6 +433,8 @@ def main():
     ap.add_argument("--workload", default="dense_tall_b", choices=sorted(WORKLOADS))
     ap.add_argument("--all", action="store_true", help="one line per workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rows", type=int, default=0, help="override the row count (same recipe), for profiling")
+    ap.add_argument("--no-extras", action="store_true", help="skip the e2e and unfused-library legs")
     args = ap.parse_args()
 
     import inputgen
@@ -406,7 +447,7 @@ def main():
             return
         for name in names:
             desc, mk = WORKLOADS[name]
-            print(json.dumps(run_reference(args, name, desc, mk(inputgen))), flush=True)
+            print(json.dumps(run_reference(args, name, desc, mk(inputgen, args.rows or None))), flush=True)
         return
 
     import torch
@@ -423,7 +464,9 @@ def main():
 
     for name in names:
         desc, mk = WORKLOADS[name]
-        p = mk(inputgen)
+        p = mk(inputgen, args.rows or None)
+        if args.rows:
+            desc = f"{desc} [rows overridden: {p.m}]"
         rec = run_fused(args, name, desc, p, rank, world, dist)
         if rank == 0 and world == 1 and not args.no_cpu_baseline:
             t, reps = cpu_oracle_time(p, budget_s=10.0, min_reps=1, max_reps=3)

@@ -141,6 +141,52 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
   e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
 }
 
+// Dot-product accumulator. The plain form is one fused multiply-add per term.
+// The compensated form (COMP, fp32 only) follows Ogita, Rump and Oishi,
+// "Accurate sum and dot product" (SIAM J. Sci. Comput. 2005), algorithm Dot2:
+// each product is split exactly into p + e (TwoProduct via FMA), p is added
+// with TwoSum, and the two error terms are collected in c. The result is as
+// accurate as if computed in twice the working precision and then rounded,
+// which keeps long fp32 dots with heavy cancellation inside the fp32 bound.
+template <typename T, bool COMP>
+struct DotAcc {
+  T s = T(0);
+  __device__ __forceinline__ void add(T a, T b) { s = fma(a, b, s); }
+  template <int W>
+  __device__ __forceinline__ void group_reduce() {
+#pragma unroll
+    for (int o = W / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  }
+  __device__ __forceinline__ T value() const { return s; }
+  __device__ __forceinline__ double value_f64() const { return (double)s; }
+};
+
+template <>
+struct DotAcc<float, true> {
+  float s = 0.f, c = 0.f;
+  __device__ __forceinline__ void add(float a, float b) {
+    const float p = __fmul_rn(a, b);
+    const float e = __fmaf_rn(a, b, -p);
+    float t, q;
+    two_sum(s, p, t, q);
+    s = t;
+    c = __fadd_rn(c, __fadd_rn(q, e));
+  }
+  template <int W>
+  __device__ __forceinline__ void group_reduce() {
+#pragma unroll
+    for (int o = W / 2; o > 0; o >>= 1) {
+      const float s2 = __shfl_xor_sync(0xffffffffu, s, o), c2 = __shfl_xor_sync(0xffffffffu, c, o);
+      float t, q;
+      two_sum(s, s2, t, q);
+      s = t;
+      c = __fadd_rn(__fadd_rn(c, c2), q);
+    }
+  }
+  __device__ __forceinline__ float value() const { return __fadd_rn(s, c); }
+  __device__ __forceinline__ double value_f64() const { return (double)s + (double)c; }
+};
+
 // Two-float accumulator: hi + lo carries about 48 bits. add() folds one float
 // into it with TwoSum, so the accumulated rounding error stays near 2^-44
 // relative to the sum of magnitudes however many values are folded in.

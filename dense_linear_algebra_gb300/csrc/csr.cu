@@ -147,16 +147,17 @@ __global__ void __launch_bounds__(512) csr_rows_kernel(const CsrArgs<T> a, const
       const int64_t s2 = __shfl_sync(FULL_MASK, st, src), e2 = __shfl_sync(FULL_MASK, en, src);
       T mv[KW];
       int32_t mc[KW];
-      T md = T(0);
+      DotAcc<T, sizeof(T) == 4> mdot;
 #pragma unroll
       for (int k = 0; k < KW; ++k) {
         const int64_t idx = s2 + lane + 32 * k;
         const bool ok = idx < e2;
         mv[k] = ok ? ldg(a.vals + idx) : T(0);
         mc[k] = ok ? ldg(a.col_idx + idx) : -1;
-        if (ok) md = fma(mv[k], ldg(a.y + mc[k]), md);
+        if (ok) mdot.add(mv[k], ldg(a.y + mc[k]));
       }
-      md = group_sum<32>(md);
+      mdot.template group_reduce<32>();
+      const T md = mdot.value();
       const T vi = a.v ? ldg(a.v + rr) : T(1);
       const T ts = alpha * (vi * md);
 #pragma unroll
@@ -198,16 +199,16 @@ __global__ void __launch_bounds__(512) csr_long_kernel(const CsrArgs<T> a, const
     if (r < 0) break;
     const int64_t st = a.row_ptr[r], en = a.row_ptr[r + 1];
     // pass 1: the dot
-    T d = T(0);
-    for (int64_t idx = st + threadIdx.x; idx < en; idx += blockDim.x) d = fma(ldg(a.vals + idx), ldg(a.y + ldg(a.col_idx + idx)), d);
-    d = group_sum<32>(d);
-    if (lane == 0) s_red[warp] = (double)d;
+    DotAcc<T, sizeof(T) == 4> d;
+    for (int64_t idx = st + threadIdx.x; idx < en; idx += blockDim.x) d.add(ldg(a.vals + idx), ldg(a.y + ldg(a.col_idx + idx)));
+    d.template group_reduce<32>();
+    if (lane == 0) s_red[warp] = d.value_f64();
     __syncthreads();
     if (threadIdx.x == 0) {
-      T u = T(0);
-      for (int w = 0; w < nw; ++w) u += (T)s_red[w];
+      double u = 0.0;
+      for (int w = 0; w < nw; ++w) u += s_red[w];
       const T vi = a.v ? a.v[r] : T(1);
-      s_t = alpha * (vi * u);
+      s_t = alpha * (vi * (T)u);
     }
     __syncthreads();
     const T ts = s_t;

@@ -38,6 +38,8 @@ __global__ void __launch_bounds__(512) dense_narrow_kernel(const DenseArgs<T> a,
   constexpr int NV = Vec16<T>::N;  // elements per 16-byte chunk
   constexpr int G = 32 / LPR;      // rows per warp pass
   constexpr int C = VPL * NV;      // columns per lane
+  // fp32 rows longer than 64 entries take the compensated dot (cancellation grows with length)
+  constexpr bool COMP = sizeof(T) == 4 && LPR * C > 64;
   extern __shared__ __align__(128) unsigned char smem[];
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -145,10 +147,11 @@ __global__ void __launch_bounds__(512) dense_narrow_kernel(const DenseArgs<T> a,
           for (int e = 0; e < NV; ++e) x[k2 * NV + e] = (valid && c0 + e < n) ? ldg(rowp + c0 + e) : T(0);
         }
       }
-      T d = T(0);
+      DotAcc<T, COMP> dacc;
 #pragma unroll
-      for (int c = 0; c < C; ++c) d = fma(x[c], yr[c], d);
-      d = group_sum<LPR>(d);
+      for (int c = 0; c < C; ++c) dacc.add(x[c], yr[c]);
+      dacc.template group_reduce<LPR>();
+      const T d = dacc.value();
       const T vi = a.v ? __shfl_sync(FULL_MASK, vcur, r & 31) : T(1);
       const T t = valid ? vi * d : T(0);
 #pragma unroll
@@ -246,9 +249,7 @@ __global__ void __launch_bounds__(WIDE_THREADS) dense_wide_kernel(const DenseArg
   for (int64_t i0 = r_begin; i0 < r_end; i0 += WIDE_R) {
     const int rows = (int)tmin<int64_t>(WIDE_R, r_end - i0);
     // pass 1: WIDE_R dots at once
-    T d[WIDE_R];
-#pragma unroll
-    for (int r = 0; r < WIDE_R; ++r) d[r] = T(0);
+    DotAcc<T, sizeof(T) == 4> d[WIDE_R];
     for (int64_t c = threadIdx.x; c < nvec; c += blockDim.x) {
       T yv[NV];
       unpack<T>(*reinterpret_cast<const VT*>(a.y + c * NV), yv);
@@ -258,7 +259,7 @@ __global__ void __launch_bounds__(WIDE_THREADS) dense_wide_kernel(const DenseArg
           T xv[NV];
           unpack<T>(*reinterpret_cast<const VT*>(a.X + (i0 + r) * ld + c * NV), xv);
 #pragma unroll
-          for (int e = 0; e < NV; ++e) d[r] = fma(xv[e], yv[e], d[r]);
+          for (int e = 0; e < NV; ++e) d[r].add(xv[e], yv[e]);
         }
       }
     }
@@ -266,12 +267,12 @@ __global__ void __launch_bounds__(WIDE_THREADS) dense_wide_kernel(const DenseArg
       const T yj = a.y[j];
 #pragma unroll
       for (int r = 0; r < WIDE_R; ++r)
-        if (r < rows) d[r] = fma(a.X[(i0 + r) * ld + j], yj, d[r]);
+        if (r < rows) d[r].add(a.X[(i0 + r) * ld + j], yj);
     }
 #pragma unroll
     for (int r = 0; r < WIDE_R; ++r) {
-      const T w = group_sum<32>(d[r]);
-      if (lane == 0) s_dot[r][warp] = (double)w;
+      d[r].template group_reduce<32>();
+      if (lane == 0) s_dot[r][warp] = d[r].value_f64();
     }
     __syncthreads();
     if (threadIdx.x < WIDE_R) {

@@ -146,16 +146,28 @@ def test_deterministic(dtype):
     assert torch.equal(a, b) and torch.equal(a, c)
 
 
-def test_dot_cancellation_f64():
-    """Rows whose dot cancels almost exactly: the bound uses |t_i|, so the dot must be accurate."""
-    m, n = 4000, 64
+@pytest.mark.parametrize("dtype,n,C", [(np.float64, 64, 100.0), (np.float64, 3000, 100.0),
+                                        (np.float32, 256, 30.0), (np.float32, 2000, 30.0)])
+def test_dot_cancellation(dtype, n, C):
+    """Rows nearly orthogonal to y: sum_j |x_ij y_j| / |x_i . y| is about C (median).
+
+    The bound scales with |t_i| = |v_i x_i . y|, not with sum_j |x_ij y_j|, so each dot
+    must stay accurate relative to its cancelled value. fp64 in working precision
+    meets it at this cancellation; fp32 needs the compensated dot for long rows.
+    (Cancellation by ~1e9 would defeat any dot computed in working precision.)
+    """
+    m = 2000
     rng = np.random.default_rng(5)
-    X = rng.uniform(-1, 1, (m, n))
+    X0 = rng.uniform(-1, 1, (m, n))
     y = rng.uniform(-1, 1, n)
-    # make every row nearly orthogonal to y, leaving a tiny residual dot
-    X -= np.outer(X @ y / (y @ y), y)
-    X += 1e-9 * rng.uniform(-1, 1, (m, n))
-    p = inputgen.Problem("cancel", "dense", np.float64, m, n, 1.0, 0.0, y=y, v=None, z=None, X=X, ld=n)
+    X0 -= np.outer(X0 @ y / (y @ y), y)  # every row orthogonal to y ...
+    r = rng.uniform(-1, 1, (m, n))
+    a = np.median(np.abs(X0) @ np.abs(y)) / C / np.median(np.abs(r @ y))
+    X = (X0 + a * r).astype(dtype)  # ... plus a residual that sets the dot
+    y = y.astype(dtype)
+    c = np.median(np.abs(X.astype(np.float64)) @ np.abs(y) / np.abs(X.astype(np.float64) @ y))
+    assert 0.5 * C < c < 2 * C, c
+    p = inputgen.Problem("cancel", "dense", dtype, m, n, 1.0, 0.0, y=y, v=None, z=None, X=X, ld=n)
     check(p)
 
 
