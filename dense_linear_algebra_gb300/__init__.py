@@ -7,7 +7,7 @@ CUDA kernels of ``libfusedxtx.so`` (sources in ``csrc/``, C ABI in
 fallback: if the library cannot be loaded, importing the binding fails.
 
 Raw C-ABI calls (pointers as ints, stream as a cudaStream_t int) carry the C names:
-``fxtx_dense_f32``, ``fxtx_dense_f64``, ``fxtx_csr_f32``, ``fxtx_csr_f64``,
+``fxtx_dense_f32``, ``fxtx_dense_f64``, ``fxtx_dense_f32_noalloc``, ``fxtx_csr_f32``, ``fxtx_csr_f64``,
 ``fxtx_csr_validate``, ``fxtx_device_error``, ``fxtx_status_string``,
 ``fxtx_plan_describe``. ``dense`` and ``csr`` take torch CUDA tensors.
 """
@@ -17,6 +17,7 @@ from ._lib import (  # noqa: F401
     FXTX_ERR_CUDA,
     FXTX_ERR_INVALID_ARG,
     FXTX_ERR_TIMEOUT,
+    FXTX_ERR_TOO_LARGE,
     FXTX_ERR_UNSUPPORTED,
     FXTX_OK,
     FxtxError,
@@ -28,6 +29,7 @@ from ._lib import (  # noqa: F401
     fxtx_csr_f64,
     fxtx_csr_validate,
     fxtx_dense_f32,
+    fxtx_dense_f32_noalloc,
     fxtx_dense_f64,
     fxtx_device_error,
     fxtx_plan_describe,

@@ -13,6 +13,7 @@ FXTX_ERR_CUDA = 3
 FXTX_ERR_ALLOC = 4
 FXTX_ERR_BAD_CSR = 5
 FXTX_ERR_TIMEOUT = 6
+FXTX_ERR_TOO_LARGE = 7
 
 
 def _load() -> ctypes.CDLL:
@@ -26,6 +27,7 @@ def _load() -> ctypes.CDLL:
     i32, i64, f32, f64, vp = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_double, ctypes.c_void_p
     lib.fxtx_dense_f32.argtypes = [i64, i64, vp, i64, vp, vp, f32, f32, vp, vp, vp]
     lib.fxtx_dense_f64.argtypes = [i64, i64, vp, i64, vp, vp, f64, f64, vp, vp, vp]
+    lib.fxtx_dense_f32_noalloc.argtypes = [i64, i64, vp, i64, vp, vp, f32, f32, vp, vp, vp]
     lib.fxtx_csr_f32.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, f32, f32, vp, vp, vp]
     lib.fxtx_csr_f64.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, f64, f64, vp, vp, vp]
     lib.fxtx_csr_validate.argtypes = [i64, i64, i64, vp, vp, vp]
@@ -33,7 +35,7 @@ def _load() -> ctypes.CDLL:
     lib.fxtx_status_string.argtypes = [i32]
     lib.fxtx_status_string.restype = ctypes.c_char_p
     lib.fxtx_plan_describe.argtypes = [i32, i32, i64, i64, i64, i64, ctypes.c_char_p, i64]
-    for name in ("fxtx_dense_f32", "fxtx_dense_f64", "fxtx_csr_f32", "fxtx_csr_f64", "fxtx_csr_validate",
+    for name in ("fxtx_dense_f32", "fxtx_dense_f64", "fxtx_dense_f32_noalloc", "fxtx_csr_f32", "fxtx_csr_f64", "fxtx_csr_validate",
                  "fxtx_device_error", "fxtx_plan_describe"):
         getattr(lib, name).restype = i32
     return lib
@@ -44,6 +46,7 @@ library_path = _build.LIB
 
 fxtx_dense_f32 = _lib.fxtx_dense_f32
 fxtx_dense_f64 = _lib.fxtx_dense_f64
+fxtx_dense_f32_noalloc = _lib.fxtx_dense_f32_noalloc
 fxtx_csr_f32 = _lib.fxtx_csr_f32
 fxtx_csr_f64 = _lib.fxtx_csr_f64
 fxtx_csr_validate = _lib.fxtx_csr_validate

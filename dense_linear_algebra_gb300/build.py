@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfusedxtx.so")
-SOURCES = ["api.cu", "dense.cu", "csr.cu", "plan.cpp"]
+SOURCES = ["api.cu", "dense.cu", "csr.cu", "plan.cpp", "noalloc.cu"]
 HEADERS = ["common.cuh", "kernels.h", "plan.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

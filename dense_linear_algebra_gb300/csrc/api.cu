@@ -241,6 +241,7 @@ const char* fxtx_status_string(fxtx_status_t status) {
     case FXTX_ERR_ALLOC: return "FXTX_ERR_ALLOC: workspace allocation failed";
     case FXTX_ERR_BAD_CSR: return "FXTX_ERR_BAD_CSR: malformed CSR structure";
     case FXTX_ERR_TIMEOUT: return "FXTX_ERR_TIMEOUT: a kernel abandoned a bounded wait";
+    case FXTX_ERR_TOO_LARGE: return "FXTX_ERR_TOO_LARGE: the problem exceeds the no-allocation scratch (n <= 512)";
   }
   return "FXTX: unknown status";
 }

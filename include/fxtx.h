@@ -47,7 +47,8 @@ typedef enum {
   FXTX_ERR_CUDA = 3,        /* a CUDA runtime call failed while enqueueing (launch, allocation) */
   FXTX_ERR_ALLOC = 4,       /* workspace allocation failed */
   FXTX_ERR_BAD_CSR = 5,     /* fxtx_csr_validate found a malformed structure */
-  FXTX_ERR_TIMEOUT = 6      /* a kernel gave up a bounded wait (reported by fxtx_device_error) */
+  FXTX_ERR_TIMEOUT = 6,     /* a kernel gave up a bounded wait (reported by fxtx_device_error) */
+  FXTX_ERR_TOO_LARGE = 7    /* the problem needs more scratch than fxtx_dense_f32_noalloc holds */
 } fxtx_status_t;
 
 /*
@@ -71,6 +72,35 @@ fxtx_status_t fxtx_dense_f32(int64_t m, int64_t n, const float* X, int64_t ld, c
 fxtx_status_t fxtx_dense_f64(int64_t m, int64_t n, const double* X, int64_t ld, const double* y,
                              const double* v, double alpha, double beta, const double* z, double* out,
                              void* stream);
+
+/*
+ * fxtx_dense_f32 without any device allocation at call time. (The paper has no
+ * counterpart: this entry point exists for callers that cannot allocate.)
+ *
+ * For callers that must not allocate device memory while they run: code whose
+ * device memory belongs to another allocator or runtime, real-time loops that
+ * allow no allocation after start-up, or paths that must not touch the stream-
+ * ordered memory pool. Arguments and results are those of fxtx_dense_f32.
+ *
+ * Scratch: one library-wide device array of FXTX_NOALLOC_SCRATCH_BYTES (1 MiB),
+ * which every GPU that loads the library holds until the process exits. The
+ * first call on a device (with that device current) looks up the array's address
+ * and caches it; make that first call before any stream capture. No call
+ * allocates or frees memory.
+ *
+ * Limits: rows of at most 512 fp32 columns (the narrow kernel); n > 512 returns
+ * FXTX_ERR_TOO_LARGE. The grid is capped so that the per-CTA partials fit the
+ * array.
+ *
+ * Concurrency: all calls on a device share the array, which keeps the last
+ * call's contents (the part that must start at zero is cleared on `stream`
+ * before each launch). Calls whose executions overlap on the GPU race on it and
+ * give wrong results: order them on one stream or with events.
+ */
+#define FXTX_NOALLOC_SCRATCH_BYTES (1u << 20)
+fxtx_status_t fxtx_dense_f32_noalloc(int64_t m, int64_t n, const float* X, int64_t ld, const float* y,
+                                     const float* v, float alpha, float beta, const float* z, float* out,
+                                     void* stream);
 
 /*
  * CSR X: row_ptr (int64, m + 1 entries), col_idx (int32, nnz entries), vals
