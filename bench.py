@@ -58,7 +58,20 @@ WORKLOADS = {
                      "columns, N(0,1) vals/y, v U[0,1], alpha=1, beta=0",
                      lambda g, m=None: g.csr_powerlaw(**_m({}, m))),
 }
-PROFILED_KERNEL = {"dense": "dense_narrow_kernel", "dense_wide": "dense_wide_kernel", "csr": "csr_rows_kernel"}
+
+
+def dominant_kernel(p) -> str:
+    """The kernel that carries the call, from the launch plan the library picks."""
+    import dense_linear_algebra_gb300 as fx
+
+    if p.kind == "csr":
+        # rows longer than 256 entries go to the long-row kernel; it dominates when they hold most entries
+        lens = np.diff(p.row_ptr)
+        return "csr_long_kernel" if lens[lens > 256].sum() > 0.5 * p.nnz else "csr_rows_kernel"
+    desc = fx.plan_describe("dense", dtype_name(p), p.m, p.n, 0, p.ld)
+    kind = dict(kv.split("=") for kv in desc.split()[1:] if "=" in kv)["kind"]
+    return {"tile_tma": "dense_tile_kernel", "narrow_tma": "dense_narrow_kernel", "narrow_direct": "dense_narrow_kernel",
+            "wide": "dense_wide_kernel"}.get(kind, kind)
 
 
 def measured_peaks():
@@ -395,7 +408,8 @@ def run_fused(args, name, desc, p, rank, world, dist):
         unfused = time_unfused(args, p, d, X if p.kind == "dense" else None, out, dev, stream, ideal, ms_step)
 
     peak, peak_kind, _ = measured_peaks()
-    key = f"{PROFILED_KERNEL['dense_wide' if (p.kind == 'dense' and launches == 2) else p.kind]} {name}"
+    kernel = dominant_kernel(p)
+    key = f"{kernel} {name}"
     traffic = profiled_traffic(key)
     achieved = ideal / (kernel_ms * 1e-3) / 1e9
     rec = {
@@ -416,7 +430,7 @@ def run_fused(args, name, desc, p, rank, world, dist):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_kind} HBM copy bandwidth",
-                     "kernel": PROFILED_KERNEL['dense_wide' if (p.kind == 'dense' and launches == 2) else p.kind]},
+                     "kernel": kernel},
         "unfused_library": unfused,
     }
     if p.kind == "csr":

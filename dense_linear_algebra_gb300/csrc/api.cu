@@ -84,8 +84,9 @@ fxtx_status_t dense_impl(int64_t m, int64_t n, const T* X, int64_t ld, const T* 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   const int elem = (int)sizeof(T);
-  const bool tma_ok = aligned16(X) && (ld * elem) % 16 == 0 && (n * elem) % 16 == 0;
-  const DensePlan plan = plan_dense(*dev, m, n, ld, elem, tma_ok);
+  const bool tile_ok = aligned16(X) && (ld * elem) % 16 == 0;
+  const bool tma_ok = tile_ok && (n * elem) % 16 == 0;
+  const DensePlan plan = plan_dense(*dev, m, n, ld, elem, tma_ok, tile_ok);
   if (log_enabled()) {
     char buf[256];
     describe(plan, buf, sizeof buf);
@@ -264,8 +265,9 @@ fxtx_status_t fxtx_plan_describe(int is_csr, int is_f64, int64_t m, int64_t n, i
   if (is_csr) {
     describe(plan_csr(*dev, m, n, nnz, elem), buf, (size_t)cap);
   } else {
-    const bool tma_ok = (ld * elem) % 16 == 0 && (n * elem) % 16 == 0;
-    describe(plan_dense(*dev, m, n, ld < n ? n : ld, elem, tma_ok), buf, (size_t)cap);
+    const int64_t l = ld < n ? n : ld;
+    const bool tile_ok = (l * elem) % 16 == 0;
+    describe(plan_dense(*dev, m, n, l, elem, tile_ok && (n * elem) % 16 == 0, tile_ok), buf, (size_t)cap);
   }
   return FXTX_OK;
 }

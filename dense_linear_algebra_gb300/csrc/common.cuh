@@ -60,6 +60,18 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// One 2-D tiled tensor copy global -> shared (box at element coordinates x, y
+// of the tensor map), completing its box bytes of transaction count on `bar`.
+// x * sizeof(element) must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
 // L2 policy for data read exactly once: evict it first.
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;

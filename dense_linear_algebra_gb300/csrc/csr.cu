@@ -4,19 +4,24 @@
 // fused kernel with its sparse specialisation, coarsening and hierarchical
 // aggregation of partial results).
 //
-// A row's entries are loaded once into registers, used for the dot with y
-// (gathered through the read-only cache), and reused for the scatter of
-// t_i * vals into the output — X is not read twice. Rows are binned on the fly
-// by length:
+// A row's entries are loaded once, used for the dot with y (gathered through
+// the read-only cache) and reused for the scatter of t_i * vals into the
+// output. Rows are binned on the fly by length:
 //   short  (<= lpr * 4)   a group of lpr lanes, entries in registers
 //   medium (<= 256)       the whole warp, entries in registers
-//   long  (> 256)         deferred to a queue and handled by a whole CTA in a
-//                         second kernel (two passes, the second served by L2)
-// Column partials are aggregated per CTA in a shared-memory window of columns
-// and flushed with one atomic per column at the end; columns outside the
-// window go straight to out with atomics. A prologue writes out = beta z and
-// splits the rows among CTAs so that each gets an equal share of
-// nnz + row_cost * rows; inside a CTA, warps take rows from a shared counter.
+//   long   (> 256)        deferred to a queue; a group of 8 warps takes each
+//                         one in the long-row kernel (pass 1 forms the dot,
+//                         pass 2 re-reads the row, from L2, for the scatter)
+// Each CTA (one per SM, 1024 threads) accumulates scatters into a shared-
+// memory window of columns and flushes it once with one atomic per column;
+// columns outside the window go straight to out with atomics. fp64 window
+// updates fold the product into the atomic itself (a CAS loop around one
+// fused multiply-add), so each entry costs two fp64 operations: the dot's
+// FMA and the scatter's.
+// The prologue writes out = beta z and splits rows among CTAs by equal shares
+// of nnz + row_cost * rows. Inside a CTA, warps take row batches in a static
+// interleave, which lets each warp prefetch its next batch's row bounds and
+// entries while it computes the current one.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -24,8 +29,22 @@ namespace fxtx {
 
 namespace {
 
-constexpr int KG = 4;  // entries per lane for short rows
-constexpr int KW = 8;  // entries per lane for medium rows
+constexpr int KG = 4;               // entries per lane for short rows
+constexpr int KW = 8;               // entries per lane for medium rows
+constexpr int LONG_UNROLL = 8;      // loads in flight per thread in the long-row kernel
+constexpr int LONG_GROUP = 256;     // threads that share one long row
+constexpr int CSR_THREADS = 1024;
+
+// out_j += a * b, with out_j in shared memory (fp64: CAS loop around one FMA).
+__device__ __forceinline__ void smem_fma_add(float* p, float a, float b) { atomicAdd(p, a * b); }
+__device__ __forceinline__ void smem_fma_add(double* p, double a, double b) {
+  unsigned long long* q = reinterpret_cast<unsigned long long*>(p);
+  unsigned long long old = *q, assumed;
+  do {
+    assumed = old;
+    old = atomicCAS(q, assumed, __double_as_longlong(fma(a, b, __longlong_as_double(assumed))));
+  } while (old != assumed);
+}
 
 template <typename T>
 struct Window {
@@ -33,12 +52,13 @@ struct Window {
   int64_t c0;
   int64_t len;
   T* out;
-  __device__ __forceinline__ void add(int32_t col, T x) const {
+  // out[col] += a * b, through the shared window when col falls inside it
+  __device__ __forceinline__ void add(int32_t col, T a, T b) const {
     const uint64_t off = (uint64_t)((int64_t)col - c0);
     if (off < (uint64_t)len)
-      atomicAdd(acc + off, x);
+      smem_fma_add(acc + off, a, b);
     else
-      atomicAdd(out + col, x);
+      atomicAdd(out + col, a * b);
   }
 };
 
@@ -53,6 +73,11 @@ __device__ __forceinline__ void window_flush(const T* acc, int64_t c0, int64_t l
     const T x = acc[j];
     if (x != T(0)) atomicAdd(out + c0 + j, x);
   }
+}
+
+// Named barrier over the `count` threads of one row group (ids 1..15; 0 is __syncthreads).
+__device__ __forceinline__ void group_barrier(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 }  // namespace
@@ -91,51 +116,68 @@ __global__ void csr_prologue_kernel(const CsrArgs<T> a, const int nparts, const 
 }
 
 template <typename T, int LPR>
-__global__ void __launch_bounds__(512) csr_rows_kernel(const CsrArgs<T> a, const int64_t win_c0, const int64_t win_len) {
-  constexpr int G = 32 / LPR;
+__global__ void __launch_bounds__(CSR_THREADS, 1)
+    csr_rows_kernel(const CsrArgs<T> a, const int64_t win_c0, const int64_t win_len) {
+  constexpr int G = 32 / LPR;  // rows per warp batch
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ unsigned long long s_next;
   T* wacc = reinterpret_cast<T*>(smem);
   const Window<T> win{wacc, win_c0, win_len, a.out};
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int g = lane / LPR, q = lane % LPR;
   const int64_t rb = a.part[blockIdx.x], re = a.part[blockIdx.x + 1];
   const T alpha = (T)a.alpha;
 
   window_zero(wacc, win_len);
-  if (threadIdx.x == 0) s_next = (unsigned long long)rb;
   __syncthreads();
 
-  for (;;) {
-    unsigned long long base = 0;
-    if (lane == 0) base = atomicAdd(&s_next, (unsigned long long)G);
-    base = __shfl_sync(FULL_MASK, base, 0);
-    if ((int64_t)base >= re) break;
-    const int64_t r = (int64_t)base + g;
-    const bool has = r < re;
-    const int64_t st = has ? a.row_ptr[r] : 0, en = has ? a.row_ptr[r + 1] : 0;
-    const int64_t len = en - st;
-
-    // short rows: one lane group, entries in registers
-    const bool small = has && len <= LPR * KG;
-    T val[KG];
-    int32_t col[KG];
-    T d = T(0);
+  // batch k of this warp covers rows rb + (warp + k * nw) * G + [0, G)
+  const int64_t step = (int64_t)nw * G;
+  int64_t r = rb + (int64_t)warp * G + g;
+  int64_t st = 0, en = 0;
+  if (r < re) { st = a.row_ptr[r]; en = a.row_ptr[r + 1]; }
+  // entries of the current batch (short rows), loaded one batch ahead
+  T val[KG];
+  int32_t col[KG];
+  auto load_short = [&](int64_t rr, int64_t s, int64_t e) {
+    const bool small = rr < re && e - s <= LPR * KG;
 #pragma unroll
     for (int k = 0; k < KG; ++k) {
-      const int64_t idx = st + q + LPR * k;
-      const bool ok = small && idx < en;
+      const int64_t idx = s + q + LPR * k;
+      const bool ok = small && idx < e;
       val[k] = ok ? ldg(a.vals + idx) : T(0);
       col[k] = ok ? ldg(a.col_idx + idx) : -1;
-      if (ok) d = fma(val[k], ldg(a.y + col[k]), d);
     }
+  };
+  load_short(r, st, en);
+
+  for (int64_t base = rb + (int64_t)warp * G; base < re; base += step) {
+    const bool has = r < re;
+    const int64_t len = en - st;
+    const bool small = has && len <= LPR * KG;
+    T cv[KG];
+    int32_t cc[KG];
+#pragma unroll
+    for (int k = 0; k < KG; ++k) { cv[k] = val[k]; cc[k] = col[k]; }
+    const int64_t cur_r = r, cur_st = st, cur_en = en;
+
+    // prefetch the next batch: row bounds, then its short-row entries
+    r += step;
+    st = en = 0;
+    if (r < re) { st = a.row_ptr[r]; en = a.row_ptr[r + 1]; }
+    load_short(r, st, en);
+
+    // short rows: one lane group, entries in registers
+    T d = T(0);
+#pragma unroll
+    for (int k = 0; k < KG; ++k)
+      if (cc[k] >= 0) d = fma(cv[k], ldg(a.y + cc[k]), d);
     d = group_sum<LPR>(d);
     if (small) {
-      const T vi = a.v ? ldg(a.v + r) : T(1);
+      const T vi = a.v ? ldg(a.v + cur_r) : T(1);
       const T ts = alpha * (vi * d);
 #pragma unroll
       for (int k = 0; k < KG; ++k)
-        if (col[k] >= 0) win.add(col[k], ts * val[k]);
+        if (cc[k] >= 0) win.add(cc[k], ts, cv[k]);
     }
 
     // medium rows: the whole warp, one row at a time
@@ -143,78 +185,115 @@ __global__ void __launch_bounds__(512) csr_rows_kernel(const CsrArgs<T> a, const
     while (mm) {
       const int src = __ffs(mm) - 1;
       mm &= mm - 1;
-      const int64_t rr = __shfl_sync(FULL_MASK, r, src);
-      const int64_t s2 = __shfl_sync(FULL_MASK, st, src), e2 = __shfl_sync(FULL_MASK, en, src);
+      const int64_t rr = __shfl_sync(FULL_MASK, cur_r, src);
+      const int64_t s2 = __shfl_sync(FULL_MASK, cur_st, src), e2 = __shfl_sync(FULL_MASK, cur_en, src);
       T mv[KW];
       int32_t mc[KW];
-      DotAcc<T, sizeof(T) == 4> mdot;
 #pragma unroll
       for (int k = 0; k < KW; ++k) {
         const int64_t idx = s2 + lane + 32 * k;
         const bool ok = idx < e2;
         mv[k] = ok ? ldg(a.vals + idx) : T(0);
         mc[k] = ok ? ldg(a.col_idx + idx) : -1;
-        if (ok) mdot.add(mv[k], ldg(a.y + mc[k]));
       }
-      mdot.template group_reduce<32>();
-      const T md = mdot.value();
-      const T vi = a.v ? ldg(a.v + rr) : T(1);
-      const T ts = alpha * (vi * md);
+      DotAcc<T, sizeof(T) == 4> mdot;
 #pragma unroll
       for (int k = 0; k < KW; ++k)
-        if (mc[k] >= 0) win.add(mc[k], ts * mv[k]);
+        if (mc[k] >= 0) mdot.add(mv[k], ldg(a.y + mc[k]));
+      mdot.template group_reduce<32>();
+      const T vi = a.v ? ldg(a.v + rr) : T(1);
+      const T ts = alpha * (vi * mdot.value());
+#pragma unroll
+      for (int k = 0; k < KW; ++k)
+        if (mc[k] >= 0) win.add(mc[k], ts, mv[k]);
     }
 
     // long rows: defer to the long-row kernel
     if (has && len > 32 * KW && q == 0) {
       const unsigned long long pos = atomicAdd(&a.counters[0], 1ull);
-      a.queue[pos] = r;
+      a.queue[pos] = cur_r;
     }
   }
   __syncthreads();
   window_flush(wacc, win_c0, win_len, a.out);
 }
 
+// Long rows: each group of LONG_GROUP threads takes queued rows one at a time.
 template <typename T>
-__global__ void __launch_bounds__(512) csr_long_kernel(const CsrArgs<T> a, const int64_t win_c0, const int64_t win_len) {
+__global__ void __launch_bounds__(CSR_THREADS, 1)
+    csr_long_kernel(const CsrArgs<T> a, const int64_t win_c0, const int64_t win_len) {
+  constexpr int GW = LONG_GROUP / 32;  // warps per group
+  constexpr int NG = CSR_THREADS / LONG_GROUP;
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ long long s_row;
-  __shared__ double s_red[16];
-  __shared__ T s_t;
+  __shared__ long long s_row[NG];
+  __shared__ double s_red[NG][GW];
+  __shared__ T s_t[NG];
   T* wacc = reinterpret_cast<T*>(smem);
   const Window<T> win{wacc, win_c0, win_len, a.out};
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int grp = threadIdx.x / LONG_GROUP, gt = threadIdx.x % LONG_GROUP, gw = gt >> 5;
+  const int bar = 1 + grp;
   const T alpha = (T)a.alpha;
 
   window_zero(wacc, win_len);
   __syncthreads();
   const unsigned long long count = a.counters[0];
   for (;;) {
-    if (threadIdx.x == 0) {
+    if (gt == 0) {
       const unsigned long long k = atomicAdd(&a.counters[1], 1ull);
-      s_row = k < count ? (long long)a.queue[k] : -1ll;
+      s_row[grp] = k < count ? (long long)a.queue[k] : -1ll;
     }
-    __syncthreads();
-    const int64_t r = s_row;
+    group_barrier(bar, LONG_GROUP);
+    const int64_t r = s_row[grp];
     if (r < 0) break;
     const int64_t st = a.row_ptr[r], en = a.row_ptr[r + 1];
-    // pass 1: the dot
+
+    // pass 1: the dot, LONG_UNROLL independent loads in flight per thread
     DotAcc<T, sizeof(T) == 4> d;
-    for (int64_t idx = st + threadIdx.x; idx < en; idx += blockDim.x) d.add(ldg(a.vals + idx), ldg(a.y + ldg(a.col_idx + idx)));
-    d.template group_reduce<32>();
-    if (lane == 0) s_red[warp] = d.value_f64();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      double u = 0.0;
-      for (int w = 0; w < nw; ++w) u += s_red[w];
-      const T vi = a.v ? a.v[r] : T(1);
-      s_t = alpha * (vi * (T)u);
+    for (int64_t b = st + gt; b < en; b += (int64_t)LONG_GROUP * LONG_UNROLL) {
+      T xv[LONG_UNROLL];
+      int32_t xc[LONG_UNROLL];
+#pragma unroll
+      for (int k = 0; k < LONG_UNROLL; ++k) {
+        const int64_t idx = b + (int64_t)k * LONG_GROUP;
+        const bool ok = idx < en;
+        xv[k] = ok ? ldg(a.vals + idx) : T(0);
+        xc[k] = ok ? ldg(a.col_idx + idx) : -1;
+      }
+      T yv[LONG_UNROLL];
+#pragma unroll
+      for (int k = 0; k < LONG_UNROLL; ++k) yv[k] = xc[k] >= 0 ? ldg(a.y + xc[k]) : T(0);
+#pragma unroll
+      for (int k = 0; k < LONG_UNROLL; ++k) d.add(xv[k], yv[k]);
     }
-    __syncthreads();
-    const T ts = s_t;
-    // pass 2: the scatter, re-reading the row from L2
-    for (int64_t idx = st + threadIdx.x; idx < en; idx += blockDim.x) win.add(ldg(a.col_idx + idx), ts * ldg(a.vals + idx));
-    __syncthreads();  // s_row / s_red / s_t reuse
+    d.template group_reduce<32>();
+    if (lane == 0) s_red[grp][gw] = d.value_f64();
+    group_barrier(bar, LONG_GROUP);
+    if (gt == 0) {
+      double u = 0.0;
+      for (int w = 0; w < GW; ++w) u += s_red[grp][w];
+      const T vi = a.v ? a.v[r] : T(1);
+      s_t[grp] = alpha * (vi * (T)u);
+    }
+    group_barrier(bar, LONG_GROUP);
+    const T ts = s_t[grp];
+
+    // pass 2: the scatter, re-reading the row (served by L2)
+    for (int64_t b = st + gt; b < en; b += (int64_t)LONG_GROUP * LONG_UNROLL) {
+      T xv[LONG_UNROLL];
+      int32_t xc[LONG_UNROLL];
+#pragma unroll
+      for (int k = 0; k < LONG_UNROLL; ++k) {
+        const int64_t idx = b + (int64_t)k * LONG_GROUP;
+        const bool ok = idx < en;
+        xv[k] = ok ? ldg(a.vals + idx) : T(0);
+        xc[k] = ok ? ldg(a.col_idx + idx) : -1;
+      }
+#pragma unroll
+      for (int k = 0; k < LONG_UNROLL; ++k)
+        if (xc[k] >= 0) win.add(xc[k], ts, xv[k]);
+    }
+    group_barrier(bar, LONG_GROUP);  // s_row / s_red / s_t reuse
   }
   __syncthreads();
   window_flush(wacc, win_c0, win_len, a.out);

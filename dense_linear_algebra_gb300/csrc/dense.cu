@@ -19,6 +19,9 @@
 //   the row is served by L1/L2, not HBM. A second kernel sums the per-CTA
 //   accumulators in fixed order and applies the epilogue.
 #include <algorithm>
+#include <mutex>
+
+#include <cuda.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -30,7 +33,48 @@ int take_dense_device_error() { return take_device_error(); }
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // ---------------------------------------------------------------------------------------------
-// Narrow kernel
+// Column partials: CTA -> grid
+// ---------------------------------------------------------------------------------------------
+// red[w][j] holds warp w's partial of column j. Sums them into the CTA partial,
+// stores it in ws[blockIdx.x], and lets the last CTA to take a ticket sum all
+// CTA partials in a fixed order and write out = alpha * w + beta * z.
+template <typename T>
+__device__ __forceinline__ void finish_from_red(const DenseArgs<T>& a, double* red, const int nw) {
+  __shared__ unsigned s_last;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t n = a.n;
+  __syncthreads();
+  for (int64_t j = threadIdx.x; j < n; j += blockDim.x) {
+    double s = 0.0;
+    for (int w = 0; w < nw; ++w) s += red[w * n + j];
+    a.ws[blockIdx.x * n + j] = s;
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = (atomicAdd(a.ticket, 1u) == gridDim.x - 1) ? 1u : 0u;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int nc = gridDim.x;
+  const int cb = nc * warp / nw, ce = nc * (warp + 1) / nw;
+  for (int64_t j = lane; j < n; j += 32) {
+    double s = 0.0;
+    for (int c = cb; c < ce; ++c) s += __ldcg(a.ws + (int64_t)c * n + j);
+    red[warp * n + j] = s;
+  }
+  __syncthreads();
+  for (int64_t j = threadIdx.x; j < n; j += blockDim.x) {
+    double s = 0.0;
+    for (int w = 0; w < nw; ++w) s += red[w * n + j];
+    double o = a.alpha * s;
+    if (a.use_z) o += a.beta * (double)a.z[j];
+    a.out[j] = (T)o;
+  }
+  if (threadIdx.x == 0) *a.ticket = 0u;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Narrow kernel (short rows, or X that the tensor copies cannot address)
 // ---------------------------------------------------------------------------------------------
 template <typename T, int LPR, int VPL, bool TMA>
 __global__ void __launch_bounds__(512) dense_narrow_kernel(const DenseArgs<T> a, const int R, const int S) {
@@ -177,7 +221,7 @@ __global__ void __launch_bounds__(512) dense_narrow_kernel(const DenseArgs<T> a,
 #pragma unroll
     for (int c = 0; c < C; ++c) part[c] += shfl_xor(part[c], o);
 
-  // warp -> CTA
+  // warp -> CTA -> grid
   __syncthreads();
   double* red = reinterpret_cast<double*>(smem);  // [nw][n]
   if (g == 0) {
@@ -189,37 +233,175 @@ __global__ void __launch_bounds__(512) dense_narrow_kernel(const DenseArgs<T> a,
         if (col < n) red[warp * n + col] = part[k2 * NV + e];
       }
   }
-  __syncthreads();
-  for (int64_t j = threadIdx.x; j < n; j += blockDim.x) {
-    double s = 0.0;
-    for (int w = 0; w < nw; ++w) s += red[w * n + j];
-    a.ws[blockIdx.x * n + j] = s;
+  finish_from_red(a, red, nw);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Tile kernel (rows of 64 B .. 2 KB, tensor-copied and swizzled)
+// ---------------------------------------------------------------------------------------------
+// A row of NB 128-byte column blocks is held by LPR = 2 * NB lanes, each taking
+// four 16-byte chunks. Tiles of R rows arrive by 2-D tensor copies (one box of
+// R x 128 bytes per column block) with the 128-byte swizzle, which stores chunk
+// c of row r at chunk position c ^ (r mod 8). chunk_of() assigns chunks so that
+// the 8 lanes of every quarter-warp read 8 distinct bank groups. Rows past m and
+// columns past n arrive as zeros, so the inner loop needs no masks.
+template <int LPR>
+__device__ __forceinline__ void chunk_of(int q, int j, int& b, int& c) {
+  if (LPR == 2) {
+    b = 0;
+    c = 4 * q + j;
+  } else if (LPR == 4) {
+    b = j >> 1;
+    c = 2 * q + (j & 1);
+  } else {
+    b = (q >> 3) + j * (LPR / 8);
+    c = q & 7;
+  }
+}
+
+template <int NB>
+struct TileShape {
+  static constexpr int LPR = 2 * NB;             // lanes per row
+  static constexpr int G = 32 / LPR;              // rows per warp pass
+  static constexpr int R = NB >= 8 ? 8 : 64 / NB;  // rows per tile (a multiple of 8)
+  static constexpr int P = R / G;                 // passes per tile
+  static constexpr int BOX = R * 128;             // bytes of one column block of a tile
+  static constexpr int TILE = NB * BOX;           // bytes of one pipeline stage
+};
+
+template <typename T, int NB>
+__global__ void __launch_bounds__(256, 1)
+    dense_tile_kernel(const __grid_constant__ CUtensorMap tmap, const DenseArgs<T> a, const int nbr, const int S) {
+  using VT = typename Vec16<T>::type;
+  using SH = TileShape<NB>;
+  constexpr int NV = Vec16<T>::N;
+  constexpr int LPR = SH::LPR, G = SH::G, R = SH::R, P = SH::P, BOX = SH::BOX, TILE = SH::TILE;
+  constexpr int CPL = 4, C = CPL * NV;  // chunks and columns per lane
+  constexpr int VR = (R + 31) / 32;      // registers holding the tile's v
+  // fp32 rows longer than 64 entries take the compensated dot
+  constexpr bool COMP = sizeof(T) == 4 && NB >= 4;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int g = lane / LPR, q = lane % LPR;
+  const int64_t n = a.n;
+
+  int cb[CPL], cc[CPL];
+  bool okc[CPL];
+  T yr[C];
+#pragma unroll
+  for (int j = 0; j < CPL; ++j) {
+    chunk_of<LPR>(q, j, cb[j], cc[j]);
+    const int64_t col0 = ((int64_t)cb[j] * 8 + cc[j]) * NV;
+    okc[j] = cb[j] < nbr && col0 < n;
+#pragma unroll
+    for (int e = 0; e < NV; ++e) yr[j * NV + e] = (okc[j] && col0 + e < n) ? ldg(a.y + col0 + e) : T(0);
   }
 
-  // CTA -> grid: the last CTA to arrive sums every CTA's partial in a fixed order
-  __threadfence();
-  __syncthreads();
-  __shared__ unsigned s_last;
-  if (threadIdx.x == 0) s_last = (atomicAdd(a.ticket, 1u) == gridDim.x - 1) ? 1u : 0u;
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  const int nc = gridDim.x;
-  const int cb = nc * warp / nw, ce = nc * (warp + 1) / nw;
-  for (int64_t j = lane; j < n; j += 32) {
-    double s = 0.0;
-    for (int c = cb; c < ce; ++c) s += __ldcg(a.ws + (int64_t)c * n + j);
-    red[warp * n + j] = s;
+  const int64_t gw = (int64_t)blockIdx.x * nw + warp, W = (int64_t)gridDim.x * nw;
+  const int64_t t0 = a.tiles * gw / W, t1 = a.tiles * (gw + 1) / W, nt = t1 - t0;
+  unsigned char* stages = smem + (size_t)warp * S * TILE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)nw * S * TILE) + warp * S;
+  const uint64_t pol = policy_evict_first();
+
+  auto issue = [&](int64_t tile, int s) {
+    if (lane == 0) mbar_arrive_expect_tx(&bars[s], (uint32_t)(nbr * BOX));
+    __syncwarp();
+    if (lane < nbr)
+      tma_load_2d(stages + (size_t)s * TILE + lane * BOX, &tmap, lane * (128 / (int)sizeof(T)), (int)(tile * R),
+                  &bars[s], pol);
+  };
+  auto load_v = [&](int64_t tile, T* vv) {
+#pragma unroll
+    for (int i = 0; i < VR; ++i) {
+      const int rl = lane + 32 * i;
+      const int64_t row = tile * R + rl;
+      vv[i] = (a.v != nullptr && tile < t1 && rl < R && row < a.m) ? ldg(a.v + row) : T(0);
+    }
+  };
+
+  if (lane == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
   }
-  __syncthreads();
-  for (int64_t j = threadIdx.x; j < n; j += blockDim.x) {
-    double s = 0.0;
-    for (int w = 0; w < nw; ++w) s += red[w * n + j];
-    double o = a.alpha * s;
-    if (a.use_z) o += a.beta * (double)a.z[j];
-    a.out[j] = (T)o;
+  __syncwarp();
+  for (int s = 0; s < S && s < nt; ++s) issue(t0 + s, s);
+
+  typename OuterAcc<T>::type acc[C];
+  T vnext[VR];
+  load_v(t0, vnext);
+  for (int64_t k = 0; k < nt; ++k) {
+    T vcur[VR];
+#pragma unroll
+    for (int i = 0; i < VR; ++i) vcur[i] = vnext[i];
+    if (k + 1 < nt) load_v(t0 + k + 1, vnext);
+    const int s = (int)(k % S);
+    const bool ok = mbar_wait_bounded(&bars[s], (uint32_t)((k / S) & 1));
+    if (__any_sync(FULL_MASK, !ok)) {
+      if (lane == 0)
+        for (int64_t j = k + 1; j < nt && j < k + S; ++j) mbar_wait_bounded(&bars[j % S], (uint32_t)((j / S) & 1));
+      break;
+    }
+    const unsigned char* stage = stages + (size_t)s * TILE;
+
+    T tacc[C];
+#pragma unroll
+    for (int c = 0; c < C; ++c) tacc[c] = T(0);
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+      const int r = p * G + g;
+      const unsigned char* rowp = stage + r * 128;
+      T x[C];
+#pragma unroll
+      for (int j = 0; j < CPL; ++j) {
+        if (okc[j]) {
+          const VT vv = *reinterpret_cast<const VT*>(rowp + cb[j] * BOX + ((cc[j] ^ (r & 7)) << 4));
+          unpack<T>(vv, &x[j * NV]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < NV; ++e) x[j * NV + e] = T(0);
+        }
+      }
+      DotAcc<T, COMP> dacc;
+#pragma unroll
+      for (int c = 0; c < C; ++c) dacc.add(x[c], yr[c]);
+      dacc.template group_reduce<LPR>();
+      const T vi = a.v ? __shfl_sync(FULL_MASK, vcur[(p * G) / 32], (p * G + g) & 31) : T(1);
+      const T t = vi * dacc.value();
+#pragma unroll
+      for (int c = 0; c < C; ++c) tacc[c] = fma(t, x[c], tacc[c]);
+    }
+#pragma unroll
+    for (int c = 0; c < C; ++c) acc[c].add(tacc[c]);
+    __syncwarp();
+    if (k + S < nt) {
+      fence_proxy_async_smem();
+      issue(t0 + k + S, s);
+    }
   }
-  if (threadIdx.x == 0) *a.ticket = 0u;
+
+  // lane -> warp: lanes with the same q hold the same columns
+  double part[C];
+#pragma unroll
+  for (int c = 0; c < C; ++c) part[c] = acc[c].value();
+#pragma unroll
+  for (int o = LPR; o < 32; o <<= 1)
+#pragma unroll
+    for (int c = 0; c < C; ++c) part[c] += shfl_xor(part[c], o);
+
+  __syncthreads();
+  double* red = reinterpret_cast<double*>(smem);  // [nw][n]
+  if (g == 0) {
+#pragma unroll
+    for (int j = 0; j < CPL; ++j)
+#pragma unroll
+      for (int e = 0; e < NV; ++e) {
+        const int64_t col = ((int64_t)cb[j] * 8 + cc[j]) * NV + e;
+        if (okc[j] && col < n) red[warp * n + col] = part[j * NV + e];
+      }
+  }
+  finish_from_red(a, red, nw);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -365,6 +547,62 @@ static cudaError_t launch_narrow(const DensePlan& p, const DenseArgs<T>& a, cuda
   return cudaGetLastError();
 }
 
+// cuTensorMapEncodeTiled, fetched from the driver once (no link against libcuda).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    cudaGetLastError();
+  });
+  return fn;
+}
+
+// Tensor map of X (n columns, m rows, row pitch ld) in boxes of rows x 128 bytes, 128-byte swizzle.
+template <typename T>
+static bool encode_x_map(CUtensorMap* map, const T* X, int64_t m, int64_t n, int64_t ld, int rows) {
+  EncodeTiledFn fn = encode_tiled();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)n, (cuuint64_t)m};
+  const cuuint64_t strides[1] = {(cuuint64_t)(ld * (int64_t)sizeof(T))};
+  const cuuint32_t box[2] = {(cuuint32_t)(128 / sizeof(T)), (cuuint32_t)rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, sizeof(T) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT64, 2,
+                        const_cast<T*>(X), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <typename T, int NB>
+static cudaError_t launch_tile_nb(const DensePlan& p, const CUtensorMap& map, const DenseArgs<T>& a, cudaStream_t st) {
+  cudaError_t e = ensure_smem((const void*)dense_tile_kernel<T, NB>, p.smem);
+  if (e != cudaSuccess) return e;
+  dense_tile_kernel<T, NB><<<p.ctas, p.warps * 32, p.smem, st>>>(map, a, p.nbr, p.stages);
+  return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t launch_tile(const DensePlan& p, const DenseArgs<T>& a, cudaStream_t st) {
+  CUtensorMap map;
+  if (!encode_x_map<T>(&map, a.X, a.m, a.n, a.ld, p.rows_per_tile)) return cudaErrorInvalidValue;
+  switch (p.nb) {
+    case 1: return launch_tile_nb<T, 1>(p, map, a, st);
+    case 2: return launch_tile_nb<T, 2>(p, map, a, st);
+    case 4: return launch_tile_nb<T, 4>(p, map, a, st);
+    case 8: return launch_tile_nb<T, 8>(p, map, a, st);
+    case 16: return launch_tile_nb<T, 16>(p, map, a, st);
+    default: return cudaErrorInvalidConfiguration;
+  }
+}
+
 template <typename T>
 cudaError_t launch_dense(const DensePlan& p, const DenseArgs<T>& a, cudaStream_t st) {
   switch (p.kind) {
@@ -375,6 +613,8 @@ cudaError_t launch_dense(const DensePlan& p, const DenseArgs<T>& a, cudaStream_t
       empty_rows_kernel<T><<<blocks, 256, 0, st>>>(a);
       return cudaGetLastError();
     }
+    case DENSE_TILE_TMA:
+      return launch_tile<T>(p, a, st);
     case DENSE_NARROW_TMA:
     case DENSE_NARROW_DIRECT: {
       const int key = p.lpr * 8 + p.vpl;

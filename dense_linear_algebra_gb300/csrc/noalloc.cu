@@ -92,10 +92,11 @@ extern "C" fxtx_status_t fxtx_dense_f32_noalloc(int64_t m, int64_t n, const floa
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
   const int elem = (int)sizeof(float);
-  const bool tma_ok = (reinterpret_cast<uintptr_t>(X) & 15u) == 0 && (ld * elem) % 16 == 0 && (n * elem) % 16 == 0;
-  DensePlan plan = plan_dense(nd->info, m, n, ld, elem, tma_ok);
-  if (plan.kind == DENSE_WIDE) return FXTX_ERR_TOO_LARGE;  // rows longer than the narrow kernel's 512 columns
-  if (plan.kind == DENSE_NARROW_TMA || plan.kind == DENSE_NARROW_DIRECT) {
+  const bool tile_ok = (reinterpret_cast<uintptr_t>(X) & 15u) == 0 && (ld * elem) % 16 == 0;
+  DensePlan plan = plan_dense(nd->info, m, n, ld, elem, tile_ok && (n * elem) % 16 == 0, tile_ok);
+  if (plan.kind == DENSE_WIDE) return FXTX_ERR_TOO_LARGE;  // rows longer than the narrow kernels' 512 columns
+  const bool partials = plan.kind == DENSE_NARROW_TMA || plan.kind == DENSE_NARROW_DIRECT || plan.kind == DENSE_TILE_TMA;
+  if (partials) {
     // fit the per-CTA partials into the scratch array by capping the grid
     const int64_t max_ctas = (int64_t)(kTicketOffset / ((size_t)n * sizeof(double)));
     if (max_ctas < 1) return FXTX_ERR_TOO_LARGE;
@@ -110,7 +111,7 @@ extern "C" fxtx_status_t fxtx_dense_f32_noalloc(int64_t m, int64_t n, const floa
   a.tiles = plan.rows_per_tile > 0 ? (m + plan.rows_per_tile - 1) / plan.rows_per_tile : 0;
   a.ws = reinterpret_cast<double*>(nd->scratch);
   a.ticket = reinterpret_cast<unsigned*>(nd->scratch + kTicketOffset);
-  if (plan.kind == DENSE_NARROW_TMA || plan.kind == DENSE_NARROW_DIRECT) {
+  if (partials) {
     if (cudaMemsetAsync(a.ticket, 0, sizeof(unsigned), st) != cudaSuccess) {
       cudaGetLastError();
       return FXTX_ERR_CUDA;

@@ -10,7 +10,7 @@ namespace {
 
 constexpr int64_t kTileTarget = 8 * 1024;      // bytes a warp takes per pipeline step
 constexpr int64_t kSmemBudget = 200 * 1024;    // dynamic shared memory a CTA may claim
-constexpr int kCsrThreads = 512;
+constexpr int kCsrThreads = 1024;
 
 int64_t pow2_ceil(int64_t x) {
   int64_t p = 1;
@@ -43,7 +43,7 @@ bool narrow_shape(int64_t chunks, int* lpr, int* vpl) {
   return true;
 }
 
-DensePlan plan_dense(const DeviceInfo& dev, int64_t m, int64_t n, int64_t ld, int elem, bool tma_ok) {
+DensePlan plan_dense(const DeviceInfo& dev, int64_t m, int64_t n, int64_t ld, int elem, bool tma_ok, bool tile_ok) {
   DensePlan p;
   if (n == 0) return p;  // nothing to write
   if (m == 0) {
@@ -52,12 +52,35 @@ DensePlan plan_dense(const DeviceInfo& dev, int64_t m, int64_t n, int64_t ld, in
   }
   const int64_t budget = std::min<int64_t>(kSmemBudget, dev.smem_optin > 0 ? dev.smem_optin : 48 * 1024);
   const int64_t chunks = cdiv(n * elem, 16);
+  const int64_t row_bytes = n * elem;
+  if (tile_ok && row_bytes >= 64 && row_bytes <= 2048 && m < (int64_t(1) << 31)) {
+    // tile kernel: 2 * nb lanes per row, four 16-byte chunks each; tiles of 8 KB (16 KB at nb = 16)
+    p.kind = DENSE_TILE_TMA;
+    p.nbr = (int)cdiv(row_bytes, 128);
+    p.nb = (int)pow2_ceil(p.nbr);
+    p.lpr = 2 * p.nb;
+    p.vpl = 4;
+    p.rows_per_tile = p.nb >= 8 ? 8 : 64 / p.nb;
+    const int64_t tile = (int64_t)p.nb * p.rows_per_tile * 128;
+    int warps = 8, S = 0;
+    for (;;) {
+      S = (int)std::min<int64_t>(8, (budget - 1024) / (warps * (tile + 8)));
+      if (S >= 3 || warps <= 2) break;
+      warps >>= 1;
+    }
+    p.stages = std::max(S, 1);
+    p.warps = warps;
+    p.smem = 1024 + std::max<size_t>((size_t)warps * p.stages * (tile + 8), (size_t)warps * n * sizeof(double));
+    const int64_t tiles = cdiv(m, p.rows_per_tile);
+    p.ctas = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)dev.sm_count, cdiv(tiles, p.warps)));
+    p.ws_bytes = align128((size_t)p.ctas * n * sizeof(double)) + 128;
+    return p;
+  }
   int lpr = 0, vpl = 0;
   if (narrow_shape(chunks, &lpr, &vpl)) {
     p.lpr = lpr;
     p.vpl = vpl;
     const int G = 32 / lpr;
-    const int64_t row_bytes = n * elem;
     if (tma_ok) {
       // coarsening: the largest power-of-two row count (G..32) whose tile fits the target
       int R = 32;
@@ -108,12 +131,12 @@ CsrPlan plan_csr(const DeviceInfo& dev, int64_t m, int64_t n, int64_t nnz, int e
   p.lpr = (int)std::min<int64_t>(16, std::max<int64_t>(2, lpr));
   p.group_cap = p.lpr * 4;
   p.warp_cap = 32 * 8;
+  // one 1024-thread CTA per SM, so that each SM's column window is as wide as possible
   p.threads = kCsrThreads;
   p.long_threads = kCsrThreads;
-  const int per_sm = 2;
-  const int64_t budget = std::min<int64_t>(kSmemBudget / per_sm, dev.smem_optin > 0 ? dev.smem_optin : 48 * 1024);
-  p.ctas = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)dev.sm_count * per_sm, cdiv(std::max<int64_t>(m, 1), 64)));
-  p.long_ctas = dev.sm_count * per_sm;
+  const int64_t budget = std::min<int64_t>(kSmemBudget, dev.smem_optin > 0 ? dev.smem_optin : 48 * 1024);
+  p.ctas = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)dev.sm_count, cdiv(std::max<int64_t>(m, 1), 256)));
+  p.long_ctas = dev.sm_count;
   p.win_c0 = 0;
   p.win_len = std::min<int64_t>(n, budget / elem);
   p.smem = (size_t)p.win_len * elem;
@@ -125,12 +148,12 @@ CsrPlan plan_csr(const DeviceInfo& dev, int64_t m, int64_t n, int64_t nnz, int e
 }
 
 int describe(const DensePlan& p, char* buf, size_t cap) {
-  static const char* names[] = {"noop", "empty_rows", "narrow_tma", "narrow_direct", "wide"};
+  static const char* names[] = {"noop", "empty_rows", "narrow_tma", "narrow_direct", "wide", "tile_tma"};
   return snprintf(buf, cap,
                   "dense kind=%s lanes_per_row=%d chunks_per_lane=%d rows_per_tile=%d stages=%d warps=%d ctas=%d "
-                  "smem=%zu smem_acc=%d ws=%zu",
+                  "smem=%zu smem_acc=%d blocks=%d ws=%zu",
                   names[p.kind], p.lpr, p.vpl, p.rows_per_tile, p.stages, p.warps, p.ctas, p.smem, (int)p.smem_acc,
-                  p.ws_bytes);
+                  p.nbr, p.ws_bytes);
 }
 
 int describe(const CsrPlan& p, char* buf, size_t cap) {

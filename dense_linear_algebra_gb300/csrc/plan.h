@@ -23,10 +23,12 @@ struct DeviceInfo {
   int smem_per_sm = 0;
 };
 
-enum DenseKind { DENSE_NOOP = 0, DENSE_EMPTY_ROWS, DENSE_NARROW_TMA, DENSE_NARROW_DIRECT, DENSE_WIDE };
+enum DenseKind { DENSE_NOOP = 0, DENSE_EMPTY_ROWS, DENSE_NARROW_TMA, DENSE_NARROW_DIRECT, DENSE_WIDE, DENSE_TILE_TMA };
 
 struct DensePlan {
   DenseKind kind = DENSE_NOOP;
+  int nb = 0;             // tile kernel: 128-byte column blocks per row, rounded up to a power of two
+  int nbr = 0;            // tile kernel: column blocks actually copied, ceil(n * elem / 128)
   int lpr = 0;            // lanes cooperating on one row (narrow)
   int vpl = 0;            // 16-byte chunks of a row held per lane (narrow)
   int rows_per_tile = 0;  // coarsening: rows a warp takes per pipeline step
@@ -43,7 +45,9 @@ struct DensePlan {
 // too long for the narrow kernel.
 bool narrow_shape(int64_t chunks, int* lpr, int* vpl);
 
-DensePlan plan_dense(const DeviceInfo& dev, int64_t m, int64_t n, int64_t ld, int elem, bool tma_ok);
+// tma_ok: X 16-byte aligned and rows whole 16-byte chunks (1-D bulk copies);
+// tile_ok: X 16-byte aligned and ld * elem a multiple of 16 (2-D tensor copies).
+DensePlan plan_dense(const DeviceInfo& dev, int64_t m, int64_t n, int64_t ld, int elem, bool tma_ok, bool tile_ok);
 
 struct CsrPlan {
   int lpr = 0;              // lanes per short row in the row-group kernel
