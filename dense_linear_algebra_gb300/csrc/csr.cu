@@ -4,24 +4,27 @@
 // fused kernel with its sparse specialisation, coarsening and hierarchical
 // aggregation of partial results).
 //
-// A row's entries are loaded once, used for the dot with y (gathered through
-// the read-only cache) and reused for the scatter of t_i * vals into the
-// output. Rows are binned on the fly by length:
-//   short  (<= lpr * 4)   a group of lpr lanes, entries in registers
-//   medium (<= 256)       the whole warp, entries in registers
-//   long   (> 256)        deferred to a queue; a group of 8 warps takes each
-//                         one in the long-row kernel (pass 1 forms the dot,
-//                         pass 2 re-reads the row, from L2, for the scatter)
-// Each CTA (one per SM, 1024 threads) accumulates scatters into a shared-
-// memory window of columns and flushes it once with one atomic per column;
-// columns outside the window go straight to out with atomics. fp64 window
-// updates fold the product into the atomic itself (a CAS loop around one
-// fused multiply-add), so each entry costs two fp64 operations: the dot's
-// FMA and the scatter's.
+// Every entry is loaded once, used for the dot with y (gathered through the
+// read-only cache) and reused for the scatter of t_i * vals into the output.
+// Rows are binned on the fly by length:
+//   short                 fp32: packed batches (consecutive short rows share a
+//                         warp, 8 consecutive entries per lane, so lanes are not
+//                         left idle by rows shorter than the warp); fp64: lane
+//                         groups of LPR lanes x 8 entries per row, which spend
+//                         fewer fp64 operations per entry
+//   medium (<= WARP_LONG) one warp per row, two passes (the second from L1/L2)
+//   long   (> WARP_LONG)  deferred to a queue; a group of 8 warps takes each one
+//                         in the long-row kernel, two passes
+// Row dots of a packed batch are formed lane-locally per row segment, and each
+// segment's partial is added once into a per-warp fp64 buffer; t_i is then
+// computed once per row. Each CTA (one per SM, 1024 threads) accumulates
+// scatters into a shared-memory window of columns and flushes it once with one
+// atomic per column; columns outside the window go straight to out with
+// atomics. fp64 window updates fold the product into the atomic itself (a CAS
+// loop around one fused multiply-add).
 // The prologue writes out = beta z and splits rows among CTAs by equal shares
-// of nnz + row_cost * rows. Inside a CTA, warps take row batches in a static
-// interleave, which lets each warp prefetch its next batch's row bounds and
-// entries while it computes the current one.
+// of nnz + row_cost * rows; inside a CTA, warps take 32-row windows from a
+// shared counter.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -29,13 +32,21 @@ namespace fxtx {
 
 namespace {
 
-constexpr int KG = 4;               // entries per lane for short rows
-constexpr int KW = 8;               // entries per lane for medium rows
-constexpr int LONG_UNROLL = 8;      // loads in flight per thread in the long-row kernel
-constexpr int LONG_GROUP = 256;     // threads that share one long row
 constexpr int CSR_THREADS = 1024;
+// consecutive entries per lane in a packed batch (fp64 keeps fewer, to fit 64 registers)
+template <typename T>
+struct Pack {
+  static constexpr int K = sizeof(T) == 4 ? 8 : 4;
+  static constexpr int CAP = 32 * K;  // entries per packed batch
+};
+constexpr int WARP_LONG = 4096;            // longest row a single warp takes
+constexpr int WARP_UNROLL = 8;             // loads in flight per lane for warp rows
+constexpr int LONG_UNROLL = 8;             // loads in flight per thread in the long-row kernel
+constexpr int LONG_GROUP = 256;            // threads that share one long row
+// per-warp scratch after the window: 32 row dots (double), 32 row scales (T), 33 row starts
+constexpr size_t WARP_SCRATCH = 32 * 8 + 32 * 8 + 33 * 8;
 
-// out_j += a * b, with out_j in shared memory (fp64: CAS loop around one FMA).
+// *p += a * b in shared memory (fp64: CAS loop around one FMA; fp32: native atomic).
 __device__ __forceinline__ void smem_fma_add(float* p, float a, float b) { atomicAdd(p, a * b); }
 __device__ __forceinline__ void smem_fma_add(double* p, double a, double b) {
   unsigned long long* q = reinterpret_cast<unsigned long long*>(p);
@@ -43,6 +54,16 @@ __device__ __forceinline__ void smem_fma_add(double* p, double a, double b) {
   do {
     assumed = old;
     old = atomicCAS(q, assumed, __double_as_longlong(fma(a, b, __longlong_as_double(assumed))));
+  } while (old != assumed);
+}
+
+// *p += x in shared memory, fp64.
+__device__ __forceinline__ void smem_add_f64(double* p, double x) {
+  unsigned long long* q = reinterpret_cast<unsigned long long*>(p);
+  unsigned long long old = *q, assumed;
+  do {
+    assumed = old;
+    old = atomicCAS(q, assumed, __double_as_longlong(__longlong_as_double(assumed) + x));
   } while (old != assumed);
 }
 
@@ -80,9 +101,17 @@ __device__ __forceinline__ void group_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+__host__ __device__ constexpr size_t window_bytes(int64_t len, size_t elem) {
+  return ((size_t)len * elem + 15) / 16 * 16;
+}
+
 }  // namespace
 
 int take_csr_device_error() { return take_device_error(); }
+
+size_t csr_rows_smem(int64_t win_len, int elem) { return window_bytes(win_len, elem) + 32 * WARP_SCRATCH; }
+int csr_pack_cap(int elem) { return elem == 4 ? Pack<float>::CAP : Pack<double>::CAP; }
+int csr_warp_long() { return WARP_LONG; }
 
 // out = beta z (or 0); row partition; counters.
 template <typename T>
@@ -115,137 +144,279 @@ __global__ void csr_prologue_kernel(const CsrArgs<T> a, const int nparts, const 
   }
 }
 
-template <typename T, int LPR>
+// One row of up to WARP_LONG entries, taken by a whole warp: pass 1 forms the
+// dot with WARP_UNROLL loads in flight per lane, pass 2 re-reads the row (from
+// L1/L2) and scatters it.
+template <typename T>
+__device__ __forceinline__ void warp_row(const CsrArgs<T>& a, const Window<T>& win, int64_t r, int64_t st, int64_t en,
+                                         T alpha, int lane) {
+  DotAcc<T, sizeof(T) == 4> d;
+  for (int64_t b = st + lane; b < en; b += 32 * WARP_UNROLL) {
+    T xv[WARP_UNROLL];
+    int32_t xc[WARP_UNROLL];
+#pragma unroll
+    for (int k = 0; k < WARP_UNROLL; ++k) {
+      const int64_t idx = b + 32 * k;
+      const bool ok = idx < en;
+      xv[k] = ok ? ldg(a.vals + idx) : T(0);
+      xc[k] = ok ? ldg(a.col_idx + idx) : -1;
+    }
+    T yv[WARP_UNROLL];
+#pragma unroll
+    for (int k = 0; k < WARP_UNROLL; ++k) yv[k] = xc[k] >= 0 ? ldg(a.y + xc[k]) : T(0);
+#pragma unroll
+    for (int k = 0; k < WARP_UNROLL; ++k) d.add(xv[k], yv[k]);
+  }
+  d.template group_reduce<32>();
+  const T vi = a.v ? ldg(a.v + r) : T(1);
+  const T ts = alpha * (vi * d.value());
+  for (int64_t b = st + lane; b < en; b += 32 * WARP_UNROLL) {
+    T xv[WARP_UNROLL];
+    int32_t xc[WARP_UNROLL];
+#pragma unroll
+    for (int k = 0; k < WARP_UNROLL; ++k) {
+      const int64_t idx = b + 32 * k;
+      const bool ok = idx < en;
+      xv[k] = ok ? ldg(a.vals + idx) : T(0);
+      xc[k] = ok ? ldg(a.col_idx + idx) : -1;
+    }
+#pragma unroll
+    for (int k = 0; k < WARP_UNROLL; ++k)
+      if (xc[k] >= 0) win.add(xc[k], ts, xv[k]);
+  }
+}
+
+template <typename T>
 __global__ void __launch_bounds__(CSR_THREADS, 1)
     csr_rows_kernel(const CsrArgs<T> a, const int64_t win_c0, const int64_t win_len) {
-  constexpr int G = 32 / LPR;  // rows per warp batch
+  constexpr int PACK_K = Pack<T>::K, PACK_CAP = Pack<T>::CAP;
   extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ unsigned long long s_next;
+  T* wacc = reinterpret_cast<T*>(smem);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned char* scratch = smem + window_bytes(win_len, sizeof(T)) + (size_t)warp * WARP_SCRATCH;
+  double* dotb = reinterpret_cast<double*>(scratch);          // [32] row dots of the current batch
+  T* tb = reinterpret_cast<T*>(scratch + 32 * 8);              // [32] row scales alpha * v_i * u_i
+  int64_t* rsb = reinterpret_cast<int64_t*>(scratch + 64 * 8);  // [33] row starts of the window
+  const Window<T> win{wacc, win_c0, win_len, a.out};
+  const int64_t rb = a.part[blockIdx.x], re = a.part[blockIdx.x + 1];
+  const T alpha = (T)a.alpha;
+
+  window_zero(wacc, win_len);
+  dotb[lane] = 0.0;
+  if (threadIdx.x == 0) s_next = (unsigned long long)rb;
+  __syncthreads();
+
+  for (;;) {
+    unsigned long long r0u = 0;
+    if (lane == 0) r0u = atomicAdd(&s_next, 32ull);
+    r0u = __shfl_sync(FULL_MASK, r0u, 0);
+    const int64_t r0 = (int64_t)r0u;
+    if (r0 >= re) break;
+    const int nr = (int)tmin<int64_t>(32, re - r0);  // rows in this window
+    const bool hasrow = lane < nr;
+    const int64_t rs = hasrow ? a.row_ptr[r0 + lane] : 0;
+    const int64_t rend = hasrow ? a.row_ptr[r0 + lane + 1] : 0;
+    const int64_t len = rend - rs;
+    const bool isshort = hasrow && len <= PACK_CAP;
+    rsb[lane] = hasrow ? rs : INT64_MAX;
+    if (lane == 0) rsb[32] = INT64_MAX;
+    __syncwarp();
+    const unsigned shortmask = __ballot_sync(FULL_MASK, isshort);
+
+    // packed batches: maximal runs of consecutive short rows holding at most PACK_CAP entries
+    int b0 = 0;
+    while (b0 < nr) {
+      const unsigned cand = shortmask & (0xffffffffu << b0);
+      if (cand == 0) break;
+      b0 = __ffs(cand) - 1;
+      const int64_t s = __shfl_sync(FULL_MASK, rs, b0);
+      const bool fits = lane >= b0 && isshort && rend - s <= PACK_CAP;
+      const unsigned notfit = ~__ballot_sync(FULL_MASK, fits) & (0xffffffffu << b0);
+      const int b1 = notfit ? __ffs(notfit) - 1 : 32;  // rows [b0, b1); b1 > b0 since row b0 fits
+      const int64_t e = __shfl_sync(FULL_MASK, rend, b1 - 1);
+      const int64_t base = s + (int64_t)lane * PACK_K;
+
+      T val[PACK_K];
+      int32_t col[PACK_K];
+#pragma unroll
+      for (int k = 0; k < PACK_K; ++k) {
+        const int64_t idx = base + k;
+        const bool ok = idx < e;
+        val[k] = ok ? ldg(a.vals + idx) : T(0);
+        col[k] = ok ? ldg(a.col_idx + idx) : -1;
+      }
+      T yv[PACK_K];
+#pragma unroll
+      for (int k = 0; k < PACK_K; ++k) yv[k] = col[k] >= 0 ? ldg(a.y + col[k]) : T(0);
+
+      // row of this lane's first entry: the last row of [b0, b1) starting at or before base
+      int lo = b0, hi = b1 - 1;
+#pragma unroll
+      for (int it = 0; it < 5; ++it) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (rsb[mid] <= base) lo = mid; else hi = mid - 1;
+      }
+      // lane-local segment sums, each flushed once into the warp's row-dot buffer
+      int cur = lo;
+      bool have = false;
+      DotAcc<T, sizeof(T) == 4> acc;
+#pragma unroll
+      for (int k = 0; k < PACK_K; ++k) {
+        if (col[k] >= 0) {
+          const int64_t idx = base + k;
+          while (rsb[cur + 1] <= idx) {  // rsb[b1] > idx: rows past the batch start after e
+            if (have) smem_add_f64(&dotb[cur], acc.value_f64());
+            acc = DotAcc<T, sizeof(T) == 4>();
+            have = false;
+            ++cur;
+          }
+          acc.add(val[k], yv[k]);
+          have = true;
+        }
+      }
+      if (have) smem_add_f64(&dotb[cur], acc.value_f64());
+      __syncwarp();
+      if (lane >= b0 && lane < b1) {
+        const double u = dotb[lane];
+        dotb[lane] = 0.0;
+        const T vi = a.v ? ldg(a.v + r0 + lane) : T(1);
+        tb[lane] = alpha * (vi * (T)u);
+      }
+      __syncwarp();
+      // scatter, walking the same row boundaries again
+      cur = lo;
+#pragma unroll
+      for (int k = 0; k < PACK_K; ++k) {
+        if (col[k] >= 0) {
+          const int64_t idx = base + k;
+          while (rsb[cur + 1] <= idx) ++cur;
+          win.add(col[k], tb[cur], val[k]);
+        }
+      }
+      __syncwarp();
+      b0 = b1;
+    }
+
+    // rows longer than a packed batch: one warp each, or the long-row queue
+    unsigned lm = __ballot_sync(FULL_MASK, hasrow && !isshort);
+    while (lm) {
+      const int j = __ffs(lm) - 1;
+      lm &= lm - 1;
+      const int64_t s2 = __shfl_sync(FULL_MASK, rs, j), e2 = __shfl_sync(FULL_MASK, rend, j);
+      if (e2 - s2 > WARP_LONG) {
+        if (lane == 0) a.queue[atomicAdd(&a.counters[0], 1ull)] = r0 + j;
+      } else {
+        warp_row(a, win, r0 + j, s2, e2, alpha, lane);
+      }
+    }
+    __syncwarp();  // rsb reuse
+  }
+  __syncthreads();
+  window_flush(wacc, win_c0, win_len, a.out);
+}
+
+// Short rows in lane groups: LPR lanes per row, KG entries per lane held in
+// registers, G = 32 / LPR rows per warp step. This costs fewer fp64 operations
+// per entry than the packed batches when rows are of similar length (no
+// per-segment flushes), so the fp64 path uses it. Rows longer than LPR * KG go
+// to warp_row or to the long-row queue.
+template <typename T, int LPR, int KG>
+__global__ void __launch_bounds__(CSR_THREADS, 1)
+    csr_group_kernel(const CsrArgs<T> a, const int64_t win_c0, const int64_t win_len) {
+  constexpr int G = 32 / LPR;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ unsigned long long s_next;
   T* wacc = reinterpret_cast<T*>(smem);
   const Window<T> win{wacc, win_c0, win_len, a.out};
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int lane = threadIdx.x & 31;
   const int g = lane / LPR, q = lane % LPR;
   const int64_t rb = a.part[blockIdx.x], re = a.part[blockIdx.x + 1];
   const T alpha = (T)a.alpha;
 
   window_zero(wacc, win_len);
+  if (threadIdx.x == 0) s_next = (unsigned long long)rb;
   __syncthreads();
 
-  // batch k of this warp covers rows rb + (warp + k * nw) * G + [0, G)
-  const int64_t step = (int64_t)nw * G;
-  int64_t r = rb + (int64_t)warp * G + g;
-  int64_t st = 0, en = 0;
-  if (r < re) { st = a.row_ptr[r]; en = a.row_ptr[r + 1]; }
-  // entries of the current batch (short rows), loaded one batch ahead
-  T val[KG];
-  int32_t col[KG];
-  auto load_short = [&](int64_t rr, int64_t s, int64_t e) {
-    const bool small = rr < re && e - s <= LPR * KG;
+  for (;;) {
+    unsigned long long base = 0;
+    if (lane == 0) base = atomicAdd(&s_next, (unsigned long long)G);
+    base = __shfl_sync(FULL_MASK, base, 0);
+    if ((int64_t)base >= re) break;
+    const int64_t r = (int64_t)base + g;
+    const bool has = r < re;
+    const int64_t st = has ? a.row_ptr[r] : 0, en = has ? a.row_ptr[r + 1] : 0;
+    const bool small = has && en - st <= LPR * KG;
+    const T vi = (small && a.v) ? ldg(a.v + r) : T(1);
+    T val[KG];
+    int32_t col[KG];
 #pragma unroll
     for (int k = 0; k < KG; ++k) {
-      const int64_t idx = s + q + LPR * k;
-      const bool ok = small && idx < e;
+      const int64_t idx = st + q + LPR * k;
+      const bool ok = small && idx < en;
       val[k] = ok ? ldg(a.vals + idx) : T(0);
       col[k] = ok ? ldg(a.col_idx + idx) : -1;
     }
-  };
-  load_short(r, st, en);
-
-  for (int64_t base = rb + (int64_t)warp * G; base < re; base += step) {
-    const bool has = r < re;
-    const int64_t len = en - st;
-    const bool small = has && len <= LPR * KG;
-    T cv[KG];
-    int32_t cc[KG];
-#pragma unroll
-    for (int k = 0; k < KG; ++k) { cv[k] = val[k]; cc[k] = col[k]; }
-    const int64_t cur_r = r, cur_st = st, cur_en = en;
-
-    // prefetch the next batch: row bounds, then its short-row entries
-    r += step;
-    st = en = 0;
-    if (r < re) { st = a.row_ptr[r]; en = a.row_ptr[r + 1]; }
-    load_short(r, st, en);
-
-    // short rows: one lane group, entries in registers
-    T d = T(0);
+    DotAcc<T, (sizeof(T) == 4 && LPR * KG > 64)> d;
 #pragma unroll
     for (int k = 0; k < KG; ++k)
-      if (cc[k] >= 0) d = fma(cv[k], ldg(a.y + cc[k]), d);
-    d = group_sum<LPR>(d);
-    if (small) {
-      const T vi = a.v ? ldg(a.v + cur_r) : T(1);
-      const T ts = alpha * (vi * d);
+      if (col[k] >= 0) d.add(val[k], ldg(a.y + col[k]));
+    d.template group_reduce<LPR>();
+    const T ts = alpha == T(1) ? vi * d.value() : alpha * (vi * d.value());
 #pragma unroll
-      for (int k = 0; k < KG; ++k)
-        if (cc[k] >= 0) win.add(cc[k], ts, cv[k]);
-    }
+    for (int k = 0; k < KG; ++k)
+      if (col[k] >= 0) win.add(col[k], ts, val[k]);
 
-    // medium rows: the whole warp, one row at a time
-    unsigned mm = __ballot_sync(FULL_MASK, has && !small && len <= 32 * KW && q == 0);
-    while (mm) {
-      const int src = __ffs(mm) - 1;
-      mm &= mm - 1;
-      const int64_t rr = __shfl_sync(FULL_MASK, cur_r, src);
-      const int64_t s2 = __shfl_sync(FULL_MASK, cur_st, src), e2 = __shfl_sync(FULL_MASK, cur_en, src);
-      T mv[KW];
-      int32_t mc[KW];
-#pragma unroll
-      for (int k = 0; k < KW; ++k) {
-        const int64_t idx = s2 + lane + 32 * k;
-        const bool ok = idx < e2;
-        mv[k] = ok ? ldg(a.vals + idx) : T(0);
-        mc[k] = ok ? ldg(a.col_idx + idx) : -1;
+    // longer rows: one warp each, or the long-row queue
+    unsigned lm = __ballot_sync(FULL_MASK, has && !small && q == 0);
+    while (lm) {
+      const int src = __ffs(lm) - 1;
+      lm &= lm - 1;
+      const int64_t rr = __shfl_sync(FULL_MASK, r, src);
+      const int64_t s2 = __shfl_sync(FULL_MASK, st, src), e2 = __shfl_sync(FULL_MASK, en, src);
+      if (e2 - s2 > WARP_LONG) {
+        if (lane == 0) a.queue[atomicAdd(&a.counters[0], 1ull)] = rr;
+      } else {
+        warp_row(a, win, rr, s2, e2, alpha, lane);
       }
-      DotAcc<T, sizeof(T) == 4> mdot;
-#pragma unroll
-      for (int k = 0; k < KW; ++k)
-        if (mc[k] >= 0) mdot.add(mv[k], ldg(a.y + mc[k]));
-      mdot.template group_reduce<32>();
-      const T vi = a.v ? ldg(a.v + rr) : T(1);
-      const T ts = alpha * (vi * mdot.value());
-#pragma unroll
-      for (int k = 0; k < KW; ++k)
-        if (mc[k] >= 0) win.add(mc[k], ts, mv[k]);
-    }
-
-    // long rows: defer to the long-row kernel
-    if (has && len > 32 * KW && q == 0) {
-      const unsigned long long pos = atomicAdd(&a.counters[0], 1ull);
-      a.queue[pos] = cur_r;
     }
   }
   __syncthreads();
   window_flush(wacc, win_c0, win_len, a.out);
 }
 
-// Long rows: each group of LONG_GROUP threads takes queued rows one at a time.
+// Rows longer than WARP_LONG: each group of LONG_GROUP threads takes queued rows
+// one at a time, with one group barrier per row. The next row's index is
+// claimed while the current one is processed, and the per-warp partial dots are
+// double-buffered by row parity, so the single barrier orders both.
 template <typename T>
 __global__ void __launch_bounds__(CSR_THREADS, 1)
     csr_long_kernel(const CsrArgs<T> a, const int64_t win_c0, const int64_t win_len) {
   constexpr int GW = LONG_GROUP / 32;  // warps per group
   constexpr int NG = CSR_THREADS / LONG_GROUP;
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ long long s_row[NG];
-  __shared__ double s_red[NG][GW];
-  __shared__ T s_t[NG];
+  __shared__ long long s_row[NG][2];
+  __shared__ double s_red[NG][2][GW];
   T* wacc = reinterpret_cast<T*>(smem);
   const Window<T> win{wacc, win_c0, win_len, a.out};
   const int lane = threadIdx.x & 31;
   const int grp = threadIdx.x / LONG_GROUP, gt = threadIdx.x % LONG_GROUP, gw = gt >> 5;
   const int bar = 1 + grp;
   const T alpha = (T)a.alpha;
+  const unsigned long long count = a.counters[0];
+  auto claim = [&]() -> long long {
+    const unsigned long long k = atomicAdd(&a.counters[1], 1ull);
+    return k < count ? (long long)a.queue[k] : -1ll;
+  };
 
   window_zero(wacc, win_len);
+  if (gt == 0) s_row[grp][0] = count > 0 ? claim() : -1ll;
   __syncthreads();
-  const unsigned long long count = a.counters[0];
-  for (;;) {
-    if (gt == 0) {
-      const unsigned long long k = atomicAdd(&a.counters[1], 1ull);
-      s_row[grp] = k < count ? (long long)a.queue[k] : -1ll;
-    }
-    group_barrier(bar, LONG_GROUP);
-    const int64_t r = s_row[grp];
+  for (int it = 0;; ++it) {
+    const int cur = it & 1;
+    const int64_t r = s_row[grp][cur];
     if (r < 0) break;
+    if (gt == 0) s_row[grp][cur ^ 1] = claim();
     const int64_t st = a.row_ptr[r], en = a.row_ptr[r + 1];
 
     // pass 1: the dot, LONG_UNROLL independent loads in flight per thread
@@ -267,16 +438,13 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
       for (int k = 0; k < LONG_UNROLL; ++k) d.add(xv[k], yv[k]);
     }
     d.template group_reduce<32>();
-    if (lane == 0) s_red[grp][gw] = d.value_f64();
+    if (lane == 0) s_red[grp][cur][gw] = d.value_f64();
     group_barrier(bar, LONG_GROUP);
-    if (gt == 0) {
-      double u = 0.0;
-      for (int w = 0; w < GW; ++w) u += s_red[grp][w];
-      const T vi = a.v ? a.v[r] : T(1);
-      s_t[grp] = alpha * (vi * (T)u);
-    }
-    group_barrier(bar, LONG_GROUP);
-    const T ts = s_t[grp];
+    double u = 0.0;
+#pragma unroll
+    for (int w = 0; w < GW; ++w) u += s_red[grp][cur][w];
+    const T vi = a.v ? ldg(a.v + r) : T(1);
+    const T ts = alpha * (vi * (T)u);
 
     // pass 2: the scatter, re-reading the row (served by L2)
     for (int64_t b = st + gt; b < en; b += (int64_t)LONG_GROUP * LONG_UNROLL) {
@@ -293,18 +461,9 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
       for (int k = 0; k < LONG_UNROLL; ++k)
         if (xc[k] >= 0) win.add(xc[k], ts, xv[k]);
     }
-    group_barrier(bar, LONG_GROUP);  // s_row / s_red / s_t reuse
   }
   __syncthreads();
   window_flush(wacc, win_c0, win_len, a.out);
-}
-
-template <typename T, int LPR>
-static cudaError_t launch_rows(const CsrPlan& p, const CsrArgs<T>& a, cudaStream_t st) {
-  cudaError_t e = ensure_smem((const void*)csr_rows_kernel<T, LPR>, p.smem);
-  if (e != cudaSuccess) return e;
-  csr_rows_kernel<T, LPR><<<p.ctas, p.threads, p.smem, st>>>(a, p.win_c0, p.win_len);
-  return cudaGetLastError();
 }
 
 template <typename T>
@@ -318,13 +477,26 @@ cudaError_t launch_csr(const CsrPlan& p, const CsrArgs<T>& a, cudaStream_t st) {
   }
   if (a.m == 0) return cudaSuccess;
   cudaError_t e;
-  switch (p.lpr) {
-    case 2: e = launch_rows<T, 2>(p, a, st); break;
-    case 4: e = launch_rows<T, 4>(p, a, st); break;
-    case 8: e = launch_rows<T, 8>(p, a, st); break;
-    case 16: e = launch_rows<T, 16>(p, a, st); break;
-    default: return cudaErrorInvalidConfiguration;
+  if (p.group_lpr == 0) {
+    e = ensure_smem((const void*)csr_rows_kernel<T>, p.smem);
+    if (e != cudaSuccess) return e;
+    csr_rows_kernel<T><<<p.ctas, p.threads, p.smem, st>>>(a, p.win_c0, p.win_len);
+  } else {
+    const void* k = p.group_lpr == 4    ? (const void*)csr_group_kernel<T, 4, 8>
+                    : p.group_lpr == 8  ? (const void*)csr_group_kernel<T, 8, 8>
+                    : p.group_lpr == 16 ? (const void*)csr_group_kernel<T, 16, 8>
+                                        : (const void*)csr_group_kernel<T, 2, 8>;
+    e = ensure_smem(k, p.long_smem);
+    if (e != cudaSuccess) return e;
+    switch (p.group_lpr) {
+      case 2: csr_group_kernel<T, 2, 8><<<p.ctas, p.threads, p.long_smem, st>>>(a, p.win_c0, p.win_len); break;
+      case 4: csr_group_kernel<T, 4, 8><<<p.ctas, p.threads, p.long_smem, st>>>(a, p.win_c0, p.win_len); break;
+      case 8: csr_group_kernel<T, 8, 8><<<p.ctas, p.threads, p.long_smem, st>>>(a, p.win_c0, p.win_len); break;
+      case 16: csr_group_kernel<T, 16, 8><<<p.ctas, p.threads, p.long_smem, st>>>(a, p.win_c0, p.win_len); break;
+      default: return cudaErrorInvalidConfiguration;
+    }
   }
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = ensure_smem((const void*)csr_long_kernel<T>, p.long_smem);
   if (e != cudaSuccess) return e;

@@ -20,6 +20,8 @@
 //   accumulators in fixed order and applies the epilogue.
 #include <algorithm>
 #include <mutex>
+#include <tuple>
+#include <vector>
 
 #include <cuda.h>
 
@@ -529,9 +531,28 @@ __global__ void empty_rows_kernel(const DenseArgs<T> a) {
 // ---------------------------------------------------------------------------------------------
 // Host launchers
 // ---------------------------------------------------------------------------------------------
+// The attribute is set once per (kernel, device) at the largest size asked for so
+// far; later calls that fit skip the driver call.
 cudaError_t ensure_smem(const void* kernel, size_t bytes) {
   if (bytes <= 48 * 1024) return cudaSuccess;
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  static std::mutex mu;
+  static std::vector<std::tuple<const void*, int, size_t>> done;
+  std::lock_guard<std::mutex> lock(mu);
+  for (auto& d : done)
+    if (std::get<0>(d) == kernel && std::get<1>(d) == dev && std::get<2>(d) >= bytes) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) {
+    bool found = false;
+    for (auto& d : done)
+      if (std::get<0>(d) == kernel && std::get<1>(d) == dev) {
+        std::get<2>(d) = bytes;
+        found = true;
+      }
+    if (!found) done.emplace_back(kernel, dev, bytes);
+  }
+  return e;
 }
 
 template <typename T, int LPR, int VPL>

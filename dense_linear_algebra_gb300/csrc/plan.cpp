@@ -125,22 +125,25 @@ DensePlan plan_dense(const DeviceInfo& dev, int64_t m, int64_t n, int64_t ld, in
 
 CsrPlan plan_csr(const DeviceInfo& dev, int64_t m, int64_t n, int64_t nnz, int elem) {
   CsrPlan p;
-  const double avg = m > 0 ? (double)nnz / (double)m : 0.0;
-  // short rows: the smallest power-of-two group whose registers (4 per lane) hold an average row
-  int64_t lpr = pow2_ceil((int64_t)(avg / 4.0 + 0.999));
-  p.lpr = (int)std::min<int64_t>(16, std::max<int64_t>(2, lpr));
-  p.group_cap = p.lpr * 4;
-  p.warp_cap = 32 * 8;
+  // fp64 short rows go to lane groups sized to the mean row (8 entries per lane); fp32 to packed batches
+  if (elem == 8) {
+    const double avg = m > 0 ? (double)nnz / (double)m : 0.0;
+    p.group_lpr = (int)std::min<int64_t>(16, std::max<int64_t>(2, pow2_ceil((int64_t)(avg / 8.0 + 0.999))));
+  }
+  p.pack_cap = csr_pack_cap(elem);
+  p.pack_k = p.pack_cap / 32;
+  p.warp_cap = csr_warp_long();
   // one 1024-thread CTA per SM, so that each SM's column window is as wide as possible
   p.threads = kCsrThreads;
   p.long_threads = kCsrThreads;
   const int64_t budget = std::min<int64_t>(kSmemBudget, dev.smem_optin > 0 ? dev.smem_optin : 48 * 1024);
-  p.ctas = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)dev.sm_count, cdiv(std::max<int64_t>(m, 1), 256)));
+  const int64_t fixed = (int64_t)csr_rows_smem(0, elem);  // per-warp scratch of the row kernel
+  p.ctas = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)dev.sm_count, cdiv(std::max<int64_t>(m, 1), 1024)));
   p.long_ctas = dev.sm_count;
   p.win_c0 = 0;
-  p.win_len = std::min<int64_t>(n, budget / elem);
-  p.smem = (size_t)p.win_len * elem;
-  p.long_smem = p.smem;
+  p.win_len = std::max<int64_t>(0, std::min<int64_t>(n, (budget - fixed) / elem));
+  p.smem = csr_rows_smem(p.win_len, elem);
+  p.long_smem = (size_t)(p.win_len * elem + 15) / 16 * 16;
   p.row_cost = 8;
   p.queue_cap = std::min<int64_t>(m, nnz / (p.warp_cap + 1) + 1);
   p.ws_bytes = align128((size_t)(p.ctas + 1) * 8) + align128((size_t)std::max<int64_t>(p.queue_cap, 1) * 8) + 128;
@@ -158,9 +161,9 @@ int describe(const DensePlan& p, char* buf, size_t cap) {
 
 int describe(const CsrPlan& p, char* buf, size_t cap) {
   return snprintf(buf, cap,
-                  "csr lanes_per_row=%d group_cap=%d warp_cap=%d ctas=%d threads=%d long_ctas=%d window=[%lld,+%lld) "
-                  "smem=%zu queue_cap=%lld ws=%zu",
-                  p.lpr, p.group_cap, p.warp_cap, p.ctas, p.threads, p.long_ctas, (long long)p.win_c0,
+                  "csr group_lanes=%d pack_k=%d pack_cap=%d warp_cap=%d ctas=%d threads=%d long_ctas=%d "
+                  "window=[%lld,+%lld) smem=%zu queue_cap=%lld ws=%zu",
+                  p.group_lpr, p.pack_k, p.pack_cap, p.warp_cap, p.ctas, p.threads, p.long_ctas, (long long)p.win_c0,
                   (long long)p.win_len, p.smem, (long long)p.queue_cap, p.ws_bytes);
 }
 

@@ -50,17 +50,24 @@ bool narrow_shape(int64_t chunks, int* lpr, int* vpl);
 DensePlan plan_dense(const DeviceInfo& dev, int64_t m, int64_t n, int64_t ld, int elem, bool tma_ok, bool tile_ok);
 
 struct CsrPlan {
-  int lpr = 0;              // lanes per short row in the row-group kernel
-  int group_cap = 0;        // longest row a lane group keeps in registers (lpr * 4)
-  int warp_cap = 0;         // longest row a whole warp keeps in registers
-  int ctas = 0, threads = 0;       // row-group kernel
+  int group_lpr = 0;        // short rows in lane groups of this many lanes (x 8 entries); 0: packed batches
+  int pack_k = 0;           // consecutive entries per lane in a packed batch of short rows
+  int pack_cap = 0;         // entries per packed batch (32 * pack_k): longer rows are not packed
+  int warp_cap = 0;         // longest row one warp takes; longer rows go to the long-row kernel
+  int ctas = 0, threads = 0;            // row kernel
   int long_ctas = 0, long_threads = 0;  // long-row kernel
-  int64_t win_c0 = 0, win_len = 0;  // columns accumulated in shared memory
+  int64_t win_c0 = 0, win_len = 0;      // columns accumulated in shared memory
   size_t smem = 0, long_smem = 0;
   int row_cost = 0;         // nnz-equivalent cost of one row, for the partition
   size_t ws_bytes = 0;
   int64_t queue_cap = 0;    // capacity of the long-row queue
 };
+
+// Constants of the CSR kernels (csr.cu): shared memory of the row kernel for a
+// window of win_len columns, the packed-batch capacity and the one-warp row limit.
+size_t csr_rows_smem(int64_t win_len, int elem);
+int csr_pack_cap(int elem);
+int csr_warp_long();
 
 CsrPlan plan_csr(const DeviceInfo& dev, int64_t m, int64_t n, int64_t nnz, int elem);
 
