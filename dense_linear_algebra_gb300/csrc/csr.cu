@@ -13,8 +13,9 @@
 //                         groups of LPR lanes x 8 entries per row, which spend
 //                         fewer fp64 operations per entry
 //   medium (<= WARP_LONG) one warp per row, two passes (the second from L1/L2)
-//   long   (> WARP_LONG)  deferred to a queue; a group of 8 warps takes each one
+//   long   (> WARP_LONG)  deferred to a queue; a group of 4 warps takes each one
 //                         in the long-row kernel, two passes
+// The y gathers of hot columns hit a copy of y[0, ylen) in shared memory.
 // Row dots of a packed batch are formed lane-locally per row segment, and each
 // segment's partial is added once into a per-warp fp64 buffer; t_i is then
 // computed once per row. Each CTA (one per SM, 1024 threads) accumulates
@@ -39,10 +40,10 @@ struct Pack {
   static constexpr int K = sizeof(T) == 4 ? 8 : 4;
   static constexpr int CAP = 32 * K;  // entries per packed batch
 };
-constexpr int WARP_LONG = 4096;            // longest row a single warp takes
+constexpr int WARP_LONG = 1024;            // longest row a single warp takes
 constexpr int WARP_UNROLL = 8;             // loads in flight per lane for warp rows
 constexpr int LONG_UNROLL = 8;             // loads in flight per thread in the long-row kernel
-constexpr int LONG_GROUP = 256;            // threads that share one long row
+constexpr int LONG_GROUP = 128;            // threads that share one long row
 // per-warp scratch after the window: 32 row dots (double), 32 row scales (T), 33 row starts
 constexpr size_t WARP_SCRATCH = 32 * 8 + 32 * 8 + 33 * 8;
 
@@ -67,12 +68,17 @@ __device__ __forceinline__ void smem_add_f64(double* p, double x) {
   } while (old != assumed);
 }
 
+// Shared-memory windows of one CTA: scatters into columns [c0, c0 + len) are
+// accumulated in `acc`, and y[0, ylen) is held in `ys` for the gathers.
 template <typename T>
 struct Window {
   T* acc;
   int64_t c0;
   int64_t len;
   T* out;
+  const T* ys;
+  int64_t ylen;
+  const T* y;
   // out[col] += a * b, through the shared window when col falls inside it
   __device__ __forceinline__ void add(int32_t col, T a, T b) const {
     const uint64_t off = (uint64_t)((int64_t)col - c0);
@@ -81,11 +87,15 @@ struct Window {
     else
       atomicAdd(out + col, a * b);
   }
+  __device__ __forceinline__ T yat(int32_t col) const { return (int64_t)col < ylen ? ys[col] : ldg(y + col); }
 };
 
+// Zeroes the accumulator window and copies y[0, ylen) into shared memory.
 template <typename T>
-__device__ __forceinline__ void window_zero(T* acc, int64_t len) {
-  for (int64_t j = threadIdx.x; j < len; j += blockDim.x) acc[j] = T(0);
+__device__ __forceinline__ void window_init(const Window<T>& w) {
+  for (int64_t j = threadIdx.x; j < w.len; j += blockDim.x) w.acc[j] = T(0);
+  T* ys = const_cast<T*>(w.ys);
+  for (int64_t j = threadIdx.x; j < w.ylen; j += blockDim.x) ys[j] = ldg(w.y + j);
 }
 
 template <typename T>
@@ -109,7 +119,9 @@ __host__ __device__ constexpr size_t window_bytes(int64_t len, size_t elem) {
 
 int take_csr_device_error() { return take_device_error(); }
 
-size_t csr_rows_smem(int64_t win_len, int elem) { return window_bytes(win_len, elem) + 32 * WARP_SCRATCH; }
+size_t csr_rows_smem(int64_t win_len, int64_t ylen, int elem) {
+  return window_bytes(win_len, elem) + window_bytes(ylen, elem) + 32 * WARP_SCRATCH;
+}
 int csr_pack_cap(int elem) { return elem == 4 ? Pack<float>::CAP : Pack<double>::CAP; }
 int csr_warp_long() { return WARP_LONG; }
 
@@ -163,7 +175,7 @@ __device__ __forceinline__ void warp_row(const CsrArgs<T>& a, const Window<T>& w
     }
     T yv[WARP_UNROLL];
 #pragma unroll
-    for (int k = 0; k < WARP_UNROLL; ++k) yv[k] = xc[k] >= 0 ? ldg(a.y + xc[k]) : T(0);
+    for (int k = 0; k < WARP_UNROLL; ++k) yv[k] = xc[k] >= 0 ? win.yat(xc[k]) : T(0);
 #pragma unroll
     for (int k = 0; k < WARP_UNROLL; ++k) d.add(xv[k], yv[k]);
   }
@@ -188,21 +200,23 @@ __device__ __forceinline__ void warp_row(const CsrArgs<T>& a, const Window<T>& w
 
 template <typename T>
 __global__ void __launch_bounds__(CSR_THREADS, 1)
-    csr_rows_kernel(const CsrArgs<T> a, const int64_t win_c0, const int64_t win_len) {
+    csr_rows_kernel(const CsrArgs<T> a, const int64_t win_c0, const int64_t win_len, const int64_t ylen) {
   constexpr int PACK_K = Pack<T>::K, PACK_CAP = Pack<T>::CAP;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ unsigned long long s_next;
   T* wacc = reinterpret_cast<T*>(smem);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  unsigned char* scratch = smem + window_bytes(win_len, sizeof(T)) + (size_t)warp * WARP_SCRATCH;
+  T* ys = reinterpret_cast<T*>(smem + window_bytes(win_len, sizeof(T)));
+  unsigned char* scratch =
+      smem + window_bytes(win_len, sizeof(T)) + window_bytes(ylen, sizeof(T)) + (size_t)warp * WARP_SCRATCH;
   double* dotb = reinterpret_cast<double*>(scratch);          // [32] row dots of the current batch
   T* tb = reinterpret_cast<T*>(scratch + 32 * 8);              // [32] row scales alpha * v_i * u_i
   int64_t* rsb = reinterpret_cast<int64_t*>(scratch + 64 * 8);  // [33] row starts of the window
-  const Window<T> win{wacc, win_c0, win_len, a.out};
+  const Window<T> win{wacc, win_c0, win_len, a.out, ys, ylen, a.y};
   const int64_t rb = a.part[blockIdx.x], re = a.part[blockIdx.x + 1];
   const T alpha = (T)a.alpha;
 
-  window_zero(wacc, win_len);
+  window_init(win);
   dotb[lane] = 0.0;
   if (threadIdx.x == 0) s_next = (unsigned long long)rb;
   __syncthreads();
@@ -248,7 +262,7 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
       }
       T yv[PACK_K];
 #pragma unroll
-      for (int k = 0; k < PACK_K; ++k) yv[k] = col[k] >= 0 ? ldg(a.y + col[k]) : T(0);
+      for (int k = 0; k < PACK_K; ++k) yv[k] = col[k] >= 0 ? win.yat(col[k]) : T(0);
 
       // row of this lane's first entry: the last row of [b0, b1) starting at or before base
       int lo = b0, hi = b1 - 1;
@@ -323,18 +337,19 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
 // to warp_row or to the long-row queue.
 template <typename T, int LPR, int KG>
 __global__ void __launch_bounds__(CSR_THREADS, 1)
-    csr_group_kernel(const CsrArgs<T> a, const int64_t win_c0, const int64_t win_len) {
+    csr_group_kernel(const CsrArgs<T> a, const int64_t win_c0, const int64_t win_len, const int64_t ylen) {
   constexpr int G = 32 / LPR;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ unsigned long long s_next;
   T* wacc = reinterpret_cast<T*>(smem);
-  const Window<T> win{wacc, win_c0, win_len, a.out};
+  const T* ys = reinterpret_cast<const T*>(smem + window_bytes(win_len, sizeof(T)));
+  const Window<T> win{wacc, win_c0, win_len, a.out, ys, ylen, a.y};
   const int lane = threadIdx.x & 31;
   const int g = lane / LPR, q = lane % LPR;
   const int64_t rb = a.part[blockIdx.x], re = a.part[blockIdx.x + 1];
   const T alpha = (T)a.alpha;
 
-  window_zero(wacc, win_len);
+  window_init(win);
   if (threadIdx.x == 0) s_next = (unsigned long long)rb;
   __syncthreads();
 
@@ -360,7 +375,7 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
     DotAcc<T, (sizeof(T) == 4 && LPR * KG > 64)> d;
 #pragma unroll
     for (int k = 0; k < KG; ++k)
-      if (col[k] >= 0) d.add(val[k], ldg(a.y + col[k]));
+      if (col[k] >= 0) d.add(val[k], win.yat(col[k]));
     d.template group_reduce<LPR>();
     const T ts = alpha == T(1) ? vi * d.value() : alpha * (vi * d.value());
 #pragma unroll
@@ -391,14 +406,15 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
 // double-buffered by row parity, so the single barrier orders both.
 template <typename T>
 __global__ void __launch_bounds__(CSR_THREADS, 1)
-    csr_long_kernel(const CsrArgs<T> a, const int64_t win_c0, const int64_t win_len) {
+    csr_long_kernel(const CsrArgs<T> a, const int64_t win_c0, const int64_t win_len, const int64_t ylen) {
   constexpr int GW = LONG_GROUP / 32;  // warps per group
   constexpr int NG = CSR_THREADS / LONG_GROUP;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ long long s_row[NG][2];
   __shared__ double s_red[NG][2][GW];
   T* wacc = reinterpret_cast<T*>(smem);
-  const Window<T> win{wacc, win_c0, win_len, a.out};
+  const T* ys = reinterpret_cast<const T*>(smem + window_bytes(win_len, sizeof(T)));
+  const Window<T> win{wacc, win_c0, win_len, a.out, ys, ylen, a.y};
   const int lane = threadIdx.x & 31;
   const int grp = threadIdx.x / LONG_GROUP, gt = threadIdx.x % LONG_GROUP, gw = gt >> 5;
   const int bar = 1 + grp;
@@ -409,7 +425,7 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
     return k < count ? (long long)a.queue[k] : -1ll;
   };
 
-  window_zero(wacc, win_len);
+  window_init(win);
   if (gt == 0) s_row[grp][0] = count > 0 ? claim() : -1ll;
   __syncthreads();
   for (int it = 0;; ++it) {
@@ -433,7 +449,7 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
       }
       T yv[LONG_UNROLL];
 #pragma unroll
-      for (int k = 0; k < LONG_UNROLL; ++k) yv[k] = xc[k] >= 0 ? ldg(a.y + xc[k]) : T(0);
+      for (int k = 0; k < LONG_UNROLL; ++k) yv[k] = xc[k] >= 0 ? win.yat(xc[k]) : T(0);
 #pragma unroll
       for (int k = 0; k < LONG_UNROLL; ++k) d.add(xv[k], yv[k]);
     }
@@ -480,7 +496,7 @@ cudaError_t launch_csr(const CsrPlan& p, const CsrArgs<T>& a, cudaStream_t st) {
   if (p.group_lpr == 0) {
     e = ensure_smem((const void*)csr_rows_kernel<T>, p.smem);
     if (e != cudaSuccess) return e;
-    csr_rows_kernel<T><<<p.ctas, p.threads, p.smem, st>>>(a, p.win_c0, p.win_len);
+    csr_rows_kernel<T><<<p.ctas, p.threads, p.smem, st>>>(a, p.win_c0, p.win_len, p.ylen);
   } else {
     const void* k = p.group_lpr == 4    ? (const void*)csr_group_kernel<T, 4, 8>
                     : p.group_lpr == 8  ? (const void*)csr_group_kernel<T, 8, 8>
@@ -489,10 +505,10 @@ cudaError_t launch_csr(const CsrPlan& p, const CsrArgs<T>& a, cudaStream_t st) {
     e = ensure_smem(k, p.long_smem);
     if (e != cudaSuccess) return e;
     switch (p.group_lpr) {
-      case 2: csr_group_kernel<T, 2, 8><<<p.ctas, p.threads, p.long_smem, st>>>(a, p.win_c0, p.win_len); break;
-      case 4: csr_group_kernel<T, 4, 8><<<p.ctas, p.threads, p.long_smem, st>>>(a, p.win_c0, p.win_len); break;
-      case 8: csr_group_kernel<T, 8, 8><<<p.ctas, p.threads, p.long_smem, st>>>(a, p.win_c0, p.win_len); break;
-      case 16: csr_group_kernel<T, 16, 8><<<p.ctas, p.threads, p.long_smem, st>>>(a, p.win_c0, p.win_len); break;
+      case 2: csr_group_kernel<T, 2, 8><<<p.ctas, p.threads, p.long_smem, st>>>(a, p.win_c0, p.win_len, p.ylen); break;
+      case 4: csr_group_kernel<T, 4, 8><<<p.ctas, p.threads, p.long_smem, st>>>(a, p.win_c0, p.win_len, p.ylen); break;
+      case 8: csr_group_kernel<T, 8, 8><<<p.ctas, p.threads, p.long_smem, st>>>(a, p.win_c0, p.win_len, p.ylen); break;
+      case 16: csr_group_kernel<T, 16, 8><<<p.ctas, p.threads, p.long_smem, st>>>(a, p.win_c0, p.win_len, p.ylen); break;
       default: return cudaErrorInvalidConfiguration;
     }
   }
@@ -500,7 +516,7 @@ cudaError_t launch_csr(const CsrPlan& p, const CsrArgs<T>& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   e = ensure_smem((const void*)csr_long_kernel<T>, p.long_smem);
   if (e != cudaSuccess) return e;
-  csr_long_kernel<T><<<p.long_ctas, p.long_threads, p.long_smem, st>>>(a, p.win_c0, p.win_len);
+  csr_long_kernel<T><<<p.long_ctas, p.long_threads, p.long_smem, st>>>(a, p.win_c0, p.win_len, p.ylen);
   return cudaGetLastError();
 }
 

@@ -137,13 +137,16 @@ CsrPlan plan_csr(const DeviceInfo& dev, int64_t m, int64_t n, int64_t nnz, int e
   p.threads = kCsrThreads;
   p.long_threads = kCsrThreads;
   const int64_t budget = std::min<int64_t>(kSmemBudget, dev.smem_optin > 0 ? dev.smem_optin : 48 * 1024);
-  const int64_t fixed = (int64_t)csr_rows_smem(0, elem);  // per-warp scratch of the row kernel
+  const int64_t fixed = (int64_t)csr_rows_smem(0, 0, elem) + 32;  // per-warp scratch of the row kernel + padding
   p.ctas = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)dev.sm_count, cdiv(std::max<int64_t>(m, 1), 1024)));
   p.long_ctas = dev.sm_count;
+  // shared memory: the accumulator window takes up to three quarters, a copy of y's head the rest
+  const int64_t room = std::max<int64_t>(0, budget - fixed) / elem;
   p.win_c0 = 0;
-  p.win_len = std::max<int64_t>(0, std::min<int64_t>(n, (budget - fixed) / elem));
-  p.smem = csr_rows_smem(p.win_len, elem);
-  p.long_smem = (size_t)(p.win_len * elem + 15) / 16 * 16;
+  p.win_len = std::min<int64_t>(n, room * 3 / 4);
+  p.ylen = std::min<int64_t>(n, room - p.win_len);
+  p.smem = csr_rows_smem(p.win_len, p.ylen, elem);
+  p.long_smem = csr_rows_smem(p.win_len, p.ylen, elem) - (size_t)csr_rows_smem(0, 0, elem);
   p.row_cost = 8;
   p.queue_cap = std::min<int64_t>(m, nnz / (p.warp_cap + 1) + 1);
   p.ws_bytes = align128((size_t)(p.ctas + 1) * 8) + align128((size_t)std::max<int64_t>(p.queue_cap, 1) * 8) + 128;
@@ -162,9 +165,9 @@ int describe(const DensePlan& p, char* buf, size_t cap) {
 int describe(const CsrPlan& p, char* buf, size_t cap) {
   return snprintf(buf, cap,
                   "csr group_lanes=%d pack_k=%d pack_cap=%d warp_cap=%d ctas=%d threads=%d long_ctas=%d "
-                  "window=[%lld,+%lld) smem=%zu queue_cap=%lld ws=%zu",
+                  "window=[%lld,+%lld) y_window=%lld smem=%zu queue_cap=%lld ws=%zu",
                   p.group_lpr, p.pack_k, p.pack_cap, p.warp_cap, p.ctas, p.threads, p.long_ctas, (long long)p.win_c0,
-                  (long long)p.win_len, p.smem, (long long)p.queue_cap, p.ws_bytes);
+                  (long long)p.win_len, (long long)p.ylen, p.smem, (long long)p.queue_cap, p.ws_bytes);
 }
 
 }  // namespace fxtx

@@ -57,15 +57,17 @@ struct CsrPlan {
   int ctas = 0, threads = 0;            // row kernel
   int long_ctas = 0, long_threads = 0;  // long-row kernel
   int64_t win_c0 = 0, win_len = 0;      // columns accumulated in shared memory
+  int64_t ylen = 0;                     // y[0, ylen) held in shared memory for the gathers
   size_t smem = 0, long_smem = 0;
   int row_cost = 0;         // nnz-equivalent cost of one row, for the partition
   size_t ws_bytes = 0;
   int64_t queue_cap = 0;    // capacity of the long-row queue
 };
 
-// Constants of the CSR kernels (csr.cu): shared memory of the row kernel for a
-// window of win_len columns, the packed-batch capacity and the one-warp row limit.
-size_t csr_rows_smem(int64_t win_len, int elem);
+// Constants of the CSR kernels (csr.cu): shared memory of the row kernel for an
+// accumulator window of win_len columns and a y window of ylen entries, the
+// packed-batch capacity and the one-warp row limit.
+size_t csr_rows_smem(int64_t win_len, int64_t ylen, int elem);
 int csr_pack_cap(int elem);
 int csr_warp_long();
 
