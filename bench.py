@@ -436,6 +436,49 @@ def run_fused(args, name, desc, p, rank, world, dist):
     return rec
 
 
+def run_solver(args):
+    """Ridge regression by CG on the tall workload's X: fused operator vs the cuBLAS pair, per iteration."""
+    import torch
+
+    import inputgen
+    from dense_linear_algebra_gb300 import solvers
+
+    p = inputgen.dense_tall(variant="c", m=args.rows or 16_000_000)
+    dev = torch.device("cuda", 0)
+    X = torch.from_numpy(p.X).to(dev)
+    w_true = torch.from_numpy(inputgen.normal(0, 7, p.n, np.float32)).to(dev)
+    b = torch.mv(X, w_true) + 0.1 * torch.from_numpy(inputgen.normal(0, 8, p.m, np.float32)).to(dev)
+    lam = 1.0
+    iters = 32
+    rhs = solvers.rmatvec(X, b)
+
+    def fused_op(q):
+        return solvers.fused(X, q, None, 1.0, lam, q)
+
+    def unfused_op(q):
+        return torch.mv(X.t(), torch.mv(X, q)) + lam * q
+
+    out = {}
+    for name, op in (("fused", fused_op), ("unfused_cublas", unfused_op)):
+        solvers.cg(op, rhs, tol=0.0, max_iter=3, check_every=3)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        w, info = solvers.cg(op, rhs, tol=0.0, max_iter=iters, check_every=iters)
+        e1.record()
+        torch.cuda.synchronize()
+        out[name] = {"ms_per_iteration": round(e0.elapsed_time(e1) / info.iterations, 4),
+                     "relative_residual": info.residual}
+    rec = {"metric": "ridge regression by conjugate gradients: ms per CG iteration", "unit": "ms",
+           "higher_is_better": False, "data": "synthetic",
+           "config": {"workload": f"X {p.m} x {p.n} fp32 N(0,1), b = X w + 0.1 noise, lambda = 1, {iters} iterations",
+                      "operator": "X^T (X p) + lambda p"},
+           "fused": out["fused"], "unfused_cublas": out["unfused_cublas"],
+           "speedup": round(out["unfused_cublas"]["ms_per_iteration"] / out["fused"]["ms_per_iteration"], 3)}
+    print(json.dumps(rec), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -447,12 +490,17 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rows", type=int, default=0, help="override the row count (same recipe), for profiling")
     ap.add_argument("--no-extras", action="store_true", help="skip the e2e and unfused-library legs")
+    ap.add_argument("--solver", action="store_true", help="time ridge-regression CG on the tall X instead")
     args = ap.parse_args()
 
     import inputgen
 
     rank, world, local = dist_env()
     names = sorted(WORKLOADS) if args.all else [args.workload]
+    if args.solver:
+        if rank == 0:
+            run_solver(args)
+        return
 
     if args.impl == "reference":
         if rank != 0:
