@@ -36,6 +36,7 @@ import numpy as np  # noqa: E402
 
 METRIC = "fused aX^T(v.*Xy)+bz: effective GB/s and % of GB300 HBM peak"
 FALLBACK_HBM_GBS = 6800.0
+FP64_PEAK_TFLOPS = 1.259  # 152 SMs x 2 DFMA/clk x 2 flops x 2.07 GHz
 
 def _m(kw, m):
     return dict(kw, m=m) if m else kw
@@ -149,24 +150,28 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def source_sha() -> str:
+KERNEL_SOURCES = {"dense": ["dense.cu", "common.cuh", "kernels.h"], "csr": ["csr.cu", "common.cuh", "kernels.h"]}
+
+
+def source_sha(kernel: str) -> str:
+    """Hash of the source files that define a kernel (its .cu file and the device headers it includes)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_linear_algebra_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    for fn in KERNEL_SOURCES["csr" if kernel.startswith("csr") else "dense"]:
         h.update(open(os.path.join(csrc, fn), "rb").read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(key: str):
+def profiled_traffic(kernel: str, name: str):
     """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     try:
-        d = json.load(open(path)).get(key)
+        d = json.load(open(path)).get(f"{kernel} {name}")
     except Exception:
         return None
-    if not d or d.get("source_sha") != source_sha():
+    if not d or d.get("source_sha") != source_sha(kernel):
         return None
     return d.get("dram_bytes_per_launch")
 
@@ -405,10 +410,9 @@ def run_fused(args, name, desc, p, rank, world, dist):
         e2e_ms, e2e_val = time_e2e(args, host, d, call, out, out_host, stream, ideal)
         unfused = time_unfused(args, p, d, X if p.kind == "dense" else None, out, dev, stream, ideal, ms_step)
 
-    peak, peak_kind, _ = measured_peaks()
+    peak, peak_kind, peaks = measured_peaks()
     kernel = dominant_kernel(p)
-    key = f"{kernel} {name}"
-    traffic = profiled_traffic(key)
+    traffic = profiled_traffic(kernel, name)
     achieved = ideal / (kernel_ms * 1e-3) / 1e9
     rec = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -431,6 +435,19 @@ def run_fused(args, name, desc, p, rank, world, dist):
                      "kernel": kernel},
         "unfused_library": unfused,
     }
+    if dtype_name(p) == "f64":
+        # fp64 runs on GB300's fp64 units: 2 DFMA per clock per SM (measured 1.254 TFLOP/s), and the
+        # pattern needs two FMAs (4 flops) per stored element, so the fp64 rate can bind before HBM
+        flops = 4.0 * (p.m * p.n if p.kind == "dense" else p.nnz)
+        fp64_peak = float(peaks.get("fp64_tflops", FP64_PEAK_TFLOPS))
+        rec["roofline_alu"] = {"bound": "alu", "achieved": round(flops / (kernel_ms * 1e-3) / 1e12, 4),
+                               "peak": fp64_peak, "unit": "TFLOP/s",
+                               "frac": round(flops / (kernel_ms * 1e-3) / 1e12 / fp64_peak, 4),
+                               "peak_source": "152 SMs x 2 DFMA/clk x 2 flops x 2.07 GHz (DFMA probe: 1.254)",
+                               "algorithmic_flops_per_step": flops}
+        hbm_time = ideal / (peak * 1e9)
+        alu_time = flops / (fp64_peak * 1e12)
+        rec["roofline"]["bound"] = "alu" if alu_time > hbm_time else "hbm"
     if p.kind == "csr":
         rec["config"]["nnz"] = p.nnz
     return rec
@@ -466,10 +483,11 @@ def run_solver(args):
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record()
         w, info = solvers.cg(op, rhs, tol=0.0, max_iter=iters, check_every=iters)
+        true_res = float(torch.linalg.vector_norm(rhs - op(w)) / torch.linalg.vector_norm(rhs))
         e1.record()
         torch.cuda.synchronize()
         out[name] = {"ms_per_iteration": round(e0.elapsed_time(e1) / info.iterations, 4),
-                     "relative_residual": info.residual}
+                     "relative_residual": true_res}
     rec = {"metric": "ridge regression by conjugate gradients: ms per CG iteration", "unit": "ms",
            "higher_is_better": False, "data": "synthetic",
            "config": {"workload": f"X {p.m} x {p.n} fp32 N(0,1), b = X w + 0.1 noise, lambda = 1, {iters} iterations",

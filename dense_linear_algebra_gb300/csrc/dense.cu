@@ -409,7 +409,7 @@ __global__ void __launch_bounds__(256, 1)
 // ---------------------------------------------------------------------------------------------
 // Wide kernel
 // ---------------------------------------------------------------------------------------------
-constexpr int WIDE_R = 4;        // rows coarsened per step
+constexpr int WIDE_R = 8;        // rows coarsened per step
 constexpr int WIDE_THREADS = 512;
 
 template <typename T, bool VEC>

@@ -115,7 +115,7 @@ DensePlan plan_dense(const DeviceInfo& dev, int64_t m, int64_t n, int64_t ld, in
   // wide rows
   p.kind = DENSE_WIDE;
   p.warps = 16;
-  p.rows_per_tile = 4;
+  p.rows_per_tile = 8;  // rows the wide kernel coarsens per step (WIDE_R)
   p.ctas = (int)std::max<int64_t>(1, std::min<int64_t>(dev.sm_count, cdiv(m, 8)));
   p.smem_acc = (int64_t)(n * sizeof(double)) <= budget;
   p.smem = p.smem_acc ? (size_t)n * sizeof(double) : 0;

@@ -90,7 +90,9 @@ def cg(apply, rhs, tol: float = 1e-6, max_iter: int = 100, x0=None, check_every:
         return x, info
     for k in range(max_iter):
         q = apply(p)
-        a = rs / torch.dot(p, q)
+        pq = torch.dot(p, q)
+        # once the residual is exactly zero, stop moving (no 0/0 on the device)
+        a = torch.where(pq > 0, rs / torch.where(pq > 0, pq, torch.ones_like(pq)), torch.zeros_like(pq))
         x.add_(a * p)
         r.sub_(a * q)
         rs_new = torch.dot(r, r)
@@ -102,7 +104,7 @@ def cg(apply, rhs, tol: float = 1e-6, max_iter: int = 100, x0=None, check_every:
             if res <= tol:
                 info.converged = True
                 break
-        p.mul_(rs_new / rs).add_(r)
+        p.mul_(torch.where(rs > 0, rs_new / torch.where(rs > 0, rs, torch.ones_like(rs)), torch.zeros_like(rs))).add_(r)
         rs = rs_new
     return x, info
 
