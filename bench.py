@@ -183,6 +183,18 @@ def dist_env():
     return rank, world, local
 
 
+def aggregate_over_ranks(ms_step, world, ideal_bytes, dist, device):
+    """Whole-job figures for `world` independent replicas: the slowest rank's step time
+    (max over ranks) and the bytes of every rank over it, in GB/s."""
+    if dist is not None and world > 1:
+        import torch
+
+        tt = torch.tensor([ms_step], dtype=torch.float64, device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_step = float(tt.item())
+    return ms_step, world * ideal_bytes / (ms_step * 1e-3) / 1e9
+
+
 def cpu_oracle_time(p, budget_s: float, min_reps: int = 1, max_reps: int = 5):
     """Times the oracle's double-accumulator pass (one thread) on problem p."""
     import oracle
@@ -395,11 +407,7 @@ def run_fused(args, name, desc, p, rank, world, dist):
     # consecutive launches from overlapping and add their drain time to every call
     total_ms = t_start.elapsed_time(t_end)
     ms_step = total_ms / args.steps
-    if dist:
-        tt = torch.tensor([ms_step], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_step = float(tt.item())
-    value = world * ideal / (ms_step * 1e-3) / 1e9
+    ms_step, value = aggregate_over_ranks(ms_step, world, ideal, dist, dev)
     kernel_ms = total_ms / args.steps
 
     h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)

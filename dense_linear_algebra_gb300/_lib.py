@@ -97,11 +97,12 @@ def _stream(stream, device):
     return stream.cuda_stream
 
 
-def _vec(t, dtype, length, name, device):
+def _vec(t, dtype, length, name, dev_index):
     if t is None:
         return None
-    if t.dtype != dtype or t.device != device or t.dim() != 1 or t.shape[0] != length or t.stride(0) != 1:
-        raise ValueError(f"{name}: expected a contiguous {dtype} vector of length {length} on {device}")
+    if (t.dtype is not dtype or not t.is_cuda or t.get_device() != dev_index or t.dim() != 1
+            or t.shape[0] != length or t.stride(0) != 1):
+        raise ValueError(f"{name}: expected a contiguous {dtype} vector of length {length} on cuda:{dev_index}")
     return t
 
 
@@ -116,14 +117,14 @@ def dense(X, y, v=None, alpha: float = 1.0, beta: float = 0.0, z=None, out=None,
         raise ValueError("X: expected a 2-D CUDA tensor with unit column stride")
     m, n = X.shape
     ld = X.stride(0) if m > 1 else max(n, 1)
-    dt, dev = X.dtype, X.device
-    y = _vec(y, dt, n, "y", dev)
-    v = _vec(v, dt, m, "v", dev)
-    z = _vec(z, dt, n, "z", dev)
+    dt, di = X.dtype, X.get_device()
+    y = _vec(y, dt, n, "y", di)
+    v = _vec(v, dt, m, "v", di)
+    z = _vec(z, dt, n, "z", di)
     if out is None:
-        out = torch.empty(n, dtype=dt, device=dev)
-    _vec(out, dt, n, "out", dev)
-    st = _stream(stream, dev)
+        out = torch.empty(n, dtype=dt, device=X.device)
+    _vec(out, dt, n, "out", di)
+    st = _stream(stream, X.device)
     if dt == torch.float32:
         rc = fxtx_dense_f32(m, n, _ptr(X), ld, _ptr(y), _ptr(v), alpha, beta, _ptr(z), _ptr(out), st)
     elif dt == torch.float64:
@@ -143,12 +144,13 @@ def csr(row_ptr, col_idx, vals, y, n: int, v=None, alpha: float = 1.0, beta: flo
     m = row_ptr.shape[0] - 1
     nnz = vals.shape[0]
     dt, dev = vals.dtype, vals.device
-    y = _vec(y, dt, n, "y", dev)
-    v = _vec(v, dt, m, "v", dev)
-    z = _vec(z, dt, n, "z", dev)
+    di = vals.get_device()
+    y = _vec(y, dt, n, "y", di)
+    v = _vec(v, dt, m, "v", di)
+    z = _vec(z, dt, n, "z", di)
     if out is None:
         out = torch.empty(n, dtype=dt, device=dev)
-    _vec(out, dt, n, "out", dev)
+    _vec(out, dt, n, "out", di)
     st = _stream(stream, dev)
     args = (m, n, nnz, _ptr(row_ptr), _ptr(col_idx), _ptr(vals), _ptr(y), _ptr(v), alpha, beta, _ptr(z), _ptr(out), st)
     if dt == torch.float32:

@@ -209,13 +209,25 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
   T* ys = reinterpret_cast<T*>(smem + window_bytes(win_len, sizeof(T)));
   unsigned char* scratch =
       smem + window_bytes(win_len, sizeof(T)) + window_bytes(ylen, sizeof(T)) + (size_t)warp * WARP_SCRATCH;
-  double* dotb = reinterpret_cast<double*>(scratch);          // [32] row dots of the current batch
+  double* dotb = reinterpret_cast<double*>(scratch);          // [32] row dots of the current batch (fp64)
+  float* dotf = reinterpret_cast<float*>(scratch);             // fp32: [32] sums and [32] compensations
   T* tb = reinterpret_cast<T*>(scratch + 32 * 8);              // [32] row scales alpha * v_i * u_i
   int64_t* rsb = reinterpret_cast<int64_t*>(scratch + 64 * 8);  // [33] row starts of the window
   const Window<T> win{wacc, win_c0, win_len, a.out, ys, ylen, a.y};
   const int64_t rb = a.part[blockIdx.x], re = a.part[blockIdx.x + 1];
   const T alpha = (T)a.alpha;
 
+  // adds a lane's partial dot of one row segment into the warp's row-dot buffer: fp64 through a
+  // CAS loop; fp32 as the compensated pair (sum and error term) with two native float atomics,
+  // which keeps fp64 units out of the fp32 path
+  auto flush = [&](int row, const DotAcc<T, sizeof(T) == 4>& part) {
+    if constexpr (sizeof(T) == 4) {
+      atomicAdd(&dotf[row], part.s);
+      atomicAdd(&dotf[32 + row], part.c);
+    } else {
+      smem_add_f64(&dotb[row], part.value_f64());
+    }
+  };
   window_init(win);
   dotb[lane] = 0.0;
   if (threadIdx.x == 0) s_next = (unsigned long long)rb;
@@ -280,7 +292,7 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
         if (col[k] >= 0) {
           const int64_t idx = base + k;
           while (rsb[cur + 1] <= idx) {  // rsb[b1] > idx: rows past the batch start after e
-            if (have) smem_add_f64(&dotb[cur], acc.value_f64());
+            if (have) flush(cur, acc);
             acc = DotAcc<T, sizeof(T) == 4>();
             have = false;
             ++cur;
@@ -289,13 +301,20 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
           have = true;
         }
       }
-      if (have) smem_add_f64(&dotb[cur], acc.value_f64());
+      if (have) flush(cur, acc);
       __syncwarp();
       if (lane >= b0 && lane < b1) {
-        const double u = dotb[lane];
-        dotb[lane] = 0.0;
+        T u;
+        if constexpr (sizeof(T) == 4) {
+          u = __fadd_rn(dotf[lane], dotf[32 + lane]);
+          dotf[lane] = 0.f;
+          dotf[32 + lane] = 0.f;
+        } else {
+          u = dotb[lane];
+          dotb[lane] = 0.0;
+        }
         const T vi = a.v ? ldg(a.v + r0 + lane) : T(1);
-        tb[lane] = alpha * (vi * (T)u);
+        tb[lane] = alpha * (vi * u);
       }
       __syncwarp();
       // scatter, walking the same row boundaries again

@@ -470,8 +470,19 @@ __global__ void __launch_bounds__(WIDE_THREADS) dense_wide_kernel(const DenseArg
     T t[WIDE_R];
 #pragma unroll
     for (int r = 0; r < WIDE_R; ++r) t[r] = (T)s_t[r];
-    // pass 2: the same rows again (served from L1/L2), scattered into the column accumulator
-    for (int64_t c = threadIdx.x; c < nvec; c += blockDim.x) {
+    // pass 2: the same rows again, scattered into the column accumulator. It walks the rows
+    // in the reverse of pass 1's order, so it starts on the lines pass 1 brought into L2 last
+    // and the re-read comes from L2 rather than HBM as far as L2 holds the CTAs' rows.
+    for (int64_t j = nvec * NV + threadIdx.x; j < n; j += blockDim.x) {
+      T s = T(0);
+#pragma unroll
+      for (int r = 0; r < WIDE_R; ++r)
+        if (r < rows) s = fma(t[r], a.X[(i0 + r) * ld + j], s);
+      acc[j] += (double)s;
+    }
+    const int64_t nk = threadIdx.x < nvec ? (nvec - 1 - threadIdx.x) / blockDim.x + 1 : 0;
+    for (int64_t kk = nk - 1; kk >= 0; --kk) {
+      const int64_t c = threadIdx.x + kk * blockDim.x;
       T s[NV];
 #pragma unroll
       for (int e = 0; e < NV; ++e) s[e] = T(0);
@@ -486,13 +497,6 @@ __global__ void __launch_bounds__(WIDE_THREADS) dense_wide_kernel(const DenseArg
       }
 #pragma unroll
       for (int e = 0; e < NV; ++e) acc[c * NV + e] += (double)s[e];
-    }
-    for (int64_t j = nvec * NV + threadIdx.x; j < n; j += blockDim.x) {
-      T s = T(0);
-#pragma unroll
-      for (int r = 0; r < WIDE_R; ++r)
-        if (r < rows) s = fma(t[r], a.X[(i0 + r) * ld + j], s);
-      acc[j] += (double)s;
     }
     __syncthreads();  // s_dot / s_t reuse
   }

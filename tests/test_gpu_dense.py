@@ -190,3 +190,22 @@ def test_full_size_wide_sampled():
     cols = np.unique(np.concatenate([[0, 1, p.n - 1], np.random.default_rng(0).integers(0, p.n, 45)]))
     ref, S = oracle.solve(p, cols=cols)
     assert_within_bound(got[cols], ref, S, 1e-12, "dense_wide")
+
+
+def test_allocation_failure_is_reported():
+    """FXTX_FAIL_ALLOC=1 makes the workspace allocation fail on the host: the call returns
+    FXTX_ERR_ALLOC without launching, and the next call (hook off) works."""
+    import os
+
+    X = torch.rand(1000, 32, device="cuda")
+    y = torch.rand(32, device="cuda")
+    os.environ["FXTX_FAIL_ALLOC"] = "1"
+    try:
+        with pytest.raises(fx.FxtxError) as ei:
+            fx.dense(X, y)
+        assert ei.value.status == fx.FXTX_ERR_ALLOC
+    finally:
+        del os.environ["FXTX_FAIL_ALLOC"]
+    out = fx.dense(X, y)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all() and fx.device_error() == fx.FXTX_OK
