@@ -51,6 +51,9 @@ WORKLOADS = {
                      lambda g, m=None: g.dense_tall(**_m({"variant": "b"}, m))),
     "dense_tall_c": ("dense f32 16,000,000 x 32, N(0,1) X/y, v=1 (X^T X y), alpha=1, beta=0",
                      lambda g, m=None: g.dense_tall(**_m({"variant": "c"}, m))),
+    "dense_tall_bf16": ("dense 16,000,000 x 32 with X in bfloat16, fp32 vectors and arithmetic, N(0,1) X/y/z, "
+                        "v U[0.1,2], alpha=2, beta=-1",
+                        lambda g, m=None: g.dense_tall(**_m({"variant": "b", "x_store": "bf16"}, m))),
     "dense_wide": ("dense f64 20,000 x 20,000, U[-1,1], alpha=0.7, beta=0.3",
                    lambda g, m=None: g.dense_wide(**_m({}, m))),
     "csr_uniform": ("CSR f64 4,000,000 x 10,000, Poisson(50) uniform distinct columns, U[-1,1], alpha=beta=1",
@@ -65,6 +68,8 @@ def dominant_kernel(p) -> str:
     """The kernel that carries the call, from the launch plan the library picks."""
     import dense_linear_algebra_gb300 as fx
 
+    if p.x_store == "bf16":
+        return "dense_tile_kernel"
     if p.kind == "csr":
         # rows longer than 256 entries go to the long-row kernel; it dominates when they hold most entries
         lens = np.diff(p.row_ptr)
@@ -247,6 +252,8 @@ def run_reference(args, name, desc, p):
 
 
 def dtype_name(p):
+    if p.x_store == "bf16":
+        return "bf16 X, f32"
     return "f32" if np.dtype(p.dtype) == np.float32 else "f64"
 
 
@@ -284,6 +291,8 @@ def time_unfused(args, p, d, X, out, dev, stream, ideal, ms_step):
     import torch
 
     # the unfused library sequence on the same GPU (dense: cuBLAS gemv, scale, transposed gemv)
+    if p.x_store == "bf16":
+        return {"error": "no library gemv takes bfloat16 X with fp32 vectors and fp32 accumulation"}
     if p.kind == "dense":
         try:
             Xt = X
@@ -355,6 +364,8 @@ def run_fused(args, name, desc, p, rank, world, dist):
     host = {}
     if p.kind == "dense":
         host["X"] = pin(p.X)
+        if p.x_store == "bf16":  # bfloat16-representable values: exact
+            host["X"] = host["X"].to(torch.bfloat16).pin_memory()
     else:
         host["row_ptr"], host["col_idx"], host["vals"] = pin(p.row_ptr), pin(p.col_idx), pin(p.vals)
     host["y"], host["v"], host["z"] = pin(p.y), pin(p.v), pin(p.z)

@@ -7,7 +7,7 @@ CUDA kernels of ``libfusedxtx.so`` (sources in ``csrc/``, C ABI in
 fallback: if the library cannot be loaded, importing the binding fails.
 
 Raw C-ABI calls (pointers as ints, stream as a cudaStream_t int) carry the C names:
-``fxtx_dense_f32``, ``fxtx_dense_f64``, ``fxtx_dense_f32_noalloc``, ``fxtx_csr_f32``, ``fxtx_csr_f64``,
+``fxtx_dense_f32``, ``fxtx_dense_f64``, ``fxtx_dense_bf16``, ``fxtx_dense_f32_noalloc``, ``fxtx_csr_f32``, ``fxtx_csr_f64``,
 ``fxtx_csr_validate``, ``fxtx_device_error``, ``fxtx_status_string``,
 ``fxtx_plan_describe``. ``dense`` and ``csr`` take torch CUDA tensors.
 """
@@ -30,6 +30,7 @@ from ._lib import (  # noqa: F401
     fxtx_csr_validate,
     fxtx_dense_f32,
     fxtx_dense_f32_noalloc,
+    fxtx_dense_bf16,
     fxtx_dense_f64,
     fxtx_device_error,
     fxtx_plan_describe,

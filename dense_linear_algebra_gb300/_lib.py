@@ -28,6 +28,7 @@ def _load() -> ctypes.CDLL:
     lib.fxtx_dense_f32.argtypes = [i64, i64, vp, i64, vp, vp, f32, f32, vp, vp, vp]
     lib.fxtx_dense_f64.argtypes = [i64, i64, vp, i64, vp, vp, f64, f64, vp, vp, vp]
     lib.fxtx_dense_f32_noalloc.argtypes = [i64, i64, vp, i64, vp, vp, f32, f32, vp, vp, vp]
+    lib.fxtx_dense_bf16.argtypes = [i64, i64, vp, i64, vp, vp, f32, f32, vp, vp, vp]
     lib.fxtx_csr_f32.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, f32, f32, vp, vp, vp]
     lib.fxtx_csr_f64.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, f64, f64, vp, vp, vp]
     lib.fxtx_csr_validate.argtypes = [i64, i64, i64, vp, vp, vp]
@@ -35,7 +36,7 @@ def _load() -> ctypes.CDLL:
     lib.fxtx_status_string.argtypes = [i32]
     lib.fxtx_status_string.restype = ctypes.c_char_p
     lib.fxtx_plan_describe.argtypes = [i32, i32, i64, i64, i64, i64, ctypes.c_char_p, i64]
-    for name in ("fxtx_dense_f32", "fxtx_dense_f64", "fxtx_dense_f32_noalloc", "fxtx_csr_f32", "fxtx_csr_f64", "fxtx_csr_validate",
+    for name in ("fxtx_dense_f32", "fxtx_dense_f64", "fxtx_dense_f32_noalloc", "fxtx_dense_bf16", "fxtx_csr_f32", "fxtx_csr_f64", "fxtx_csr_validate",
                  "fxtx_device_error", "fxtx_plan_describe"):
         getattr(lib, name).restype = i32
     return lib
@@ -47,6 +48,7 @@ library_path = _build.LIB
 fxtx_dense_f32 = _lib.fxtx_dense_f32
 fxtx_dense_f64 = _lib.fxtx_dense_f64
 fxtx_dense_f32_noalloc = _lib.fxtx_dense_f32_noalloc
+fxtx_dense_bf16 = _lib.fxtx_dense_bf16
 fxtx_csr_f32 = _lib.fxtx_csr_f32
 fxtx_csr_f64 = _lib.fxtx_csr_f64
 fxtx_csr_validate = _lib.fxtx_csr_validate
@@ -109,6 +111,9 @@ def _vec(t, dtype, length, name, dev_index):
 def dense(X, y, v=None, alpha: float = 1.0, beta: float = 0.0, z=None, out=None, stream=None):
     """out = alpha * X^T (v * (X y)) + beta * z for a row-major CUDA tensor X (m, n), X.stride(1) == 1.
 
+    X may be float32, float64 or bfloat16; for bfloat16 X the vectors are float32 and the
+    arithmetic is fp32.
+
     ``v=None`` means v = 1; ``z=None`` (or beta = 0) drops the beta z term. A column slice of a
     wider matrix is accepted: its row stride is passed as the leading dimension.
     """
@@ -117,7 +122,8 @@ def dense(X, y, v=None, alpha: float = 1.0, beta: float = 0.0, z=None, out=None,
         raise ValueError("X: expected a 2-D CUDA tensor with unit column stride")
     m, n = X.shape
     ld = X.stride(0) if m > 1 else max(n, 1)
-    dt, di = X.dtype, X.get_device()
+    # bfloat16 X computes in fp32: y, v, z and out are float32
+    dt, di = (torch.float32 if X.dtype == torch.bfloat16 else X.dtype), X.get_device()
     y = _vec(y, dt, n, "y", di)
     v = _vec(v, dt, m, "v", di)
     z = _vec(z, dt, n, "z", di)
@@ -125,7 +131,9 @@ def dense(X, y, v=None, alpha: float = 1.0, beta: float = 0.0, z=None, out=None,
         out = torch.empty(n, dtype=dt, device=X.device)
     _vec(out, dt, n, "out", di)
     st = _stream(stream, X.device)
-    if dt == torch.float32:
+    if X.dtype == torch.bfloat16:
+        rc = fxtx_dense_bf16(m, n, _ptr(X), ld, _ptr(y), _ptr(v), alpha, beta, _ptr(z), _ptr(out), st)
+    elif dt == torch.float32:
         rc = fxtx_dense_f32(m, n, _ptr(X), ld, _ptr(y), _ptr(v), alpha, beta, _ptr(z), _ptr(out), st)
     elif dt == torch.float64:
         rc = fxtx_dense_f64(m, n, _ptr(X), ld, _ptr(y), _ptr(v), alpha, beta, _ptr(z), _ptr(out), st)

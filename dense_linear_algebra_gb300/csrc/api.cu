@@ -121,6 +121,52 @@ fxtx_status_t dense_impl(int64_t m, int64_t n, const T* X, int64_t ld, const T* 
   return FXTX_OK;
 }
 
+// bfloat16 X, fp32 everything else and fp32 arithmetic.
+fxtx_status_t dense_bf16_impl(int64_t m, int64_t n, const __nv_bfloat16* X, int64_t ld, const float* y,
+                              const float* v, float alpha, float beta, const float* z, float* out, void* stream) {
+  if (m < 0 || n < 0) return FXTX_ERR_INVALID_ARG;
+  if (n == 0) return FXTX_OK;
+  if (ld < n || y == nullptr || out == nullptr) return FXTX_ERR_INVALID_ARG;
+  if (m > 0 && X == nullptr) return FXTX_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  fxtx_status_t s = current_device(&dev);
+  if (s != FXTX_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool tile_ok = aligned16(X) && (ld * 2) % 16 == 0;
+  const DensePlan plan = plan_dense(*dev, m, n, ld, 2, false, tile_ok);
+  if (plan.kind == DENSE_WIDE || plan.kind == DENSE_NARROW_TMA) return FXTX_ERR_UNSUPPORTED;  // n > 512
+  if (log_enabled()) {
+    char buf[256];
+    describe(plan, buf, sizeof buf);
+    fprintf(stderr, "[fxtx] bf16 m=%lld n=%lld ld=%lld %s\n", (long long)m, (long long)n, (long long)ld, buf);
+  }
+  DenseArgs<float, __nv_bfloat16> a;
+  a.m = m; a.n = n; a.ld = ld;
+  a.X = X; a.y = y; a.v = v; a.z = z; a.out = out;
+  a.alpha = (double)alpha; a.beta = (double)beta;
+  a.use_z = (z != nullptr && beta != 0.0f);
+  a.tiles = plan.rows_per_tile > 0 ? (m + plan.rows_per_tile - 1) / plan.rows_per_tile : 0;
+  void* ws = nullptr;
+  s = alloc_ws(&ws, plan.ws_bytes, st);
+  if (s != FXTX_OK) return s;
+  if (ws) {
+    a.ws = static_cast<double*>(ws);
+    a.ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + plan.ws_bytes - 128);
+    if (cudaMemsetAsync(a.ticket, 0, sizeof(unsigned), st) != cudaSuccess) {
+      cudaGetLastError();
+      cudaFreeAsync(ws, st);
+      return FXTX_ERR_CUDA;
+    }
+  }
+  cudaError_t e = launch_dense_bf16(plan, a, st);
+  if (ws) cudaFreeAsync(ws, st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FXTX_ERR_CUDA;
+  }
+  return FXTX_OK;
+}
+
 template <typename T>
 fxtx_status_t csr_impl(int64_t m, int64_t n, int64_t nnz, const int64_t* row_ptr, const int32_t* col_idx,
                        const T* vals, const T* y, const T* v, T alpha, T beta, const T* z, T* out, void* stream) {
@@ -182,6 +228,11 @@ fxtx_status_t fxtx_dense_f64(int64_t m, int64_t n, const double* X, int64_t ld, 
   return dense_impl<double>(m, n, X, ld, y, v, alpha, beta, z, out, stream);
 }
 
+fxtx_status_t fxtx_dense_bf16(int64_t m, int64_t n, const uint16_t* X, int64_t ld, const float* y, const float* v,
+                              float alpha, float beta, const float* z, float* out, void* stream) {
+  return dense_bf16_impl(m, n, reinterpret_cast<const __nv_bfloat16*>(X), ld, y, v, alpha, beta, z, out, stream);
+}
+
 fxtx_status_t fxtx_csr_f32(int64_t m, int64_t n, int64_t nnz, const int64_t* row_ptr, const int32_t* col_idx,
                            const float* vals, const float* y, const float* v, float alpha, float beta, const float* z,
                            float* out, void* stream) {
@@ -237,7 +288,8 @@ const char* fxtx_status_string(fxtx_status_t status) {
   switch (status) {
     case FXTX_OK: return "FXTX_OK";
     case FXTX_ERR_INVALID_ARG: return "FXTX_ERR_INVALID_ARG: invalid argument";
-    case FXTX_ERR_UNSUPPORTED: return "FXTX_ERR_UNSUPPORTED: no compute capability 10.3 device is current";
+    case FXTX_ERR_UNSUPPORTED:
+      return "FXTX_ERR_UNSUPPORTED: no compute capability 10.3 device is current, or a shape this entry does not take";
     case FXTX_ERR_CUDA: return "FXTX_ERR_CUDA: a CUDA call failed while enqueueing";
     case FXTX_ERR_ALLOC: return "FXTX_ERR_ALLOC: workspace allocation failed";
     case FXTX_ERR_BAD_CSR: return "FXTX_ERR_BAD_CSR: malformed CSR structure";

@@ -40,8 +40,8 @@ __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + 
 // red[w][j] holds warp w's partial of column j. Sums them into the CTA partial,
 // stores it in ws[blockIdx.x], and lets the last CTA to take a ticket sum all
 // CTA partials in a fixed order and write out = alpha * w + beta * z.
-template <typename T>
-__device__ __forceinline__ void finish_from_red(const DenseArgs<T>& a, double* red, const int nw) {
+template <typename T, typename TX>
+__device__ __forceinline__ void finish_from_red(const DenseArgs<T, TX>& a, double* red, const int nw) {
   __shared__ unsigned s_last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t n = a.n;
@@ -75,11 +75,20 @@ __device__ __forceinline__ void finish_from_red(const DenseArgs<T>& a, double* r
   if (threadIdx.x == 0) *a.ticket = 0u;
 }
 
+// One element of X in the compute type (bfloat16 widens exactly: its bits are the top
+// half of the fp32 pattern).
+__device__ __forceinline__ float load_x(const float* p) { return ldg(p); }
+__device__ __forceinline__ double load_x(const double* p) { return ldg(p); }
+__device__ __forceinline__ float load_x(const __nv_bfloat16* p) {
+  return __uint_as_float((unsigned)__ldg(reinterpret_cast<const unsigned short*>(p)) << 16);
+}
+
 // ---------------------------------------------------------------------------------------------
 // Narrow kernel (short rows, or X that the tensor copies cannot address)
 // ---------------------------------------------------------------------------------------------
-template <typename T, int LPR, int VPL, bool TMA>
-__global__ void __launch_bounds__(512) dense_narrow_kernel(const DenseArgs<T> a, const int R, const int S) {
+template <typename T, int LPR, int VPL, bool TMA, typename TX = T>
+__global__ void __launch_bounds__(512) dense_narrow_kernel(const DenseArgs<T, TX> a, const int R, const int S) {
+  static_assert(!TMA || sizeof(TX) == sizeof(T), "bulk-copied rows are read in the compute type");
   using VT = typename Vec16<T>::type;
   constexpr int NV = Vec16<T>::N;  // elements per 16-byte chunk
   constexpr int G = 32 / LPR;      // rows per warp pass
@@ -154,7 +163,8 @@ __global__ void __launch_bounds__(512) dense_narrow_kernel(const DenseArgs<T> a,
     const T vcur = vnext;
     if (k + 1 < nt) vnext = load_v(tile + 1);
     const int s = (int)(k % S);
-    const T* tx;
+    const T* tx = nullptr;    // the tile in shared memory (bulk-copied path)
+    const TX* txg = nullptr;  // the tile in global memory (direct path)
     if constexpr (TMA) {
       const bool ok = mbar_wait_bounded(&bars[s], (uint32_t)((k / S) & 1));
       if (__any_sync(FULL_MASK, !ok)) {
@@ -165,7 +175,7 @@ __global__ void __launch_bounds__(512) dense_narrow_kernel(const DenseArgs<T> a,
       }
       tx = reinterpret_cast<const T*>(stages + (size_t)s * stage_bytes);
     } else {
-      tx = a.X + row0 * a.ld;
+      txg = a.X + row0 * a.ld;
     }
 
     T tacc[C];
@@ -175,7 +185,8 @@ __global__ void __launch_bounds__(512) dense_narrow_kernel(const DenseArgs<T> a,
     for (int r0 = 0; r0 < rows; r0 += G) {
       const int r = r0 + g;
       const bool valid = r < rows;
-      const T* rowp = tx + (int64_t)r * pitch;
+      const T* rowp = TMA ? tx + (int64_t)r * pitch : nullptr;
+      const TX* rowg = TMA ? nullptr : txg + (int64_t)r * pitch;
       T x[C];
 #pragma unroll
       for (int k2 = 0; k2 < VPL; ++k2) {
@@ -190,7 +201,7 @@ __global__ void __launch_bounds__(512) dense_narrow_kernel(const DenseArgs<T> a,
           }
         } else {
 #pragma unroll
-          for (int e = 0; e < NV; ++e) x[k2 * NV + e] = (valid && c0 + e < n) ? ldg(rowp + c0 + e) : T(0);
+          for (int e = 0; e < NV; ++e) x[k2 * NV + e] = (valid && c0 + e < n) ? load_x(rowg + c0 + e) : T(0);
         }
       }
       DotAcc<T, COMP> dacc;
@@ -247,41 +258,106 @@ __global__ void __launch_bounds__(512) dense_narrow_kernel(const DenseArgs<T> a,
 // c of row r at chunk position c ^ (r mod 8). chunk_of() assigns chunks so that
 // the 8 lanes of every quarter-warp read 8 distinct bank groups. Rows past m and
 // columns past n arrive as zeros, so the inner loop needs no masks.
-template <int LPR>
+template <int LPR, int CPL, int BW>
 __device__ __forceinline__ void chunk_of(int q, int j, int& b, int& c) {
-  if (LPR == 2) {
+  if (BW == 64) {  // one 64-byte block: LPR 1 (CPL 4) or LPR 2 (CPL 2)
+    b = 0;
+    c = LPR == 1 ? j : 2 * q + j;
+  } else if (LPR == 2) {  // CPL 4, one block
     b = 0;
     c = 4 * q + j;
-  } else if (LPR == 4) {
+  } else if (LPR == 4 && CPL == 4) {
     b = j >> 1;
     c = 2 * q + (j & 1);
+  } else if (LPR == 4) {  // CPL 2, one block
+    b = 0;
+    c = 2 * q + j;
   } else {
     b = (q >> 3) + j * (LPR / 8);
     c = q & 7;
   }
 }
 
-template <int NB>
-struct TileShape {
-  static constexpr int LPR = 2 * NB;             // lanes per row
-  static constexpr int G = 32 / LPR;              // rows per warp pass
-  static constexpr int R = NB >= 8 ? 8 : 64 / NB;  // rows per tile (a multiple of 8)
-  static constexpr int P = R / G;                 // passes per tile
-  static constexpr int BOX = R * 128;             // bytes of one column block of a tile
-  static constexpr int TILE = NB * BOX;           // bytes of one pipeline stage
+// Byte offset of chunk c of tile row r inside its box. The 128-byte swizzle stores
+// chunk c of row r at chunk c ^ (r mod 8); the 64-byte swizzle (rows of 64 bytes) at
+// c ^ ((r / 2) mod 4).
+template <int BW>
+__device__ __forceinline__ int swizzled(int r, int c) {
+  return BW == 128 ? r * 128 + ((c ^ (r & 7)) << 4) : r * 64 + ((c ^ ((r >> 1) & 3)) << 4);
+}
+
+// What the tile kernel needs to know about X's storage type: elements per 16-byte
+// chunk, the compute type, the tensor-map data type, and the unpacking of a chunk.
+template <typename TX>
+struct Store;
+template <>
+struct Store<float> {
+  using T = float;
+  static constexpr int NV = 4;
+  static constexpr CUtensorMapDataType MAP = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  __device__ static __forceinline__ void unpack(const uint4& u, float* e) {
+    e[0] = __uint_as_float(u.x); e[1] = __uint_as_float(u.y); e[2] = __uint_as_float(u.z); e[3] = __uint_as_float(u.w);
+  }
+};
+template <>
+struct Store<double> {
+  using T = double;
+  static constexpr int NV = 2;
+  static constexpr CUtensorMapDataType MAP = CU_TENSOR_MAP_DATA_TYPE_FLOAT64;
+  __device__ static __forceinline__ void unpack(const uint4& u, double* e) {
+    e[0] = __hiloint2double((int)u.y, (int)u.x);
+    e[1] = __hiloint2double((int)u.w, (int)u.z);
+  }
+};
+template <>
+struct Store<__nv_bfloat16> {
+  using T = float;
+  static constexpr int NV = 8;
+  static constexpr CUtensorMapDataType MAP = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  // each 32-bit word holds two bfloat16, the lower-addressed one in its low half
+  __device__ static __forceinline__ void unpack(const uint4& u, float* e) {
+    const unsigned w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      e[2 * i] = __uint_as_float(w[i] << 16);
+      e[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
 };
 
-template <typename T, int NB>
+// Tile geometry for rows of NB blocks of BW bytes (BW = 128, or 64 for rows of at
+// most 64 bytes) and CPL chunks per lane. A tile is 8 KB (16 KB at NB = 16).
+template <int NB, int CPL, int BW = 128>
+struct TileShape {
+  static constexpr int CPB = BW / 16;                                      // chunks per block
+  static constexpr int LPR = CPB * NB / CPL;                               // lanes per row
+  static constexpr int G = 32 / LPR;                                       // rows per warp pass
+  static constexpr int R = BW == 64 ? 128 : (NB >= 8 ? 8 : 64 / NB);       // rows per tile (multiple of 8)
+  static constexpr int P = R / G;                                          // passes per tile
+  static constexpr int BOX = R * BW;                                       // bytes of one column block of a tile
+  static constexpr int TILE = NB * BOX;                                    // bytes of one pipeline stage
+};
+
+// chunks per lane: four for 4- and 8-byte elements, two for bfloat16 (16 columns either way)
+template <typename TX>
+__host__ __device__ constexpr int tile_cpl() {
+  return sizeof(TX) == 2 ? 2 : 4;
+}
+
+template <typename TX, int NB, int BW>
 __global__ void __launch_bounds__(256, 1)
-    dense_tile_kernel(const __grid_constant__ CUtensorMap tmap, const DenseArgs<T> a, const int nbr, const int S) {
-  using VT = typename Vec16<T>::type;
-  using SH = TileShape<NB>;
-  constexpr int NV = Vec16<T>::N;
+    dense_tile_kernel(const __grid_constant__ CUtensorMap tmap, const DenseArgs<typename Store<TX>::T, TX> a,
+                      const int nbr, const int S) {
+  using T = typename Store<TX>::T;
+  constexpr int CPL = tile_cpl<TX>();
+  using SH = TileShape<NB, CPL, BW>;
+  constexpr int NV = Store<TX>::NV;  // elements per 16-byte chunk
+  constexpr int CPB = SH::CPB;
   constexpr int LPR = SH::LPR, G = SH::G, R = SH::R, P = SH::P, BOX = SH::BOX, TILE = SH::TILE;
-  constexpr int CPL = 4, C = CPL * NV;  // chunks and columns per lane
+  constexpr int C = CPL * NV;            // columns per lane
   constexpr int VR = (R + 31) / 32;      // registers holding the tile's v
   // fp32 rows longer than 64 entries take the compensated dot
-  constexpr bool COMP = sizeof(T) == 4 && NB >= 4;
+  constexpr bool COMP = sizeof(T) == 4 && NB * CPB * NV > 64;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -294,8 +370,8 @@ __global__ void __launch_bounds__(256, 1)
   T yr[C];
 #pragma unroll
   for (int j = 0; j < CPL; ++j) {
-    chunk_of<LPR>(q, j, cb[j], cc[j]);
-    const int64_t col0 = ((int64_t)cb[j] * 8 + cc[j]) * NV;
+    chunk_of<LPR, CPL, BW>(q, j, cb[j], cc[j]);
+    const int64_t col0 = ((int64_t)cb[j] * CPB + cc[j]) * NV;
     okc[j] = cb[j] < nbr && col0 < n;
 #pragma unroll
     for (int e = 0; e < NV; ++e) yr[j * NV + e] = (okc[j] && col0 + e < n) ? ldg(a.y + col0 + e) : T(0);
@@ -311,7 +387,7 @@ __global__ void __launch_bounds__(256, 1)
     if (lane == 0) mbar_arrive_expect_tx(&bars[s], (uint32_t)(nbr * BOX));
     __syncwarp();
     if (lane < nbr)
-      tma_load_2d(stages + (size_t)s * TILE + lane * BOX, &tmap, lane * (128 / (int)sizeof(T)), (int)(tile * R),
+      tma_load_2d(stages + (size_t)s * TILE + lane * BOX, &tmap, lane * (BW / (int)sizeof(TX)), (int)(tile * R),
                   &bars[s], pol);
   };
   auto load_v = [&](int64_t tile, T* vv) {
@@ -353,24 +429,33 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
     for (int p = 0; p < P; ++p) {
       const int r = p * G + g;
-      const unsigned char* rowp = stage + r * 128;
       T x[C];
 #pragma unroll
       for (int j = 0; j < CPL; ++j) {
         if (okc[j]) {
-          const VT vv = *reinterpret_cast<const VT*>(rowp + cb[j] * BOX + ((cc[j] ^ (r & 7)) << 4));
-          unpack<T>(vv, &x[j * NV]);
+          const uint4 u = *reinterpret_cast<const uint4*>(stage + cb[j] * BOX + swizzled<BW>(r, cc[j]));
+          Store<TX>::unpack(u, &x[j * NV]);
         } else {
 #pragma unroll
           for (int e = 0; e < NV; ++e) x[j * NV + e] = T(0);
         }
       }
-      DotAcc<T, COMP> dacc;
+      T dsum;
+      if constexpr (COMP) {
+        DotAcc<T, true> dacc;
 #pragma unroll
-      for (int c = 0; c < C; ++c) dacc.add(x[c], yr[c]);
-      dacc.template group_reduce<LPR>();
+        for (int c = 0; c < C; ++c) dacc.add(x[c], yr[c]);
+        dacc.template group_reduce<LPR>();
+        dsum = dacc.value();
+      } else {
+        // four independent partial sums: a chain of C/4 FMAs instead of C
+        T d4[4] = {T(0), T(0), T(0), T(0)};
+#pragma unroll
+        for (int c = 0; c < C; ++c) d4[c & 3] = fma(x[c], yr[c], d4[c & 3]);
+        dsum = group_sum<LPR>((d4[0] + d4[1]) + (d4[2] + d4[3]));
+      }
       const T vi = a.v ? __shfl_sync(FULL_MASK, vcur[(p * G) / 32], (p * G + g) & 31) : T(1);
-      const T t = vi * dacc.value();
+      const T t = vi * dsum;
 #pragma unroll
       for (int c = 0; c < C; ++c) tacc[c] = fma(t, x[c], tacc[c]);
     }
@@ -399,7 +484,7 @@ __global__ void __launch_bounds__(256, 1)
     for (int j = 0; j < CPL; ++j)
 #pragma unroll
       for (int e = 0; e < NV; ++e) {
-        const int64_t col = ((int64_t)cb[j] * 8 + cc[j]) * NV + e;
+        const int64_t col = ((int64_t)cb[j] * CPB + cc[j]) * NV + e;
         if (okc[j] && col < n) red[warp * n + col] = part[j * NV + e];
       }
   }
@@ -591,39 +676,44 @@ static EncodeTiledFn encode_tiled() {
   return fn;
 }
 
-// Tensor map of X (n columns, m rows, row pitch ld) in boxes of rows x 128 bytes, 128-byte swizzle.
-template <typename T>
-static bool encode_x_map(CUtensorMap* map, const T* X, int64_t m, int64_t n, int64_t ld, int rows) {
+// Tensor map of X (n columns, m rows, row pitch ld) in boxes of rows x bw bytes, with the
+// swizzle of the same width (bw = 128 or 64).
+template <typename TX>
+static bool encode_x_map(CUtensorMap* map, const TX* X, int64_t m, int64_t n, int64_t ld, int rows, int bw) {
   EncodeTiledFn fn = encode_tiled();
   if (!fn) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)n, (cuuint64_t)m};
-  const cuuint64_t strides[1] = {(cuuint64_t)(ld * (int64_t)sizeof(T))};
-  const cuuint32_t box[2] = {(cuuint32_t)(128 / sizeof(T)), (cuuint32_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)(ld * (int64_t)sizeof(TX))};
+  const cuuint32_t box[2] = {(cuuint32_t)(bw / sizeof(TX)), (cuuint32_t)rows};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = fn(map, sizeof(T) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT64, 2,
-                        const_cast<T*>(X), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = fn(map, Store<TX>::MAP, 2, const_cast<TX*>(X), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, bw == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-template <typename T, int NB>
-static cudaError_t launch_tile_nb(const DensePlan& p, const CUtensorMap& map, const DenseArgs<T>& a, cudaStream_t st) {
-  cudaError_t e = ensure_smem((const void*)dense_tile_kernel<T, NB>, p.smem);
+template <typename TX, int NB, int BW = 128>
+static cudaError_t launch_tile_nb(const DensePlan& p, const CUtensorMap& map,
+                                  const DenseArgs<typename Store<TX>::T, TX>& a, cudaStream_t st) {
+  cudaError_t e = ensure_smem((const void*)dense_tile_kernel<TX, NB, BW>, p.smem);
   if (e != cudaSuccess) return e;
-  dense_tile_kernel<T, NB><<<p.ctas, p.warps * 32, p.smem, st>>>(map, a, p.nbr, p.stages);
+  dense_tile_kernel<TX, NB, BW><<<p.ctas, p.warps * 32, p.smem, st>>>(map, a, p.nbr, p.stages);
   return cudaGetLastError();
 }
 
-template <typename T>
-static cudaError_t launch_tile(const DensePlan& p, const DenseArgs<T>& a, cudaStream_t st) {
+template <typename TX>
+static cudaError_t launch_tile(const DensePlan& p, const DenseArgs<typename Store<TX>::T, TX>& a, cudaStream_t st) {
   CUtensorMap map;
-  if (!encode_x_map<T>(&map, a.X, a.m, a.n, a.ld, p.rows_per_tile)) return cudaErrorInvalidValue;
+  if (!encode_x_map<TX>(&map, a.X, a.m, a.n, a.ld, p.rows_per_tile, p.box_bytes)) return cudaErrorInvalidValue;
+  if (p.box_bytes == 64) return launch_tile_nb<TX, 1, 64>(p, map, a, st);
   switch (p.nb) {
-    case 1: return launch_tile_nb<T, 1>(p, map, a, st);
-    case 2: return launch_tile_nb<T, 2>(p, map, a, st);
-    case 4: return launch_tile_nb<T, 4>(p, map, a, st);
-    case 8: return launch_tile_nb<T, 8>(p, map, a, st);
-    case 16: return launch_tile_nb<T, 16>(p, map, a, st);
+    case 1: return launch_tile_nb<TX, 1>(p, map, a, st);
+    case 2: return launch_tile_nb<TX, 2>(p, map, a, st);
+    case 4: return launch_tile_nb<TX, 4>(p, map, a, st);
+    case 8: return launch_tile_nb<TX, 8>(p, map, a, st);
+    case 16:
+      if constexpr (tile_cpl<TX>() == 4) return launch_tile_nb<TX, 16>(p, map, a, st);
+      return cudaErrorInvalidConfiguration;
     default: return cudaErrorInvalidConfiguration;
   }
 }
@@ -672,6 +762,45 @@ cudaError_t launch_dense(const DensePlan& p, const DenseArgs<T>& a, cudaStream_t
     }
   }
   return cudaErrorInvalidConfiguration;
+}
+
+cudaError_t launch_dense_bf16(const DensePlan& p, const DenseArgs<float, __nv_bfloat16>& a, cudaStream_t st) {
+  switch (p.kind) {
+    case DENSE_NOOP:
+      return cudaSuccess;
+    case DENSE_EMPTY_ROWS: {
+      DenseArgs<float> e;
+      e.n = a.n; e.z = a.z; e.out = a.out; e.beta = a.beta; e.use_z = a.use_z;
+      const int blocks = (int)std::min<int64_t>((a.n + 255) / 256, 4096);
+      empty_rows_kernel<float><<<blocks, 256, 0, st>>>(e);
+      return cudaGetLastError();
+    }
+    case DENSE_TILE_TMA:
+      return launch_tile<__nv_bfloat16>(p, a, st);
+    case DENSE_NARROW_DIRECT: {
+      const int key = p.lpr * 8 + p.vpl;
+      auto go = [&](auto kernel) -> cudaError_t {
+        cudaError_t e = ensure_smem((const void*)kernel, p.smem);
+        if (e != cudaSuccess) return e;
+        kernel<<<p.ctas, p.warps * 32, p.smem, st>>>(a, p.rows_per_tile, 1);
+        return cudaGetLastError();
+      };
+      using B = __nv_bfloat16;
+      switch (key) {
+        case 1 * 8 + 1: return go(dense_narrow_kernel<float, 1, 1, false, B>);
+        case 2 * 8 + 1: return go(dense_narrow_kernel<float, 2, 1, false, B>);
+        case 4 * 8 + 1: return go(dense_narrow_kernel<float, 4, 1, false, B>);
+        case 8 * 8 + 1: return go(dense_narrow_kernel<float, 8, 1, false, B>);
+        case 8 * 8 + 2: return go(dense_narrow_kernel<float, 8, 2, false, B>);
+        case 8 * 8 + 4: return go(dense_narrow_kernel<float, 8, 4, false, B>);
+        case 16 * 8 + 4: return go(dense_narrow_kernel<float, 16, 4, false, B>);
+        case 32 * 8 + 4: return go(dense_narrow_kernel<float, 32, 4, false, B>);
+        default: return cudaErrorInvalidConfiguration;
+      }
+    }
+    default:
+      return cudaErrorInvalidConfiguration;  // wide rows are not offered for bfloat16 X
+  }
 }
 
 template cudaError_t launch_dense<float>(const DensePlan&, const DenseArgs<float>&, cudaStream_t);

@@ -2,17 +2,19 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "plan.h"
 
 namespace fxtx {
 
-// One dense call. alpha and beta are carried in double (exact for float).
-template <typename T>
+// One dense call. T is the compute type of y, v, z and out; TX the storage type of X
+// (T itself, or bfloat16 with T = float). alpha and beta are carried in double.
+template <typename T, typename TX = T>
 struct DenseArgs {
   int64_t m = 0, n = 0, ld = 0;
-  const T* X = nullptr;
+  const TX* X = nullptr;
   const T* y = nullptr;
   const T* v = nullptr;  // NULL: v_i = 1
   const T* z = nullptr;  // read only when use_z
@@ -26,6 +28,9 @@ struct DenseArgs {
 
 template <typename T>
 cudaError_t launch_dense(const DensePlan& p, const DenseArgs<T>& a, cudaStream_t st);
+
+// X stored as bfloat16, computed in fp32 (tile kernel, or the direct-load narrow kernel).
+cudaError_t launch_dense_bf16(const DensePlan& p, const DenseArgs<float, __nv_bfloat16>& a, cudaStream_t st);
 
 // One CSR call. alpha is folded into t_i; out is pre-set to beta z (or 0) by the
 // prologue and then receives atomic additions.

@@ -51,17 +51,21 @@ DensePlan plan_dense(const DeviceInfo& dev, int64_t m, int64_t n, int64_t ld, in
     return p;
   }
   const int64_t budget = std::min<int64_t>(kSmemBudget, dev.smem_optin > 0 ? dev.smem_optin : 48 * 1024);
-  const int64_t chunks = cdiv(n * elem, 16);
+  // bfloat16 X (elem 2) is computed in fp32: the narrow kernel counts its chunks in fp32 elements
+  const int64_t chunks = cdiv(n * (elem == 2 ? 4 : elem), 16);
   const int64_t row_bytes = n * elem;
-  if (tile_ok && row_bytes >= 64 && row_bytes <= 2048 && m < (int64_t(1) << 31)) {
-    // tile kernel: 2 * nb lanes per row, four 16-byte chunks each; tiles of 8 KB (16 KB at nb = 16)
+  const int cpl = elem == 2 ? 2 : 4;  // 16-byte chunks per lane in the tile kernel
+  const int64_t max_tile_row = elem == 2 ? 1024 : 2048;
+  if (tile_ok && row_bytes >= 32 && row_bytes <= max_tile_row && m < (int64_t(1) << 31)) {
+    // tile kernel: boxes of 128 bytes (64 for rows of at most 64 bytes); 8-KB tiles (16 KB at nb = 16)
     p.kind = DENSE_TILE_TMA;
-    p.nbr = (int)cdiv(row_bytes, 128);
+    p.box_bytes = row_bytes <= 64 ? 64 : 128;
+    p.nbr = (int)cdiv(row_bytes, p.box_bytes);
     p.nb = (int)pow2_ceil(p.nbr);
-    p.lpr = 2 * p.nb;
-    p.vpl = 4;
-    p.rows_per_tile = p.nb >= 8 ? 8 : 64 / p.nb;
-    const int64_t tile = (int64_t)p.nb * p.rows_per_tile * 128;
+    p.lpr = (p.box_bytes / 16) * p.nb / cpl;
+    p.vpl = cpl;
+    p.rows_per_tile = p.box_bytes == 64 ? 128 : (p.nb >= 8 ? 8 : 64 / p.nb);
+    const int64_t tile = (int64_t)p.nb * p.rows_per_tile * p.box_bytes;
     int warps = 8, S = 0;
     for (;;) {
       S = (int)std::min<int64_t>(8, (budget - 1024) / (warps * (tile + 8)));
@@ -81,7 +85,7 @@ DensePlan plan_dense(const DeviceInfo& dev, int64_t m, int64_t n, int64_t ld, in
     p.lpr = lpr;
     p.vpl = vpl;
     const int G = 32 / lpr;
-    if (tma_ok) {
+    if (tma_ok && elem != 2) {
       // coarsening: the largest power-of-two row count (G..32) whose tile fits the target
       int R = 32;
       while (R > G && R * row_bytes > kTileTarget) R >>= 1;
@@ -106,6 +110,7 @@ DensePlan plan_dense(const DeviceInfo& dev, int64_t m, int64_t n, int64_t ld, in
       p.warps = 8;
       p.smem = (size_t)p.warps * n * sizeof(double);
     }
+    (void)G;
     const int64_t tiles = cdiv(m, p.rows_per_tile);
     const int per_sm = p.kind == DENSE_NARROW_DIRECT ? 4 : 1;
     p.ctas = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)dev.sm_count * per_sm, cdiv(tiles, p.warps)));
@@ -157,9 +162,9 @@ int describe(const DensePlan& p, char* buf, size_t cap) {
   static const char* names[] = {"noop", "empty_rows", "narrow_tma", "narrow_direct", "wide", "tile_tma"};
   return snprintf(buf, cap,
                   "dense kind=%s lanes_per_row=%d chunks_per_lane=%d rows_per_tile=%d stages=%d warps=%d ctas=%d "
-                  "smem=%zu smem_acc=%d blocks=%d ws=%zu",
+                  "smem=%zu smem_acc=%d blocks=%d box=%d ws=%zu",
                   names[p.kind], p.lpr, p.vpl, p.rows_per_tile, p.stages, p.warps, p.ctas, p.smem, (int)p.smem_acc,
-                  p.nbr, p.ws_bytes);
+                  p.nbr, p.box_bytes, p.ws_bytes);
 }
 
 int describe(const CsrPlan& p, char* buf, size_t cap) {

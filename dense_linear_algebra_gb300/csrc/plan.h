@@ -28,7 +28,8 @@ enum DenseKind { DENSE_NOOP = 0, DENSE_EMPTY_ROWS, DENSE_NARROW_TMA, DENSE_NARRO
 struct DensePlan {
   DenseKind kind = DENSE_NOOP;
   int nb = 0;             // tile kernel: 128-byte column blocks per row, rounded up to a power of two
-  int nbr = 0;            // tile kernel: column blocks actually copied, ceil(n * elem / 128)
+  int nbr = 0;            // tile kernel: column blocks actually copied, ceil(n * elem / box_bytes)
+  int box_bytes = 0;      // tile kernel: width of a tensor-copy box (128, or 64 for rows of at most 64 bytes)
   int lpr = 0;            // lanes cooperating on one row (narrow)
   int vpl = 0;            // 16-byte chunks of a row held per lane (narrow)
   int rows_per_tile = 0;  // coarsening: rows a warp takes per pipeline step

@@ -43,7 +43,7 @@ extern "C" {
 typedef enum {
   FXTX_OK = 0,
   FXTX_ERR_INVALID_ARG = 1, /* a size is negative, ld < n, or a required pointer is NULL */
-  FXTX_ERR_UNSUPPORTED = 2, /* no CUDA device of compute capability 10.3 is current */
+  FXTX_ERR_UNSUPPORTED = 2, /* no compute capability 10.3 device is current, or a shape an entry does not take */
   FXTX_ERR_CUDA = 3,        /* a CUDA runtime call failed while enqueueing (launch, allocation) */
   FXTX_ERR_ALLOC = 4,       /* workspace allocation failed */
   FXTX_ERR_BAD_CSR = 5,     /* fxtx_csr_validate found a malformed structure */
@@ -72,6 +72,19 @@ fxtx_status_t fxtx_dense_f32(int64_t m, int64_t n, const float* X, int64_t ld, c
 fxtx_status_t fxtx_dense_f64(int64_t m, int64_t n, const double* X, int64_t ld, const double* y,
                              const double* v, double alpha, double beta, const double* z, double* out,
                              void* stream);
+
+/*
+ * Dense X stored as bfloat16 (the upper 16 bits of an IEEE binary32, given as
+ * uint16_t), with y, v, z and out in fp32 and all arithmetic in fp32 as in
+ * fxtx_dense_f32 (each bfloat16 widens exactly). Reading X in bfloat16 halves the
+ * bytes of the dominant stream. Shapes: n <= 512. Rows of at least 64 bytes with
+ * X 16-byte aligned and ld * 2 a multiple of 16 take the tensor-copied tile
+ * kernel; others a direct-load kernel. n > 512 returns FXTX_ERR_UNSUPPORTED.
+ * Arguments, ownership and the bound are otherwise those of fxtx_dense_f32.
+ */
+fxtx_status_t fxtx_dense_bf16(int64_t m, int64_t n, const uint16_t* X, int64_t ld, const float* y,
+                              const float* v, float alpha, float beta, const float* z, float* out,
+                              void* stream);
 
 /*
  * fxtx_dense_f32 without any device allocation at call time. (The paper has no

@@ -96,6 +96,17 @@ def integers(seed: int, stream: int, shape, lo: int, hi: int, dtype=np.float64) 
     return out
 
 
+def round_to_bf16(a: np.ndarray) -> np.ndarray:
+    """float32 values rounded to the nearest bfloat16 (ties to even), kept as float32.
+
+    Every result is exactly representable in bfloat16, so a device copy in bfloat16 and
+    the float32 array hold the same numbers.
+    """
+    bits = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+    rounded = (bits + np.uint32(0x7FFF) + ((bits >> np.uint32(16)) & np.uint32(1))) & np.uint32(0xFFFF0000)
+    return rounded.view(np.float32)
+
+
 def poisson_lengths(seed: int, m: int, lam: float, cap: int) -> np.ndarray:
     lens = np.empty(m, dtype=np.int64)
     _load().ig_poisson_lengths(seed, STRUCTURE, m, lam, cap, _ptr(lens))
@@ -146,6 +157,7 @@ class Problem:
     col_idx: Optional[np.ndarray] = None
     vals: Optional[np.ndarray] = None
     info: dict = field(default_factory=dict)
+    x_store: str = ""  # "bf16": X holds bfloat16-representable values, stored on the device as bfloat16
 
     @property
     def nnz(self) -> int:
@@ -164,7 +176,7 @@ class Problem:
         if self.z is not None and self.beta != 0.0:
             b += self.n * s
         if self.kind == "dense":
-            b += self.m * self.n * s
+            b += self.m * self.n * (2 if self.x_store == "bf16" else s)
         else:
             b += self.nnz * (s + 4) + (self.m + 1) * 8
         return b
@@ -179,9 +191,17 @@ def dense_small(seed: int = 0, m: int = 1000, n: int = 64) -> Problem:
                    z=uniform(seed, ZSTREAM, n, -1.0, 1.0, d))
 
 
-def dense_tall(seed: int = 0, m: int = 16_000_000, n: int = 32, variant: str = "b") -> Problem:
+def dense_tall(seed: int = 0, m: int = 16_000_000, n: int = 32, variant: str = "b", x_store: str = "") -> Problem:
     d = np.float32
     X = normal(seed, XSTREAM, (m, n), d)
+    if x_store == "bf16":
+        p = dense_tall(seed, m=1, n=n, variant=variant)  # the vectors and scalars of the same recipe
+        p.X = round_to_bf16(X)
+        p.m = m
+        p.v = None if p.v is None else uniform(seed, VSTREAM, m, 0.1, 2.0, d)
+        p.x_store = "bf16"
+        p.name = p.name.replace("dense_f32_1x", "dense_bf16_%dx" % m)
+        return p
     y = normal(seed, YSTREAM, n, d)
     v = uniform(seed, VSTREAM, m, 0.1, 2.0, d)
     if variant == "a":

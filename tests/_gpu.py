@@ -21,6 +21,8 @@ class DeviceProblem:
         self.z = to_dev(p.z, device)
         if p.kind == "dense":
             Xd = to_dev(p.X, device)  # (m, ld)
+            if p.x_store == "bf16":  # the values are bfloat16-representable: the conversion is exact
+                Xd = Xd.to(torch.bfloat16)
             self.X = Xd[:, : p.n]
         else:
             self.row_ptr = to_dev(p.row_ptr, device)

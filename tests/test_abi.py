@@ -68,7 +68,9 @@ def test_no_device_is_reported_as_unsupported():
         (("dense", "f32", 16_000_000, 32), "kind=tile_tma lanes_per_row=2 chunks_per_lane=4 rows_per_tile=64"),
         (("dense", "f64", 1000, 64), "kind=tile_tma lanes_per_row=8 chunks_per_lane=4 rows_per_tile=16"),
         (("dense", "f32", 1000, 512), "kind=tile_tma lanes_per_row=32 chunks_per_lane=4 rows_per_tile=8"),
-        (("dense", "f32", 1000, 8), "kind=narrow_tma lanes_per_row=2 chunks_per_lane=1 rows_per_tile=32"),
+        (("dense", "f32", 1000, 8), "kind=tile_tma lanes_per_row=1 chunks_per_lane=4 rows_per_tile=128"),
+        (("dense", "f32", 1000, 16), "box=64"),
+        (("dense", "f32", 1000, 4), "kind=narrow_tma lanes_per_row=1 chunks_per_lane=1 rows_per_tile=32"),
         (("dense", "f64", 20_000, 20_000), "kind=wide"),
         (("dense", "f32", 10, 3), "kind=narrow_direct"),
         (("dense", "f32", 0, 3), "kind=empty_rows"),
