@@ -170,11 +170,11 @@ class Problem:
     def ideal_bytes(self) -> int:
         """Algorithmic bytes: X once, y, v (if given), z (if read), out once."""
         s = self.itemsize
-        b = self.n * s + self.n * s  # y, out
+        b = 2 * self.y.size * s  # y, out (n, or n x k for several right-hand sides)
         if self.v is not None:
-            b += self.m * s
+            b += self.v.size * s
         if self.z is not None and self.beta != 0.0:
-            b += self.n * s
+            b += self.z.size * s
         if self.kind == "dense":
             b += self.m * self.n * (2 if self.x_store == "bf16" else s)
         else:
@@ -212,6 +212,28 @@ def dense_tall(seed: int = 0, m: int = 16_000_000, n: int = 32, variant: str = "
     if variant == "c":
         return Problem("dense_f32_%dx%d_c" % (m, n), "dense", d, m, n, 1.0, 0.0, X=X, ld=n, y=y, v=None, z=None)
     raise ValueError(variant)
+
+
+def dense_multi(seed: int = 0, m: int = 16_000_000, n: int = 32, k: int = 8, dtype=np.float32,
+                v_mode: str = "full") -> Problem:
+    """Several right-hand sides on the tall-skinny recipe: Y (n, k) and Z (n, k) N(0,1);
+    V U[0.1, 2] either (m, k) ("full"), one m-vector shared by all k ("shared"), or
+    absent ("none"); alpha = 2, beta = -1."""
+    d = dtype
+    X = normal(seed, XSTREAM, (m, n), d)
+    Y = normal(seed, YSTREAM, (n, k), d)
+    Z = normal(seed, ZSTREAM, (n, k), d)
+    if v_mode == "full":
+        V = uniform(seed, VSTREAM, (m, k), 0.1, 2.0, d)
+    elif v_mode == "shared":
+        V = uniform(seed, VSTREAM, m, 0.1, 2.0, d)
+    elif v_mode == "none":
+        V = None
+    else:
+        raise ValueError(v_mode)
+    tag = "f32" if d == np.float32 else "f64"
+    return Problem("dense_multi_%s_%dx%dx%d_%s" % (tag, m, n, k, v_mode), "dense", d, m, n, 2.0, -1.0,
+                   X=X, ld=n, y=Y, v=V, z=Z)
 
 
 def dense_wide(seed: int = 0, m: int = 20_000, n: int = 20_000) -> Problem:

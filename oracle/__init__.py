@@ -11,6 +11,9 @@ It is compiled twice into ``liboracle.so``: with a ``long double`` accumulator
 the timed CPU baseline). Both return the output and the per-column error scale
 ``S_j = |alpha| sum_i |t_i| |X_ij| + |beta z_j|``.
 
+``dense_multi`` is the multi-vector instantiation ``OUT = alpha * X^T (V * (X Y)) +
+beta * Z`` with k right-hand sides: column by column, the single-vector oracle.
+
 Parity: every function here is pinned by ``tests/test_oracle.py`` (worked example,
 closed-form identities, exact arithmetic on tiny inputs, dense-vs-CSR, a library
 composition and planted-mistake checks). Nothing is left unpinned.
@@ -162,8 +165,45 @@ def csr_is_valid(row_ptr, col_idx, n: int, lib=None) -> bool:
     return lib.oracle_csr_check_ld(m, n, col_idx.shape[0], _p(row_ptr), _p(col_idx)) == 0
 
 
+def _vcol(V, c):
+    """Column c of the row weights: None (all ones), one shared m-vector, or an (m, k) matrix."""
+    if V is None or V.ndim == 1:
+        return V
+    return np.ascontiguousarray(V[:, c])
+
+
+def dense_multi(X: np.ndarray, Y: np.ndarray, V, alpha: float, beta: float, Z, n: int | None = None, cols=None,
+                acc: str = "ld", lib=None):
+    """Oracle for the multi-vector instantiation ``OUT = alpha * X^T (V * (X Y)) + beta * Z``.
+
+    Y is (n, k); V is None (all ones), an m-vector shared by every right-hand side, or
+    an (m, k) matrix; Z is None or (n, k). The k right-hand sides do not interact: each
+    column c of OUT is the single-vector pattern with y = Y[:, c], v = V[:, c] (or the
+    shared v) and z = Z[:, c], computed by ``dense``. Returns (OUT, S), each (nout, k).
+    """
+    X = np.ascontiguousarray(X)
+    n = X.shape[1] if n is None else n
+    if Y.ndim != 2 or Y.shape[0] != n:
+        raise ValueError(f"Y: expected shape ({n}, k), got {Y.shape}")
+    k = Y.shape[1]
+    if V is not None and V.ndim == 2 and V.shape != (X.shape[0], k):
+        raise ValueError(f"V: expected shape ({X.shape[0]}, {k}), got {V.shape}")
+    if Z is not None and Z.shape != (n, k):
+        raise ValueError(f"Z: expected shape ({n}, {k}), got {Z.shape}")
+    nout = n if cols is None else len(cols)
+    OUT = np.empty((nout, k), dtype=np.float64)
+    S = np.empty((nout, k), dtype=np.float64)
+    for c in range(k):
+        zc = None if Z is None else np.ascontiguousarray(Z[:, c])
+        OUT[:, c], S[:, c] = dense(X, np.ascontiguousarray(Y[:, c]), _vcol(V, c), alpha, beta, zc, n=n, cols=cols,
+                                   acc=acc, lib=lib)
+    return OUT, S
+
+
 def solve(p, cols=None, acc: str = "ld", lib=None):
     """Oracle for an ``inputgen.Problem``."""
+    if p.kind == "dense" and p.y.ndim == 2:
+        return dense_multi(p.X, p.y, p.v, p.alpha, p.beta, p.z, n=p.n, cols=cols, acc=acc, lib=lib)
     if p.kind == "dense":
         return dense(p.X, p.y, p.v, p.alpha, p.beta, p.z, n=p.n, cols=cols, acc=acc, lib=lib)
     if cols is not None:

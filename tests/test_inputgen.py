@@ -61,3 +61,10 @@ def test_workload_shapes_small():
     assert inputgen.dense_tall(m=10, variant="a").z is None
     p = inputgen.dense_small()
     assert p.ideal_bytes() == 1000 * 64 * 8 + 64 * 8 * 3 + 1000 * 8
+    p = inputgen.dense_multi(m=100, n=32, k=8)
+    assert p.y.shape == (32, 8) and p.z.shape == (32, 8) and p.v.shape == (100, 8)
+    assert p.ideal_bytes() == 100 * 32 * 4 + 2 * 32 * 8 * 4 + 100 * 8 * 4 + 32 * 8 * 4
+    assert inputgen.dense_multi(m=10, k=3, v_mode="shared").v.shape == (10,)
+    assert inputgen.dense_multi(m=10, k=3, v_mode="none").v is None
+    q = inputgen.dense_multi(m=100, n=32, k=8)
+    assert np.array_equal(p.X, q.X) and np.array_equal(p.y, q.y) and np.array_equal(p.v, q.v)

@@ -14,7 +14,9 @@ learning workloads via kernel fusion", abstract). The pins are:
   summing;
 * the textbook composition X.T @ (X @ y) from numpy;
 * the instantiations' special cases (m = 0, n = 0, v absent, z absent, beta = 0
-  with z unread).
+  with z unread);
+* for the multi-vector instantiation (k right-hand sides), exact rational arithmetic
+  over the matrix form and the numpy matrix composition, with its own planted mistakes.
 
 ``test_planted_mistakes`` compiles altered copies of the oracle (a dropped term, a
 wrong sign, a transposed index, an off-by-one row range, ...) and checks that every
@@ -331,6 +333,122 @@ def test_accumulators_agree_on_workload_recipe():
     b, _ = oracle.solve(p, acc="d")
     assert np.all(np.abs(a - b) <= 1e-12 * S)
     assert np.all(S > 0)
+
+
+# ---------------------------------------------------------------------------------------------
+# The multi-vector instantiation OUT = alpha * X^T (V * (X Y)) + beta * Z ("On optimizing
+# machine learning workloads via kernel fusion", abstract: the pattern and its
+# instantiations, here with k right-hand sides at once).
+# ---------------------------------------------------------------------------------------------
+def _exact_multi(Xq, Yq, Vq, alpha, beta, Zq):
+    """Exact rational OUT over the whole matrix, written out as row sums and column sums."""
+    m, n, k = len(Xq), len(Yq), len(Yq[0]) if Yq else 0
+    a, b = Fraction(alpha), Fraction(beta)
+    T = [[sum((Xq[i][j] * Yq[j][c] for j in range(n)), Fraction(0)) for c in range(k)] for i in range(m)]
+    if Vq is not None:
+        T = [[T[i][c] * (Vq[i][c] if isinstance(Vq[i], list) else Vq[i]) for c in range(k)] for i in range(m)]
+    out = []
+    for j in range(n):
+        row = []
+        for c in range(k):
+            w = sum((Xq[i][j] * T[i][c] for i in range(m)), Fraction(0))
+            row.append(a * w + (b * Zq[j][c] if Zq is not None and beta != 0 else Fraction(0)))
+        out.append(row)
+    return out
+
+
+def _fracm(A):
+    return None if A is None else [[Fraction(float(x)) for x in row] for row in A] if A.ndim == 2 else _frac(A)
+
+
+def pin_multi_exact(lib, fn=None):
+    """Tiny integer inputs: the multi-vector oracle equals exact rational arithmetic for
+    full (m, k) weights, one shared weight vector, and no weights."""
+    fn = fn or oracle.dense_multi
+    rng = np.random.default_rng(21)
+    for (m, n, k) in ((4, 3, 2), (5, 2, 3), (1, 4, 4), (3, 3, 1)):
+        X = rng.integers(-3, 4, (m, n)).astype(np.float64)
+        Y = rng.integers(-3, 4, (n, k)).astype(np.float64)
+        Z = rng.integers(-3, 4, (n, k)).astype(np.float64)
+        for V in (rng.integers(-2, 3, (m, k)).astype(np.float64), rng.integers(-2, 3, m).astype(np.float64), None):
+            ref = _exact_multi(_fracm(X), _fracm(Y), None if V is None else _fracm(V), -1.5, 2.0, _fracm(Z))
+            out, _ = fn(X, Y, V, -1.5, 2.0, Z, lib=lib)
+            assert out.shape == (n, k)
+            assert [[Fraction(o) for o in row] for row in out] == ref, (m, n, k, None if V is None else V.ndim)
+
+
+def pin_multi_library(lib, fn=None):
+    """The matrix form from numpy, and the bound's scale per (column, right-hand side)."""
+    fn = fn or oracle.dense_multi
+    rng = np.random.default_rng(22)
+    m, n, k = 300, 11, 5
+    X = rng.standard_normal((m, n))
+    Y = rng.standard_normal((n, k))
+    V = rng.uniform(0.1, 2.0, (m, k))
+    Z = rng.standard_normal((n, k))
+    T = V * (X @ Y)
+    ref = 0.75 * (X.T @ T) + 0.5 * Z
+    out, S = fn(X, Y, V, 0.75, 0.5, Z, lib=lib)
+    scale = 0.75 * (np.abs(X).T @ (np.abs(V) * (np.abs(X) @ np.abs(Y)))) + 0.5 * np.abs(Z)
+    assert np.all(np.abs(out - ref) <= 1e-13 * scale)
+    assert np.allclose(S, 0.75 * (np.abs(X).T @ np.abs(T)) + 0.5 * np.abs(Z), rtol=1e-12)
+    # one shared v is the same as that v repeated in every column
+    v = rng.uniform(0.1, 2.0, m)
+    a, _ = fn(X, Y, v, 0.75, 0.5, Z, lib=lib)
+    b, _ = fn(X, Y, np.repeat(v[:, None], k, axis=1), 0.75, 0.5, Z, lib=lib)
+    assert np.array_equal(a, b)
+    # k = 1 is the single-vector pattern; sampled columns equal the full computation
+    one, _ = oracle.dense(X, Y[:, 2].copy(), V[:, 2].copy(), 0.75, 0.5, Z[:, 2].copy(), lib=lib)
+    c1, _ = fn(X, Y[:, 2:3], V[:, 2:3], 0.75, 0.5, Z[:, 2:3], lib=lib)
+    assert np.array_equal(c1[:, 0], one) and np.array_equal(out[:, 2], one)
+    cols = np.array([7, 0, 3])
+    part, Sp = fn(X, Y, V, 0.75, 0.5, Z, cols=cols, lib=lib)
+    assert np.array_equal(part, out[cols]) and np.array_equal(Sp, S[cols])
+    # the right-hand sides do not interact: permuting Y's columns (with V and Z) permutes OUT's
+    perm = np.array([3, 1, 4, 0, 2])
+    pout, _ = fn(X, Y[:, perm], V[:, perm], 0.75, 0.5, Z[:, perm], lib=lib)
+    assert np.array_equal(pout, out[:, perm])
+    # beta = 0 leaves Z unread
+    a, _ = fn(X, Y, V, 0.75, 0.0, np.full((n, k), np.nan), lib=lib)
+    b, _ = fn(X, Y, V, 0.75, 0.0, None, lib=lib)
+    assert np.array_equal(a, b)
+
+
+MULTI_PINS = [pin_multi_exact, pin_multi_library]
+
+
+@pytest.mark.parametrize("pin", MULTI_PINS, ids=lambda f: f.__name__)
+def test_multi_pin(pin):
+    pin(oracle._load())
+
+
+# Planted mistakes in the multi-vector wrapper: (description, exact text, replacement).
+MULTI_MUTANTS = [
+    ("every right-hand side reads Y's first column", "np.ascontiguousarray(Y[:, c])", "np.ascontiguousarray(Y[:, 0])"),
+    ("weights taken from the wrong column", "np.ascontiguousarray(V[:, c])", "np.ascontiguousarray(V[:, -1 - c])"),
+    ("Z's columns shifted", "zc = None if Z is None else np.ascontiguousarray(Z[:, c])",
+     "zc = None if Z is None else np.ascontiguousarray(Z[:, (c + 1) % k])"),
+    ("shared weights ignored", "if V is None or V.ndim == 1:\n        return V", "if V is None or V.ndim == 1:\n        return None"),
+]
+
+
+@pytest.mark.parametrize("mutant", MULTI_MUTANTS, ids=lambda m: m[0])
+def test_multi_planted_mistakes(mutant):
+    """An altered multi-vector oracle must fail at least one of its pins."""
+    import inspect
+    import textwrap
+    desc, old, new = mutant
+    src = textwrap.dedent(inspect.getsource(oracle._vcol)) + "\n" + textwrap.dedent(inspect.getsource(oracle.dense_multi))
+    assert old in src, f"mutation target for '{desc}' not found in the oracle source"
+    ns = dict(vars(oracle))
+    exec(compile(src.replace(old, new), "<mutant>", "exec"), ns)
+    failures = []
+    for pin in MULTI_PINS:
+        try:
+            pin(oracle._load(), fn=ns["dense_multi"])
+        except (AssertionError, ValueError):
+            failures.append(pin.__name__)
+    assert failures, f"mutant '{desc}' passed every pin"
 
 
 # Each entry: (description, exact text in fxtx_oracle.c, replacement, occurrence count to replace)
