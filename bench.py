@@ -37,6 +37,7 @@ import numpy as np  # noqa: E402
 METRIC = "fused aX^T(v.*Xy)+bz: effective GB/s and % of GB300 HBM peak"
 FALLBACK_HBM_GBS = 6800.0
 FP64_PEAK_TFLOPS = 1.259  # 152 SMs x 2 DFMA/clk x 2 flops x 2.07 GHz
+FP32_PEAK_TFLOPS = 78.5   # 152 SMs x 124.7 FFMA/clk (measured issue rate) x 2 flops x 2.07 GHz
 
 def _m(kw, m):
     return dict(kw, m=m) if m else kw
@@ -58,6 +59,12 @@ WORKLOADS = {
                    lambda g, m=None: g.dense_wide(**_m({}, m))),
     "csr_uniform": ("CSR f64 4,000,000 x 10,000, Poisson(50) uniform distinct columns, U[-1,1], alpha=beta=1",
                     lambda g, m=None: g.csr_uniform(**_m({}, m))),
+    "dense_multi": ("dense f32 16,000,000 x 32 with k=8 right-hand sides: Y, Z (32 x 8) N(0,1), V (16,000,000 x 8) "
+                    "U[0.1,2], alpha=2, beta=-1",
+                    lambda g, m=None: g.dense_multi(**_m({}, m))),
+    "dense_multi_shared": ("dense f32 16,000,000 x 32 with k=8 right-hand sides and one shared v: Y, Z (32 x 8) "
+                           "N(0,1), v U[0.1,2], alpha=2, beta=-1",
+                           lambda g, m=None: g.dense_multi(**_m({"v_mode": "shared"}, m))),
     "csr_powerlaw": ("CSR f32 2,000,000 x 1,000,000, Zipf(1.5) row lengths (mean 100, cap 50,000), Zipf(1.1) "
                      "columns, N(0,1) vals/y, v U[0,1], alpha=1, beta=0",
                      lambda g, m=None: g.csr_powerlaw(**_m({}, m))),
@@ -70,6 +77,8 @@ def dominant_kernel(p) -> str:
 
     if p.x_store == "bf16":
         return "dense_tile_kernel"
+    if is_multi(p):
+        return "dense_multi_kernel"
     if p.kind == "csr":
         # rows longer than 256 entries go to the long-row kernel; it dominates when they hold most entries
         lens = np.diff(p.row_ptr)
@@ -78,6 +87,10 @@ def dominant_kernel(p) -> str:
     kind = dict(kv.split("=") for kv in desc.split()[1:] if "=" in kv)["kind"]
     return {"tile_tma": "dense_tile_kernel", "narrow_tma": "dense_narrow_kernel", "narrow_direct": "dense_narrow_kernel",
             "wide": "dense_wide_kernel"}.get(kind, kind)
+
+
+def is_multi(p) -> bool:
+    return p.kind == "dense" and p.y.ndim == 2
 
 
 def measured_peaks():
@@ -155,14 +168,16 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-KERNEL_SOURCES = {"dense": ["dense.cu", "common.cuh", "kernels.h"], "csr": ["csr.cu", "common.cuh", "kernels.h"]}
+KERNEL_SOURCES = {"dense": ["dense.cu", "common.cuh", "kernels.h"], "csr": ["csr.cu", "common.cuh", "kernels.h"],
+                  "multi": ["multi.cu", "multi.h", "common.cuh", "kernels.h"]}
 
 
 def source_sha(kernel: str) -> str:
     """Hash of the source files that define a kernel (its .cu file and the device headers it includes)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_linear_algebra_gb300", "csrc")
-    for fn in KERNEL_SOURCES["csr" if kernel.startswith("csr") else "dense"]:
+    group = "csr" if kernel.startswith("csr") else ("multi" if kernel.startswith("dense_multi") else "dense")
+    for fn in KERNEL_SOURCES[group]:
         h.update(open(os.path.join(csrc, fn), "rb").read())
     return h.hexdigest()[:16]
 
@@ -293,6 +308,32 @@ def time_unfused(args, p, d, X, out, dev, stream, ideal, ms_step):
     # the unfused library sequence on the same GPU (dense: cuBLAS gemv, scale, transposed gemv)
     if p.x_store == "bf16":
         return {"error": "no library gemv takes bfloat16 X with fp32 vectors and fp32 accumulation"}
+    if is_multi(p):
+        try:
+            k = p.y.shape[1]
+            tz = d["z"] if (d["z"] is not None and p.beta != 0) else torch.zeros((p.n, k), dtype=out.dtype, device=dev)
+            vv = None if d["v"] is None else (d["v"] if d["v"].dim() == 2 else d["v"][:, None])
+
+            def lib_seq():
+                u = torch.mm(X, d["y"])
+                t = u * vv if vv is not None else u
+                return torch.addmm(tz, X.t(), t, beta=p.beta, alpha=p.alpha)
+            for _ in range(3):
+                lib_seq()
+            torch.cuda.synchronize()
+            u0 = torch.cuda.Event(enable_timing=True)
+            u1 = torch.cuda.Event(enable_timing=True)
+            u0.record(stream)
+            for _ in range(args.steps):
+                lib_seq()
+            u1.record(stream)
+            torch.cuda.synchronize()
+            ums = u0.elapsed_time(u1) / args.steps
+            return {"what": "torch.mm (cuBLAS GEMM X Y), V scale, torch.addmm on X^T (cuBLAS GEMM)",
+                    "ms_per_step": round(ums, 4), "value": round(ideal / (ums * 1e-3) / 1e9, 2), "unit": "GB/s",
+                    "fused_speedup": round(ums / ms_step, 3)}
+        except Exception as e:  # report, do not fail the bench
+            return {"error": str(e)[:200]}
     if p.kind == "dense":
         try:
             Xt = X
@@ -370,10 +411,18 @@ def run_fused(args, name, desc, p, rank, world, dist):
         host["row_ptr"], host["col_idx"], host["vals"] = pin(p.row_ptr), pin(p.col_idx), pin(p.vals)
     host["y"], host["v"], host["z"] = pin(p.y), pin(p.v), pin(p.z)
     d = {k: (None if t is None else t.to(dev, non_blocking=False)) for k, t in host.items()}
-    out = torch.empty(p.n, dtype=d["y"].dtype, device=dev)
-    out_host = torch.empty(p.n, dtype=d["y"].dtype).pin_memory()
+    out = torch.empty(p.y.shape, dtype=d["y"].dtype, device=dev)
+    out_host = torch.empty(p.y.shape, dtype=d["y"].dtype).pin_memory()
 
-    if p.kind == "dense":
+    if is_multi(p):
+        X = d["X"][:, : p.n]
+
+        def call(o=out):
+            return fx.dense_multi(X, d["y"], d["v"], p.alpha, p.beta, d["z"], out=o, stream=stream)
+        plan = fx.multi_plan_describe(dtype_name(p), p.m, p.n, p.y.shape[1],
+                                      "none" if p.v is None else ("full" if p.v.ndim == 2 else "shared"), p.ld)
+        launches = int(dict(kv.split("=") for kv in plan.split()[1:])["passes"])
+    elif p.kind == "dense":
         X = d["X"][:, : p.n]
 
         def call(o=out):
@@ -454,7 +503,20 @@ def run_fused(args, name, desc, p, rank, world, dist):
                      "kernel": kernel},
         "unfused_library": unfused,
     }
-    if dtype_name(p) == "f64":
+    if is_multi(p):
+        # k right-hand sides: two FMAs (4 flops) per stored element per right-hand side, on the fp32 or fp64 pipe
+        flops = 4.0 * p.m * p.n * p.y.shape[1]
+        alu_peak = FP32_PEAK_TFLOPS if dtype_name(p) == "f32" else float(peaks.get("fp64_tflops", FP64_PEAK_TFLOPS))
+        rec["roofline_alu"] = {"bound": "alu", "achieved": round(flops / (kernel_ms * 1e-3) / 1e12, 4),
+                               "peak": alu_peak, "unit": "TFLOP/s",
+                               "frac": round(flops / (kernel_ms * 1e-3) / 1e12 / alu_peak, 4),
+                               "peak_source": "152 SMs x 124.7 FFMA/clk (probe) x 2 flops x 2.07 GHz" if alu_peak ==
+                               FP32_PEAK_TFLOPS else "152 SMs x 2 DFMA/clk x 2 flops x 2.07 GHz (DFMA probe: 1.254)",
+                               "algorithmic_flops_per_step": flops}
+        rec["config"]["right_hand_sides"] = int(p.y.shape[1])
+        if flops / (alu_peak * 1e12) > ideal / (peak * 1e9):
+            rec["roofline"]["bound"] = "alu"
+    elif dtype_name(p) == "f64":
         # fp64 runs on GB300's fp64 units: 2 DFMA per clock per SM (measured 1.254 TFLOP/s), and the
         # pattern needs two FMAs (4 flops) per stored element, so the fp64 rate can bind before HBM
         flops = 4.0 * (p.m * p.n if p.kind == "dense" else p.nnz)

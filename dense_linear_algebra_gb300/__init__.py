@@ -7,9 +7,11 @@ CUDA kernels of ``libfusedxtx.so`` (sources in ``csrc/``, C ABI in
 fallback: if the library cannot be loaded, importing the binding fails.
 
 Raw C-ABI calls (pointers as ints, stream as a cudaStream_t int) carry the C names:
-``fxtx_dense_f32``, ``fxtx_dense_f64``, ``fxtx_dense_bf16``, ``fxtx_dense_f32_noalloc``, ``fxtx_csr_f32``, ``fxtx_csr_f64``,
+``fxtx_dense_f32``, ``fxtx_dense_f64``, ``fxtx_dense_bf16``, ``fxtx_dense_f32_noalloc``,
+``fxtx_dense_multi_f32``, ``fxtx_dense_multi_f64``, ``fxtx_csr_f32``, ``fxtx_csr_f64``,
 ``fxtx_csr_validate``, ``fxtx_device_error``, ``fxtx_status_string``,
-``fxtx_plan_describe``. ``dense`` and ``csr`` take torch CUDA tensors.
+``fxtx_plan_describe``, ``fxtx_multi_plan_describe``. ``dense``, ``dense_multi`` and
+``csr`` take torch CUDA tensors.
 """
 from ._lib import (  # noqa: F401
     FXTX_ERR_ALLOC,
@@ -24,6 +26,7 @@ from ._lib import (  # noqa: F401
     csr,
     csr_validate,
     dense,
+    dense_multi,
     device_error,
     fxtx_csr_f32,
     fxtx_csr_f64,
@@ -32,9 +35,13 @@ from ._lib import (  # noqa: F401
     fxtx_dense_f32_noalloc,
     fxtx_dense_bf16,
     fxtx_dense_f64,
+    fxtx_dense_multi_f32,
+    fxtx_dense_multi_f64,
     fxtx_device_error,
+    fxtx_multi_plan_describe,
     fxtx_plan_describe,
     fxtx_status_string,
     library_path,
+    multi_plan_describe,
     plan_describe,
 )

@@ -29,6 +29,8 @@ def _load() -> ctypes.CDLL:
     lib.fxtx_dense_f64.argtypes = [i64, i64, vp, i64, vp, vp, f64, f64, vp, vp, vp]
     lib.fxtx_dense_f32_noalloc.argtypes = [i64, i64, vp, i64, vp, vp, f32, f32, vp, vp, vp]
     lib.fxtx_dense_bf16.argtypes = [i64, i64, vp, i64, vp, vp, f32, f32, vp, vp, vp]
+    lib.fxtx_dense_multi_f32.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, f32, f32, vp, i64, vp, i64, vp]
+    lib.fxtx_dense_multi_f64.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, f64, f64, vp, i64, vp, i64, vp]
     lib.fxtx_csr_f32.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, f32, f32, vp, vp, vp]
     lib.fxtx_csr_f64.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, f64, f64, vp, vp, vp]
     lib.fxtx_csr_validate.argtypes = [i64, i64, i64, vp, vp, vp]
@@ -36,8 +38,10 @@ def _load() -> ctypes.CDLL:
     lib.fxtx_status_string.argtypes = [i32]
     lib.fxtx_status_string.restype = ctypes.c_char_p
     lib.fxtx_plan_describe.argtypes = [i32, i32, i64, i64, i64, i64, ctypes.c_char_p, i64]
-    for name in ("fxtx_dense_f32", "fxtx_dense_f64", "fxtx_dense_f32_noalloc", "fxtx_dense_bf16", "fxtx_csr_f32", "fxtx_csr_f64", "fxtx_csr_validate",
-                 "fxtx_device_error", "fxtx_plan_describe"):
+    lib.fxtx_multi_plan_describe.argtypes = [i32, i64, i64, i64, i64, i32, ctypes.c_char_p, i64]
+    for name in ("fxtx_dense_f32", "fxtx_dense_f64", "fxtx_dense_f32_noalloc", "fxtx_dense_bf16", "fxtx_dense_multi_f32",
+                 "fxtx_dense_multi_f64", "fxtx_csr_f32", "fxtx_csr_f64", "fxtx_csr_validate", "fxtx_device_error",
+                 "fxtx_plan_describe", "fxtx_multi_plan_describe"):
         getattr(lib, name).restype = i32
     return lib
 
@@ -49,11 +53,14 @@ fxtx_dense_f32 = _lib.fxtx_dense_f32
 fxtx_dense_f64 = _lib.fxtx_dense_f64
 fxtx_dense_f32_noalloc = _lib.fxtx_dense_f32_noalloc
 fxtx_dense_bf16 = _lib.fxtx_dense_bf16
+fxtx_dense_multi_f32 = _lib.fxtx_dense_multi_f32
+fxtx_dense_multi_f64 = _lib.fxtx_dense_multi_f64
 fxtx_csr_f32 = _lib.fxtx_csr_f32
 fxtx_csr_f64 = _lib.fxtx_csr_f64
 fxtx_csr_validate = _lib.fxtx_csr_validate
 fxtx_device_error = _lib.fxtx_device_error
 fxtx_plan_describe = _lib.fxtx_plan_describe
+fxtx_multi_plan_describe = _lib.fxtx_multi_plan_describe
 
 
 def fxtx_status_string(status: int) -> str:
@@ -76,6 +83,15 @@ def plan_describe(kind: str, dtype: str, m: int, n: int, nnz: int = 0, ld: int |
     buf = ctypes.create_string_buffer(512)
     _check(fxtx_plan_describe(1 if kind == "csr" else 0, 1 if dtype in ("f64", "float64") else 0, m, n, nnz,
                               n if ld is None else ld, buf, 512), "fxtx_plan_describe")
+    return buf.value.decode()
+
+
+def multi_plan_describe(dtype: str, m: int, n: int, k: int, v_mode: str = "full", ld: int | None = None) -> str:
+    """The launch plan of a multi-vector call (host only); v_mode "none", "shared" or "full"."""
+    buf = ctypes.create_string_buffer(512)
+    vm = {"none": 0, "shared": 1, "full": 2}[v_mode]
+    _check(fxtx_multi_plan_describe(1 if dtype in ("f64", "float64") else 0, m, n, k, n if ld is None else ld, vm,
+                                    buf, 512), "fxtx_multi_plan_describe")
     return buf.value.decode()
 
 
@@ -140,6 +156,56 @@ def dense(X, y, v=None, alpha: float = 1.0, beta: float = 0.0, z=None, out=None,
     else:
         raise TypeError(f"unsupported dtype {dt}")
     _check(rc, "fxtx_dense")
+    return out
+
+
+def _rows(t, dtype, shape, name, dev_index):
+    """A 2-D row-major CUDA tensor (unit column stride); returns its row stride."""
+    if (t.dtype is not dtype or not t.is_cuda or t.get_device() != dev_index or t.dim() != 2
+            or tuple(t.shape) != tuple(shape) or (shape[0] > 0 and shape[1] > 1 and t.stride(1) != 1)):
+        raise ValueError(f"{name}: expected a row-major {dtype} tensor of shape {tuple(shape)} on cuda:{dev_index}")
+    return t.stride(0) if shape[0] > 1 else max(shape[1], 1)
+
+
+def dense_multi(X, Y, V=None, alpha: float = 1.0, beta: float = 0.0, Z=None, out=None, stream=None):
+    """OUT = alpha * X^T (V * (X Y)) + beta * Z for k right-hand sides in one pass over X.
+
+    X (m, n) as in ``dense`` (float32 or float64); Y (n, k), Z (n, k) and ``out`` (n, k)
+    row-major. ``V`` is None (weights 1), an m-vector shared by every right-hand side,
+    or an (m, k) row-major matrix. Column slices with unit column stride are accepted.
+    """
+    torch = _torch()
+    if X.dim() != 2 or (X.shape[0] > 1 and X.shape[1] > 1 and X.stride(1) != 1) or not X.is_cuda:
+        raise ValueError("X: expected a 2-D CUDA tensor with unit column stride")
+    m, n = X.shape
+    ld = X.stride(0) if m > 1 else max(n, 1)
+    dt, di = X.dtype, X.get_device()
+    if Y.dim() != 2:
+        raise ValueError("Y: expected a 2-D tensor (n, k)")
+    k = Y.shape[1]
+    ldy = _rows(Y, dt, (n, k), "Y", di)
+    if V is None:
+        ldv = 0
+    elif V.dim() == 1:
+        _vec(V, dt, m, "V", di)
+        ldv = 0
+    else:
+        ldv = _rows(V, dt, (m, k), "V", di)
+        ldv = max(ldv, k)
+    ldz = 0 if Z is None else _rows(Z, dt, (n, k), "Z", di)
+    if out is None:
+        out = torch.empty((n, k), dtype=dt, device=X.device)
+    ldo = _rows(out, dt, (n, k), "out", di)
+    st = _stream(stream, X.device)
+    if dt == torch.float32:
+        fn = fxtx_dense_multi_f32
+    elif dt == torch.float64:
+        fn = fxtx_dense_multi_f64
+    else:
+        raise TypeError(f"unsupported dtype {dt}")
+    rc = fn(m, n, k, _ptr(X), ld, _ptr(Y), max(ldy, k), _ptr(V), ldv, alpha, beta, _ptr(Z), max(ldz, k) if Z is not None else 0,
+            _ptr(out), max(ldo, k), st)
+    _check(rc, "fxtx_dense_multi")
     return out
 
 

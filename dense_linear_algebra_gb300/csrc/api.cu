@@ -8,6 +8,7 @@
 
 #include "fxtx.h"
 #include "kernels.h"
+#include "multi.h"
 #include "plan.h"
 
 namespace fxtx {
@@ -211,6 +212,62 @@ fxtx_status_t csr_impl(int64_t m, int64_t n, int64_t nnz, const int64_t* row_ptr
   return FXTX_OK;
 }
 
+// k right-hand sides: ceil(k / kb) passes over X, each for kb of them.
+template <typename T>
+fxtx_status_t dense_multi_impl(int64_t m, int64_t n, int64_t k, const T* X, int64_t ld, const T* Y, int64_t ldy,
+                               const T* V, int64_t ldv, T alpha, T beta, const T* Z, int64_t ldz, T* OUT,
+                               int64_t ldo, void* stream) {
+  if (m < 0 || n < 0 || k < 0) return FXTX_ERR_INVALID_ARG;
+  if (n == 0 || k == 0) return FXTX_OK;
+  if (ld < n || Y == nullptr || OUT == nullptr || ldy < k || ldo < k) return FXTX_ERR_INVALID_ARG;
+  if (m > 0 && X == nullptr) return FXTX_ERR_INVALID_ARG;
+  if (V != nullptr && ldv != 0 && ldv < k) return FXTX_ERR_INVALID_ARG;
+  if (ldv < 0) return FXTX_ERR_INVALID_ARG;
+  const bool use_z = Z != nullptr && beta != T(0);
+  if (use_z && ldz < k) return FXTX_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  fxtx_status_t s = current_device(&dev);
+  if (s != FXTX_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  const int elem = (int)sizeof(T);
+  const bool tma_ok = aligned16(X) && (ld * elem) % 16 == 0;
+  const MultiPlan plan = plan_multi(*dev, m, n, k, elem, tma_ok, V != nullptr && ldv != 0, V != nullptr);
+  if (!plan.ok) return FXTX_ERR_UNSUPPORTED;
+  if (log_enabled()) {
+    char buf[256];
+    describe_multi(plan, buf, sizeof buf);
+    fprintf(stderr, "[fxtx] m=%lld n=%lld k=%lld ld=%lld %s\n", (long long)m, (long long)n, (long long)k,
+            (long long)ld, buf);
+  }
+
+  void* ws = nullptr;
+  s = alloc_ws(&ws, plan.ws_bytes, st);
+  if (s != FXTX_OK) return s;
+  MultiArgs<T> a;
+  a.m = m; a.n = n; a.ld = ld; a.X = X;
+  a.ldy = ldy; a.ldv = V != nullptr ? ldv : 0; a.ldz = ldz; a.ldo = ldo;
+  a.alpha = (double)alpha; a.beta = (double)beta; a.use_z = use_z;
+  a.tiles = (m + plan.rows_per_tile - 1) / plan.rows_per_tile;
+  a.ws = static_cast<double*>(ws);
+  a.ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + plan.ws_bytes - 128);
+  cudaError_t e = cudaMemsetAsync(a.ticket, 0, sizeof(unsigned), st);
+  for (int64_t c0 = 0; c0 < k && e == cudaSuccess; c0 += a.kb) {
+    a.kb = multi_pass_kb(plan, k, c0);
+    a.Y = Y + c0;
+    a.V = V == nullptr ? nullptr : (ldv != 0 ? V + c0 : V);
+    a.Z = use_z ? Z + c0 : nullptr;
+    a.OUT = OUT + c0;
+    e = launch_multi<T>(plan, a, st);
+  }
+  cudaFreeAsync(ws, st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FXTX_ERR_CUDA;
+  }
+  return FXTX_OK;
+}
+
 }  // namespace
 }  // namespace fxtx
 
@@ -231,6 +288,18 @@ fxtx_status_t fxtx_dense_f64(int64_t m, int64_t n, const double* X, int64_t ld, 
 fxtx_status_t fxtx_dense_bf16(int64_t m, int64_t n, const uint16_t* X, int64_t ld, const float* y, const float* v,
                               float alpha, float beta, const float* z, float* out, void* stream) {
   return dense_bf16_impl(m, n, reinterpret_cast<const __nv_bfloat16*>(X), ld, y, v, alpha, beta, z, out, stream);
+}
+
+fxtx_status_t fxtx_dense_multi_f32(int64_t m, int64_t n, int64_t k, const float* X, int64_t ld, const float* Y,
+                                   int64_t ldy, const float* V, int64_t ldv, float alpha, float beta, const float* Z,
+                                   int64_t ldz, float* OUT, int64_t ldo, void* stream) {
+  return dense_multi_impl<float>(m, n, k, X, ld, Y, ldy, V, ldv, alpha, beta, Z, ldz, OUT, ldo, stream);
+}
+
+fxtx_status_t fxtx_dense_multi_f64(int64_t m, int64_t n, int64_t k, const double* X, int64_t ld, const double* Y,
+                                   int64_t ldy, const double* V, int64_t ldv, double alpha, double beta,
+                                   const double* Z, int64_t ldz, double* OUT, int64_t ldo, void* stream) {
+  return dense_multi_impl<double>(m, n, k, X, ld, Y, ldy, V, ldv, alpha, beta, Z, ldz, OUT, ldo, stream);
 }
 
 fxtx_status_t fxtx_csr_f32(int64_t m, int64_t n, int64_t nnz, const int64_t* row_ptr, const int32_t* col_idx,
@@ -277,11 +346,12 @@ fxtx_status_t fxtx_device_error(void* stream) {
   }
   const int a = take_dense_device_error();
   const int b = take_csr_device_error();
-  if (a < 0 || b < 0) {
+  const int c = take_multi_device_error();
+  if (a < 0 || b < 0 || c < 0) {
     cudaGetLastError();
     return FXTX_ERR_CUDA;
   }
-  return (a || b) ? FXTX_ERR_TIMEOUT : FXTX_OK;
+  return (a || b || c) ? FXTX_ERR_TIMEOUT : FXTX_OK;
 }
 
 const char* fxtx_status_string(fxtx_status_t status) {
@@ -321,6 +391,25 @@ fxtx_status_t fxtx_plan_describe(int is_csr, int is_f64, int64_t m, int64_t n, i
     const bool tile_ok = (l * elem) % 16 == 0;
     describe(plan_dense(*dev, m, n, l, elem, tile_ok && (n * elem) % 16 == 0, tile_ok), buf, (size_t)cap);
   }
+  return FXTX_OK;
+}
+
+fxtx_status_t fxtx_multi_plan_describe(int is_f64, int64_t m, int64_t n, int64_t k, int64_t ld, int v_mode, char* buf,
+                                       int64_t cap) {
+  if (buf == nullptr || cap <= 0 || m < 0 || n < 0 || k < 0 || v_mode < 0 || v_mode > 2) return FXTX_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  DeviceInfo fallback;
+  if (current_device(&dev) != FXTX_OK) {
+    fallback.sm_count = 152;
+    fallback.cc_major = 10;
+    fallback.cc_minor = 3;
+    fallback.smem_optin = 232448;
+    fallback.smem_per_sm = 233472;
+    dev = &fallback;
+  }
+  const int elem = is_f64 ? 8 : 4;
+  const int64_t l = ld < n ? n : ld;
+  describe_multi(plan_multi(*dev, m, n, k, elem, (l * elem) % 16 == 0, v_mode == 2, v_mode != 0), buf, (size_t)cap);
   return FXTX_OK;
 }
 

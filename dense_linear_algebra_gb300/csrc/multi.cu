@@ -1,0 +1,452 @@
+// multi.cu — the multi-vector instantiation OUT = alpha * X^T (V ⊙ (X Y)) + beta * Z
+// (declared in multi.h): one pass over X serves kb right-hand sides at once.
+//
+// "On optimizing machine learning workloads via kernel fusion" (abstract): the fused
+// pattern and its instantiations. Each right-hand side c is the single-vector pattern
+// with y = Y[:, c], v = V[:, c] and z = Z[:, c]; reading X once for all of them raises
+// the arithmetic intensity kb-fold, so small kb stays on the HBM roof and large kb
+// moves to the FMA roof.
+//
+// Tiles of R rows of X arrive in shared memory as in the single-vector tile kernel
+// (2-D tensor copies, 128-byte swizzle, a 3- or 4-deep pipeline per warp). The warp's
+// lanes split three ways: lane = cg + KB * (jg + NB * rs). Lane (rs, jg, cg) keeps in
+// registers the eight 16-byte chunks jg, jg + NB, ... of Y's rows for right-hand side
+// cg, and per row it reads the same eight chunks of X. The NB lanes of a row sum their
+// partial dots with shuffles; each lane then has t = v * (x . y_cg) and adds t * x into
+// its own column sums. No dot needs another right-hand side's data, so no lane holds
+// more than one right-hand side.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "multi.h"
+#include "tmap.h"
+
+namespace fxtx {
+namespace {
+
+constexpr int MULTI_THREADS = 256;
+constexpr size_t MULTI_SMEM_BUDGET = 220 * 1024;
+
+template <typename T>
+struct Chunk;
+template <>
+struct Chunk<float> {
+  static constexpr CUtensorMapDataType MAP = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  __device__ static __forceinline__ void unpack(const uint4& u, float* e) {
+    e[0] = __uint_as_float(u.x); e[1] = __uint_as_float(u.y); e[2] = __uint_as_float(u.z); e[3] = __uint_as_float(u.w);
+  }
+};
+template <>
+struct Chunk<double> {
+  static constexpr CUtensorMapDataType MAP = CU_TENSOR_MAP_DATA_TYPE_FLOAT64;
+  __device__ static __forceinline__ void unpack(const uint4& u, double* e) {
+    e[0] = __hiloint2double((int)u.y, (int)u.x);
+    e[1] = __hiloint2double((int)u.w, (int)u.z);
+  }
+};
+
+// Geometry for rows of NB 128-byte blocks and KB right-hand sides per pass.
+template <typename T, int NB, int KB>
+struct MShape {
+  static constexpr int NV = 16 / (int)sizeof(T);  // elements per chunk
+  static constexpr int Q = 8;                     // chunks per lane
+  static constexpr int C = Q * NV;                // columns per lane
+  static constexpr int RS = 32 / (NB * KB);       // row slots of a warp
+  static constexpr int R = NB >= 4 ? 8 : 32 / NB; // rows per tile
+  static constexpr int IT = R / RS;               // rows per lane per tile
+  static constexpr int BOX = R * 128;             // bytes of one 128-byte column block of a tile
+  static constexpr int TILE = NB * BOX;           // bytes of one pipeline stage
+  // Row order inside a tile. The RS rows read at once must fall in different
+  // 128-byte-swizzle phases beyond what the NB lanes of a row already cover: row
+  // index bits are rotated left by log2(NB) when NB < 8.
+  static constexpr int LOGR = NB >= 4 ? 3 : (NB == 2 ? 4 : 5);
+  static constexpr int ROT = NB == 2 ? 1 : (NB == 4 ? 2 : 0);
+  static_assert(NB * KB <= 32 && RS >= 1 && R % RS == 0, "lane split");
+};
+
+template <int R, int LOGR, int ROT>
+__device__ __forceinline__ int tile_row(int idx) {
+  if constexpr (ROT == 0) return idx;
+  else return ((idx << ROT) | (idx >> (LOGR - ROT))) & (R - 1);
+}
+
+// Byte offset of chunk ch of tile row r (128-byte swizzle: chunk c of a block row
+// sits at position c ^ (r mod 8)).
+template <int BOX>
+__device__ __forceinline__ int chunk_offset(int r, int ch) {
+  return (ch >> 3) * BOX + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+}
+
+// Element-sized asynchronous copy global -> shared (no alignment beyond the element's).
+template <typename T>
+__device__ __forceinline__ void cp_async_elem(T* dst, const T* src) {
+  if constexpr (sizeof(T) == 4)
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+  else
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Sums a value over the NB lanes of a row (lanes KB apart).
+template <typename T, int NB, int KB>
+__device__ __forceinline__ T row_sum(T s) {
+#pragma unroll
+  for (int o = KB; o < KB * NB; o <<= 1) s += __shfl_xor_sync(FULL_MASK, s, o);
+  return s;
+}
+
+// Sums a compensated (s, c) pair over the NB lanes of a row.
+template <int NB, int KB>
+__device__ __forceinline__ float row_sum_comp(float s, float c) {
+#pragma unroll
+  for (int o = KB; o < KB * NB; o <<= 1) {
+    const float s2 = __shfl_xor_sync(FULL_MASK, s, o), c2 = __shfl_xor_sync(FULL_MASK, c, o);
+    float t, q;
+    two_sum(s, s2, t, q);
+    s = t;
+    c = __fadd_rn(__fadd_rn(c, c2), q);
+  }
+  return __fadd_rn(s, c);
+}
+
+// CTA partials -> workspace; the last CTA to arrive sums them in a fixed order and
+// writes OUT = alpha * W + beta * Z for the pass's kb right-hand sides.
+template <typename T, int KB>
+__device__ __forceinline__ void multi_finish(const MultiArgs<T>& a, double* red, const int nw) {
+  __shared__ unsigned s_last;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t N = a.n * KB;
+  __syncthreads();
+  for (int64_t e = threadIdx.x; e < N; e += blockDim.x) {
+    double s = 0.0;
+    for (int w = 0; w < nw; ++w) s += red[w * N + e];
+    a.ws[blockIdx.x * N + e] = s;
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = (atomicAdd(a.ticket, 1u) == gridDim.x - 1) ? 1u : 0u;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int nc = gridDim.x;
+  const int cb = nc * warp / nw, ce = nc * (warp + 1) / nw;
+  for (int64_t e = lane; e < N; e += 32) {
+    double s = 0.0;
+    for (int c = cb; c < ce; ++c) s += __ldcg(a.ws + (int64_t)c * N + e);
+    red[warp * N + e] = s;
+  }
+  __syncthreads();
+  for (int64_t e = threadIdx.x; e < N; e += blockDim.x) {
+    const int64_t col = e / KB;
+    const int c = (int)(e % KB);
+    if (c >= a.kb) continue;
+    double s = 0.0;
+    for (int w = 0; w < nw; ++w) s += red[w * N + e];
+    double o = a.alpha * s;
+    if (a.use_z) o += a.beta * (double)a.Z[col * a.ldz + c];
+    a.OUT[col * a.ldo + c] = (T)o;
+  }
+  if (threadIdx.x == 0) *a.ticket = 0u;
+}
+
+// vmode: 0 no weights, 1 one shared m-vector, 2 an (m x k) matrix.
+template <typename T, int NB, int KB>
+__global__ void __launch_bounds__(MULTI_THREADS, 1)
+    dense_multi_kernel(const __grid_constant__ CUtensorMap tmap, const MultiArgs<T> a, const int S, const int tma,
+                       const int vmode) {
+  using SH = MShape<T, NB, KB>;
+  constexpr int NV = SH::NV, Q = SH::Q, C = SH::C, RS = SH::RS, R = SH::R, IT = SH::IT;
+  constexpr int BOX = SH::BOX, TILE = SH::TILE;
+  // fp32 rows longer than 64 entries (NB >= 4) take the compensated dot
+  constexpr bool COMP = sizeof(T) == 4 && NB >= 4;
+  // fp32: plain per-lane column sums over about 32 rows, then folded into a two-float sum
+  constexpr int FOLD = IT >= 32 ? 1 : 32 / IT;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int cg = lane % KB, jg = (lane / KB) % NB, rs = lane / (KB * NB);
+  const int64_t n = a.n, m = a.m;
+  const int VB = vmode == 2 ? R * KB : (vmode == 1 ? R : 0);  // weights per tile
+
+  unsigned char* stages = smem + (size_t)warp * S * TILE;
+  T* vbuf = reinterpret_cast<T*>(smem + (size_t)nw * S * TILE) + (size_t)warp * 2 * VB;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)nw * S * TILE + (size_t)nw * 2 * VB * sizeof(T)) + warp * S;
+
+  // this lane's slice of Y: columns of chunks jg + q NB, right-hand side cg
+  T yr[C];
+#pragma unroll
+  for (int q = 0; q < Q; ++q)
+#pragma unroll
+    for (int e = 0; e < NV; ++e) {
+      const int64_t col = (int64_t)(jg + q * NB) * NV + e;
+      yr[q * NV + e] = (col < n && cg < a.kb) ? ldg(a.Y + col * a.ldy + cg) : T(0);
+    }
+
+  const int64_t gw = (int64_t)blockIdx.x * nw + warp, W = (int64_t)gridDim.x * nw;
+  const int64_t t0 = a.tiles * gw / W, t1 = a.tiles * (gw + 1) / W, nt = t1 - t0;
+  const uint64_t pol = policy_evict_first();
+
+  auto issue = [&](int64_t tile, int s) {
+    if (lane == 0) mbar_arrive_expect_tx(&bars[s], (uint32_t)TILE);
+    __syncwarp();
+    if (lane < NB) tma_load_2d(stages + (size_t)s * TILE + lane * BOX, &tmap, lane * (128 / (int)sizeof(T)),
+                               (int)(tile * R), &bars[s], pol);
+  };
+  // weights of one tile into buffer `slot` (asynchronous; zeros past the last row)
+  auto stage_v = [&](int64_t tile, int slot) {
+    T* vb = vbuf + slot * VB;
+    for (int e = lane; e < VB; e += 32) {
+      const int r = vmode == 2 ? e / KB : e, c = vmode == 2 ? e % KB : 0;
+      const int64_t row = tile * R + r;
+      if (row < m && c < a.kb)
+        cp_async_elem(vb + e, a.V + (vmode == 2 ? row * a.ldv + c : row));
+      else
+        vb[e] = T(0);
+    }
+  };
+  // X of one tile by plain loads, in the layout the tensor copy would give
+  auto load_direct = [&](int64_t tile, unsigned char* stage) {
+    constexpr int CPR = NB * 8;
+    for (int idx = lane; idx < R * CPR; idx += 32) {
+      const int r = idx / CPR, ch = idx % CPR;
+      const int64_t row = tile * R + r;
+      alignas(16) T e[NV];
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const int64_t col = (int64_t)ch * NV + i;
+        e[i] = (row < m && col < n) ? ldg(a.X + row * a.ld + col) : T(0);
+      }
+      *reinterpret_cast<uint4*>(stage + chunk_offset<BOX>(r, ch)) = *reinterpret_cast<const uint4*>(e);
+    }
+  };
+
+  if (tma) {
+    if (lane == 0) {
+      for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+      fence_mbar_init();
+    }
+    __syncwarp();
+    for (int s = 0; s < S && s < nt; ++s) issue(t0 + s, s);
+  }
+  if (vmode && nt > 0) stage_v(t0, 0);
+  cp_async_commit();
+
+  typename OuterAcc<T>::type acc[C];
+  T tacc[C];
+#pragma unroll
+  for (int c = 0; c < C; ++c) tacc[c] = T(0);
+
+  for (int64_t k = 0; k < nt; ++k) {
+    const int64_t tile = t0 + k;
+    if (vmode && k + 1 < nt) stage_v(tile + 1, (int)((k + 1) & 1));
+    cp_async_commit();
+    cp_async_wait<1>();  // this tile's weights have landed (this lane's copies)
+
+    const int s = tma ? (int)(k % S) : 0;
+    unsigned char* stage = stages + (size_t)s * TILE;
+    if (tma) {
+      const bool ok = mbar_wait_bounded(&bars[s], (uint32_t)((k / S) & 1));
+      if (__any_sync(FULL_MASK, !ok)) {
+        if (lane == 0)
+          for (int64_t j = k + 1; j < nt && j < k + S; ++j) mbar_wait_bounded(&bars[j % S], (uint32_t)((j / S) & 1));
+        break;
+      }
+    } else {
+      load_direct(tile, stage);
+    }
+    __syncwarp();  // every lane's weights and (direct path) X are visible to the warp
+    const T* vb = vbuf + (int)(k & 1) * VB;
+
+#pragma unroll 1
+    for (int it = 0; it < IT; ++it) {
+      const int r = tile_row<R, SH::LOGR, SH::ROT>(it * RS + rs);
+      T x[C];
+#pragma unroll
+      for (int q = 0; q < Q; ++q) {
+        const uint4 u = *reinterpret_cast<const uint4*>(stage + chunk_offset<BOX>(r, jg + q * NB));
+        Chunk<T>::unpack(u, &x[q * NV]);
+      }
+      T d;
+      if constexpr (COMP) {
+        DotAcc<float, true> dacc;
+#pragma unroll
+        for (int c = 0; c < C; ++c) dacc.add(x[c], yr[c]);
+        d = row_sum_comp<NB, KB>(dacc.s, dacc.c);
+      } else {
+        T d4[4] = {T(0), T(0), T(0), T(0)};
+#pragma unroll
+        for (int c = 0; c < C; ++c) d4[c & 3] = fma(x[c], yr[c], d4[c & 3]);
+        d = row_sum<T, NB, KB>((d4[0] + d4[1]) + (d4[2] + d4[3]));
+      }
+      const T t = vmode == 0 ? d : vb[vmode == 2 ? r * KB + cg : r] * d;
+#pragma unroll
+      for (int c = 0; c < C; ++c) tacc[c] = fma(t, x[c], tacc[c]);
+    }
+    if constexpr (sizeof(T) == 4) {
+      if ((k + 1) % FOLD == 0 || k + 1 == nt) {
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+          acc[c].add(tacc[c]);
+          tacc[c] = T(0);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < C; ++c) {
+        acc[c].add(tacc[c]);
+        tacc[c] = T(0);
+      }
+    }
+    __syncwarp();
+    if (tma && k + S < nt) {
+      fence_proxy_async_smem();
+      issue(tile + S, s);
+    }
+  }
+  cp_async_wait<0>();
+
+  // lane -> warp: lanes with the same (jg, cg) hold the same entries
+  double part[C];
+#pragma unroll
+  for (int c = 0; c < C; ++c) part[c] = acc[c].value();
+#pragma unroll
+  for (int o = KB * NB; o < 32; o <<= 1)
+#pragma unroll
+    for (int c = 0; c < C; ++c) part[c] += shfl_xor(part[c], o);
+
+  __syncthreads();
+  double* red = reinterpret_cast<double*>(smem);  // [nw][n][KB]
+  const int64_t N = n * KB;
+  if (rs == 0) {
+#pragma unroll
+    for (int q = 0; q < Q; ++q)
+#pragma unroll
+      for (int e = 0; e < NV; ++e) {
+        const int64_t col = (int64_t)(jg + q * NB) * NV + e;
+        if (col < n) red[warp * N + col * KB + cg] = part[q * NV + e];
+      }
+  }
+  multi_finish<T, KB>(a, red, nw);
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------------------------
+static int pow2ceil(int64_t x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+static int multi_rows(int nb) { return nb >= 4 ? 8 : 32 / nb; }
+
+MultiPlan plan_multi(const DeviceInfo& dev, int64_t m, int64_t n, int64_t k, int elem, bool tma_ok, bool full_v,
+                     bool has_v) {
+  MultiPlan p;
+  if (n <= 0 || k <= 0 || n * elem > 2048) return p;
+  p.ok = true;
+  p.nb = pow2ceil((n * elem + 127) / 128);
+  p.kb_max = (int)std::min<int64_t>(32 / p.nb, pow2ceil(k));
+  p.passes = (int)((k + p.kb_max - 1) / p.kb_max);
+  p.rows_per_tile = multi_rows(p.nb);
+  // m == 0 runs the same kernel over no tiles (it writes beta Z); tensor maps need m > 0
+  p.tma = tma_ok && m > 0 && m < (int64_t(1) << 31);
+  const size_t tile = (size_t)p.nb * p.rows_per_tile * 128;
+  const size_t vb = full_v ? (size_t)p.rows_per_tile * p.kb_max : (has_v ? (size_t)p.rows_per_tile : 0);
+  const size_t vbytes = 2 * vb * elem;
+  const size_t budget = std::min<size_t>(MULTI_SMEM_BUDGET, dev.smem_optin > 0 ? (size_t)dev.smem_optin : MULTI_SMEM_BUDGET);
+  // eight warps with a pipeline of 2 to 4 tiles each; four warps where eight do not fit (16 KB tiles)
+  p.warps = MULTI_THREADS / 32;
+  if (p.tma) {
+    for (;;) {
+      const size_t room = budget - 1024 - p.warps * vbytes;
+      p.stages = (int)std::min<size_t>(4, room / (p.warps * (tile + 8)));
+      if (p.stages >= 2 || p.warps == 4) break;
+      p.warps = 4;
+    }
+  } else {
+    p.stages = 1;
+  }
+  const size_t pipe = 1024 + p.warps * (p.stages * (tile + 8) + vbytes);
+  const size_t red = 1024 + (size_t)p.warps * n * p.kb_max * sizeof(double);
+  p.smem = std::max(pipe, red);
+  const int64_t tiles = (m + p.rows_per_tile - 1) / p.rows_per_tile;
+  p.ctas = (int)std::max<int64_t>(1, std::min<int64_t>(dev.sm_count, (tiles + p.warps - 1) / p.warps));
+  p.ws_bytes = (size_t)p.ctas * n * p.kb_max * sizeof(double) + 128;
+  return p;
+}
+
+int multi_pass_kb(const MultiPlan& p, int64_t k, int64_t c0) {
+  return (int)std::min<int64_t>(p.kb_max, k - c0);
+}
+
+int describe_multi(const MultiPlan& p, char* buf, size_t cap) {
+  return snprintf(buf, cap, "multi ok=%d tma=%d blocks=%d kb=%d passes=%d rows_per_tile=%d stages=%d warps=%d ctas=%d smem=%zu ws=%zu",
+                  (int)p.ok, (int)p.tma, p.nb, p.kb_max, p.passes, p.rows_per_tile, p.stages, p.warps, p.ctas, p.smem,
+                  p.ws_bytes);
+}
+
+int take_multi_device_error() { return take_device_error(); }
+
+template <typename T, int NB, int KB>
+static cudaError_t launch_kb(const MultiPlan& p, const CUtensorMap& map, const MultiArgs<T>& a, int vmode,
+                             cudaStream_t st) {
+  const void* kern = (const void*)dense_multi_kernel<T, NB, KB>;
+  cudaError_t e = ensure_smem(kern, p.smem);
+  if (e != cudaSuccess) return e;
+  dense_multi_kernel<T, NB, KB><<<p.ctas, p.warps * 32, p.smem, st>>>(map, a, p.stages, p.tma ? 1 : 0, vmode);
+  return cudaGetLastError();
+}
+
+template <typename T, int NB>
+static cudaError_t launch_nb(const MultiPlan& p, const CUtensorMap& map, const MultiArgs<T>& a, int vmode,
+                             cudaStream_t st) {
+  switch (pow2ceil(a.kb)) {
+    case 1: return launch_kb<T, NB, 1>(p, map, a, vmode, st);
+    case 2: return launch_kb<T, NB, 2>(p, map, a, vmode, st);
+    case 4: if constexpr (NB <= 8) return launch_kb<T, NB, 4>(p, map, a, vmode, st); break;
+    case 8: if constexpr (NB <= 4) return launch_kb<T, NB, 8>(p, map, a, vmode, st); break;
+    case 16: if constexpr (NB <= 2) return launch_kb<T, NB, 16>(p, map, a, vmode, st); break;
+    case 32: if constexpr (NB == 1) return launch_kb<T, NB, 32>(p, map, a, vmode, st); break;
+    default: break;
+  }
+  return cudaErrorInvalidConfiguration;
+}
+
+template <typename T>
+cudaError_t launch_multi(const MultiPlan& p, const MultiArgs<T>& a, cudaStream_t st) {
+  if (!p.ok || a.kb < 1 || a.kb > p.kb_max) return cudaErrorInvalidConfiguration;
+  CUtensorMap map;
+  memset(&map, 0, sizeof map);
+  // a map the driver refuses sends the pass to the plain-load staging
+  MultiPlan q = p;
+  q.tma = p.tma && encode_rows_map(&map, Chunk<T>::MAP, a.X, a.m, a.n, a.ld * (int64_t)sizeof(T), (int)sizeof(T),
+                                   p.rows_per_tile, 128);
+  const int vmode = a.V == nullptr ? 0 : (a.ldv == 0 ? 1 : 2);
+  switch (p.nb) {
+    case 1: return launch_nb<T, 1>(q, map, a, vmode, st);
+    case 2: return launch_nb<T, 2>(q, map, a, vmode, st);
+    case 4: return launch_nb<T, 4>(q, map, a, vmode, st);
+    case 8: return launch_nb<T, 8>(q, map, a, vmode, st);
+    case 16: return launch_nb<T, 16>(q, map, a, vmode, st);
+    default: return cudaErrorInvalidConfiguration;
+  }
+}
+
+template cudaError_t launch_multi<float>(const MultiPlan&, const MultiArgs<float>&, cudaStream_t);
+template cudaError_t launch_multi<double>(const MultiPlan&, const MultiArgs<double>&, cudaStream_t);
+
+}  // namespace fxtx

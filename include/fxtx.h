@@ -87,6 +87,41 @@ fxtx_status_t fxtx_dense_bf16(int64_t m, int64_t n, const uint16_t* X, int64_t l
                               void* stream);
 
 /*
+ * Multi-vector instantiation: k right-hand sides in one pass over dense X.
+ * ("On optimizing machine learning workloads via kernel fusion", abstract: the
+ * fused pattern and its instantiations, here with k vectors y at once.)
+ *
+ *     OUT[:, c] = alpha * X^T (V[:, c] * (X Y[:, c])) + beta * Z[:, c],  c = 0 .. k-1
+ *
+ * X as in fxtx_dense_f32 (m x n, row pitch ld >= n). Y, Z and OUT are n x k,
+ * row-major: entry (j, c) at Y[j * ldy + c], Z[j * ldz + c], OUT[j * ldo + c],
+ * with ldy, ldz, ldo >= k. V holds the row weights:
+ *   V == NULL          all weights 1;
+ *   ldv == 0           V is one m-vector, V[i], shared by every right-hand side;
+ *   ldv >= k           V is m x k, entry (i, c) at V[i * ldv + c].
+ * Z is read only when beta != 0 (it may then be NULL). OUT may equal Z with
+ * ldo == ldz (in place); any other overlap of OUT with an input is undefined.
+ *
+ * Shapes: rows of at most 2 KB (n <= 512 in fp32, n <= 256 in fp64); wider
+ * rows return FXTX_ERR_UNSUPPORTED. Each pass over X takes up to 32 / b
+ * right-hand sides, b = the row's 128-byte blocks rounded up to a power of
+ * two (32 for n <= 32 fp32 or n <= 16 fp64); larger k runs ceil(k / that)
+ * passes. X 16-byte aligned with ld * sizeof(T) a multiple of 16 is staged by
+ * tensor copies; otherwise by plain loads. m, n, k >= 0; n == 0 or k == 0 does
+ * nothing; m == 0 gives OUT = beta * Z (or 0).
+ *
+ * Each column c meets the bound of fxtx_dense_f32 / _f64 with its own
+ * S_jc = |alpha| sum_i |t_ic| |X_ij| + |beta Z_jc|, t_ic = V_ic (x_i . Y[:, c]).
+ * Workspace, streams, determinism and errors are those of fxtx_dense_f32.
+ */
+fxtx_status_t fxtx_dense_multi_f32(int64_t m, int64_t n, int64_t k, const float* X, int64_t ld, const float* Y,
+                                   int64_t ldy, const float* V, int64_t ldv, float alpha, float beta, const float* Z,
+                                   int64_t ldz, float* OUT, int64_t ldo, void* stream);
+fxtx_status_t fxtx_dense_multi_f64(int64_t m, int64_t n, int64_t k, const double* X, int64_t ld, const double* Y,
+                                   int64_t ldy, const double* V, int64_t ldv, double alpha, double beta,
+                                   const double* Z, int64_t ldz, double* OUT, int64_t ldo, void* stream);
+
+/*
  * fxtx_dense_f32 without any device allocation at call time. (The paper has no
  * counterpart: this entry point exists for callers that cannot allocate.)
  *
@@ -160,6 +195,14 @@ const char* fxtx_status_string(fxtx_status_t status);
  */
 fxtx_status_t fxtx_plan_describe(int is_csr, int is_f64, int64_t m, int64_t n, int64_t nnz,
                                   int64_t ld, char* buf, int64_t cap);
+
+/*
+ * The launch plan of a multi-vector call (fxtx_dense_multi_*), for logging and
+ * tests: v_mode 0 = no weights, 1 = one shared m-vector, 2 = an m x k matrix.
+ * Host only; writes a NUL-terminated description of at most `cap` bytes.
+ */
+fxtx_status_t fxtx_multi_plan_describe(int is_f64, int64_t m, int64_t n, int64_t k, int64_t ld, int v_mode, char* buf,
+                                       int64_t cap);
 
 #ifdef __cplusplus
 }

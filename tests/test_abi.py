@@ -92,3 +92,51 @@ def test_launch_model_grid_and_smem_limits():
     d = fx.plan_describe("dense", "f32", 100, 32)  # few rows: a CTA per few tiles
     fields = dict(kv.split("=") for kv in d.split()[1:])
     assert int(fields["ctas"]) == 1
+
+
+@pytest.mark.parametrize(
+    "args,expect",
+    [
+        (("f32", 16_000_000, 32, 8), "tma=1 blocks=1 kb=8 passes=1 rows_per_tile=32 stages=4 warps=8 ctas=152"),
+        (("f32", 16_000_000, 32, 40), "kb=32 passes=2"),
+        (("f32", 1000, 32, 3), "kb=4 passes=1"),
+        (("f64", 1000, 128, 8, "shared"), "blocks=8 kb=4 passes=2 rows_per_tile=8"),
+        (("f32", 1000, 512, 8, "none"), "blocks=16 kb=2 passes=4 rows_per_tile=8 stages=3 warps=4"),
+        (("f32", 1000, 513, 8), "ok=0"),
+        (("f64", 0, 17, 8), "tma=0"),
+        (("f32", 1000, 32, 8, "full", 33), "tma=0 blocks=1 kb=8"),
+    ],
+)
+def test_multi_launch_model(args, expect):
+    desc = fx.multi_plan_describe(*args)
+    assert expect in desc, desc
+
+
+def test_multi_plans_fit_shared_memory():
+    """Every shape the multi-vector entry takes plans within the 227 KB per-CTA limit,
+    with at least two pipeline stages when tensor copies stage X."""
+    for dt, elem in (("f32", 4), ("f64", 8)):
+        for n in (1, 16, 17, 32, 33, 64, 65, 128, 129, 256, 257, 512):
+            if n * elem > 2048:
+                continue
+            for k in (1, 3, 8, 16, 32, 33, 100):
+                for vm in ("none", "shared", "full"):
+                    f = dict(kv.split("=") for kv in fx.multi_plan_describe(dt, 10**6, n, k, vm).split()[1:])
+                    assert f["ok"] == "1" and int(f["smem"]) <= 227 * 1024, (dt, n, k, vm, f)
+                    tma = (n * elem) % 16 == 0  # ld = n: a 16-byte pitch is needed for tensor copies
+                    assert f["tma"] == ("1" if tma else "0") and int(f["stages"]) >= (2 if tma else 1)
+                    kb = int(f["kb"])
+                    assert kb & (kb - 1) == 0 and kb * int(f["blocks"]) <= 32
+                    assert int(f["passes"]) == -(-k // kb)
+
+
+def test_multi_invalid_arguments_rejected_on_host():
+    m32 = fx.fxtx_dense_multi_f32
+    assert m32(-1, 4, 2, None, 4, None, 2, None, 0, 1.0, 0.0, None, 0, None, 2, None) == fx.FXTX_ERR_INVALID_ARG
+    assert m32(4, 4, 2, 16, 4, 16, 1, None, 0, 1.0, 0.0, None, 0, 16, 2, None) == fx.FXTX_ERR_INVALID_ARG  # ldy < k
+    assert m32(4, 4, 2, 16, 4, 16, 2, None, 0, 1.0, 0.0, None, 0, 16, 1, None) == fx.FXTX_ERR_INVALID_ARG  # ldo < k
+    assert m32(4, 4, 2, 16, 4, 16, 2, 16, 1, 1.0, 0.0, None, 0, 16, 2, None) == fx.FXTX_ERR_INVALID_ARG  # 0 < ldv < k
+    assert m32(4, 4, 2, 16, 4, 16, 2, None, 0, 1.0, 1.0, 16, 1, 16, 2, None) == fx.FXTX_ERR_INVALID_ARG  # ldz < k
+    assert fx.fxtx_dense_multi_f64(4, 8, 2, None, 8, 16, 2, None, 0, 1.0, 0.0, None, 0, 16, 2, None) == fx.FXTX_ERR_INVALID_ARG
+    assert m32(4, 0, 2, None, 1, None, 2, None, 0, 1.0, 0.0, None, 0, None, 2, None) == fx.FXTX_OK  # n == 0
+    assert m32(4, 4, 0, None, 4, None, 0, None, 0, 1.0, 0.0, None, 0, None, 0, None) == fx.FXTX_OK  # k == 0
