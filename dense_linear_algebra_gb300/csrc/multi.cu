@@ -7,11 +7,11 @@
 // the arithmetic intensity kb-fold, so small kb stays on the HBM roof and large kb
 // moves to the FMA roof.
 //
-// Tiles of R rows of X arrive in shared memory as in the single-vector tile kernel
-// (2-D tensor copies, 128-byte swizzle, a 3- or 4-deep pipeline per warp). The warp's
-// lanes split three ways: lane = cg + KB * (jg + NB * rs). Lane (rs, jg, cg) keeps in
-// registers the eight 16-byte chunks jg, jg + NB, ... of Y's rows for right-hand side
-// cg, and per row it reads the same eight chunks of X. The NB lanes of a row sum their
+// Tiles of R rows of X arrive in shared memory by 2-D tensor copies (one R x 128-byte
+// box per column block, a 2- to 4-deep pipeline per warp), with the tile's weights
+// beside them. The warp's lanes split three ways: lane = cg + KB * (jg + NB * rs).
+// Lane (rs, jg, cg) keeps in registers the eight 16-byte chunks jg, jg + NB, ... of
+// Y's rows for right-hand side cg, and per row it reads the same eight chunks of X. The NB lanes of a row sum their
 // partial dots with shuffles; each lane then has t = v * (x . y_cg) and adds t * x into
 // its own column sums. No dot needs another right-hand side's data, so no lane holds
 // more than one right-hand side.
@@ -61,26 +61,26 @@ struct MShape {
   static constexpr int R = NB >= 4 ? 8 : 32 / NB; // rows per tile
   static constexpr int IT = R / RS;               // rows per lane per tile
   static constexpr int BOX = R * 128;             // bytes of one 128-byte column block of a tile
-  static constexpr int TILE = NB * BOX;           // bytes of one pipeline stage
-  // Row order inside a tile. The RS rows read at once must fall in different
-  // 128-byte-swizzle phases beyond what the NB lanes of a row already cover: row
-  // index bits are rotated left by log2(NB) when NB < 8.
-  static constexpr int LOGR = NB >= 4 ? 3 : (NB == 2 ? 4 : 5);
-  static constexpr int ROT = NB == 2 ? 1 : (NB == 4 ? 2 : 0);
-  static_assert(NB * KB <= 32 && RS >= 1 && R % RS == 0, "lane split");
+  static constexpr int TILE = NB * BOX;           // bytes of X in one pipeline stage
+  static constexpr int UNROLL = IT < 8 ? IT : 8;  // rows per lane between pointer updates
+  static_assert(NB * KB <= 32 && RS >= 1 && R % RS == 0 && IT % UNROLL == 0, "lane split");
 };
 
-template <int R, int LOGR, int ROT>
-__device__ __forceinline__ int tile_row(int idx) {
-  if constexpr (ROT == 0) return idx;
-  else return ((idx << ROT) | (idx >> (LOGR - ROT))) & (R - 1);
+// Byte offset of chunk ch of tile row r: one R x 128-byte box per 128-byte column
+// block, rows unswizzled.
+template <int BOX>
+__host__ __device__ __forceinline__ int chunk_offset(int r, int ch) {
+  return (ch >> 3) * BOX + r * 128 + ((ch & 7) << 4);
 }
 
-// Byte offset of chunk ch of tile row r (128-byte swizzle: chunk c of a block row
-// sits at position c ^ (r mod 8)).
-template <int BOX>
-__device__ __forceinline__ int chunk_offset(int r, int ch) {
-  return (ch >> 3) * BOX + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+// The chunk lane (rs, jg) reads at step q. The rotation by rs spreads the RS rows a
+// warp reads at once over distinct 16-byte bank groups (rows are 128 bytes apart, so
+// without it they would all hit the same group), and keeps every lane's offsets
+// fixed from row to row.
+template <int NB>
+__host__ __device__ __forceinline__ int lane_chunk(int rs, int jg, int q) {
+  const int rot = NB < 8 ? (rs & (8 / NB - 1)) : 0;
+  return jg + ((q + rot) & 7) * NB;
 }
 
 // Element-sized asynchronous copy global -> shared (no alignment beyond the element's).
@@ -91,11 +91,16 @@ __device__ __forceinline__ void cp_async_elem(T* dst, const T* src) {
   else
     asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
+// An arrive on `bar` once every asynchronous copy this thread issued so far has landed
+// (counted in the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+// Waits until every asynchronous copy this thread issued has landed (committed or not).
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Sums a value over the NB lanes of a row (lanes KB apart).
 template <typename T, int NB, int KB>
@@ -122,14 +127,14 @@ __device__ __forceinline__ float row_sum_comp(float s, float c) {
 // CTA partials -> workspace; the last CTA to arrive sums them in a fixed order and
 // writes OUT = alpha * W + beta * Z for the pass's kb right-hand sides.
 template <typename T, int KB>
-__device__ __forceinline__ void multi_finish(const MultiArgs<T>& a, double* red, const int nw) {
+__device__ __forceinline__ void multi_finish(const MultiArgs<T>& a, double* red, const int nred, const int nw) {
   __shared__ unsigned s_last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t N = a.n * KB;
   __syncthreads();
   for (int64_t e = threadIdx.x; e < N; e += blockDim.x) {
     double s = 0.0;
-    for (int w = 0; w < nw; ++w) s += red[w * N + e];
+    for (int w = 0; w < nred; ++w) s += red[w * N + e];
     a.ws[blockIdx.x * N + e] = s;
   }
   __threadfence();
@@ -159,53 +164,65 @@ __device__ __forceinline__ void multi_finish(const MultiArgs<T>& a, double* red,
   if (threadIdx.x == 0) *a.ticket = 0u;
 }
 
-// vmode: 0 no weights, 1 one shared m-vector, 2 an (m x k) matrix.
+// vmode: 0 no weights, 1 one shared m-vector, 2 an (m x k) matrix. v16: the weights
+// of a tile arrive in 16-byte copies (vmode 2, a full pass, V and ldv 16-byte aligned).
 template <typename T, int NB, int KB>
 __global__ void __launch_bounds__(MULTI_THREADS, 1)
     dense_multi_kernel(const __grid_constant__ CUtensorMap tmap, const MultiArgs<T> a, const int S, const int tma,
-                       const int vmode) {
+                       const int vmode, const int v16) {
   using SH = MShape<T, NB, KB>;
-  constexpr int NV = SH::NV, Q = SH::Q, C = SH::C, RS = SH::RS, R = SH::R, IT = SH::IT;
+  constexpr int NV = SH::NV, Q = SH::Q, C = SH::C, RS = SH::RS, R = SH::R, IT = SH::IT, UNROLL = SH::UNROLL;
   constexpr int BOX = SH::BOX, TILE = SH::TILE;
   // fp32 rows longer than 64 entries (NB >= 4) take the compensated dot
   constexpr bool COMP = sizeof(T) == 4 && NB >= 4;
   // fp32: plain per-lane column sums over about 32 rows, then folded into a two-float sum
   constexpr int FOLD = IT >= 32 ? 1 : 32 / IT;
   extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int cg = lane % KB, jg = (lane / KB) % NB, rs = lane / (KB * NB);
   const int64_t n = a.n, m = a.m;
-  const int VB = vmode == 2 ? R * KB : (vmode == 1 ? R : 0);  // weights per tile
+  const int VB = vmode == 2 ? R * KB : (vmode == 1 ? R : 0);                  // weights per tile
+  const int STAGE = TILE + ((VB * (int)sizeof(T) + 127) & ~127);             // X tile + weights
+  unsigned char* stages = smem + (size_t)warp * S * STAGE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)nw * S * STAGE) + warp * S;
 
-  unsigned char* stages = smem + (size_t)warp * S * TILE;
-  T* vbuf = reinterpret_cast<T*>(smem + (size_t)nw * S * TILE) + (size_t)warp * 2 * VB;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)nw * S * TILE + (size_t)nw * 2 * VB * sizeof(T)) + warp * S;
-
-  // this lane's slice of Y: columns of chunks jg + q NB, right-hand side cg
+  // this lane's eight chunks (rotated order) and its slice of Y for right-hand side cg
+  int off[Q];
   T yr[C];
 #pragma unroll
-  for (int q = 0; q < Q; ++q)
+  for (int q = 0; q < Q; ++q) {
+    const int ch = lane_chunk<NB>(rs, jg, q);
+    off[q] = chunk_offset<BOX>(rs, ch);
 #pragma unroll
     for (int e = 0; e < NV; ++e) {
-      const int64_t col = (int64_t)(jg + q * NB) * NV + e;
+      const int64_t col = (int64_t)ch * NV + e;
       yr[q * NV + e] = (col < n && cg < a.kb) ? ldg(a.Y + col * a.ldy + cg) : T(0);
     }
+  }
 
   const int64_t gw = (int64_t)blockIdx.x * nw + warp, W = (int64_t)gridDim.x * nw;
   const int64_t t0 = a.tiles * gw / W, t1 = a.tiles * (gw + 1) / W, nt = t1 - t0;
   const uint64_t pol = policy_evict_first();
 
-  auto issue = [&](int64_t tile, int s) {
-    if (lane == 0) mbar_arrive_expect_tx(&bars[s], (uint32_t)TILE);
-    __syncwarp();
-    if (lane < NB) tma_load_2d(stages + (size_t)s * TILE + lane * BOX, &tmap, lane * (128 / (int)sizeof(T)),
-                               (int)(tile * R), &bars[s], pol);
-  };
-  // weights of one tile into buffer `slot` (asynchronous; zeros past the last row)
-  auto stage_v = [&](int64_t tile, int slot) {
-    T* vb = vbuf + slot * VB;
+  // weights of one tile into vb (asynchronous copies; zeros past the last row)
+  auto stage_v = [&](int64_t tile, T* vb) {
+    if constexpr (KB * sizeof(T) >= 16) {
+      if (v16) {
+        constexpr int CPV = KB * (int)sizeof(T) / 16;  // 16-byte chunks per row of weights
+        for (int e = lane; e < R * CPV; e += 32) {
+          const int r = e / CPV, j = e % CPV;
+          const int64_t row = tile * R + r;
+          T* dst = vb + r * KB + j * NV;
+          if (row < m)
+            cp_async16(dst, a.V + row * a.ldv + j * NV);
+          else
+            *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        return;
+      }
+    }
     for (int e = lane; e < VB; e += 32) {
       const int r = vmode == 2 ? e / KB : e, c = vmode == 2 ? e % KB : 0;
       const int64_t row = tile * R + r;
@@ -214,6 +231,16 @@ __global__ void __launch_bounds__(MULTI_THREADS, 1)
       else
         vb[e] = T(0);
     }
+  };
+  auto issue = [&](int64_t tile, int s) {
+    unsigned char* st = stages + (size_t)s * STAGE;
+    if (vmode) {
+      stage_v(tile, reinterpret_cast<T*>(st + TILE));
+      cp_async_arrive(&bars[s]);
+    }
+    if (lane == 0) mbar_arrive_expect_tx(&bars[s], (uint32_t)TILE);
+    __syncwarp();
+    if (lane < NB) tma_load_2d(st + lane * BOX, &tmap, lane * (128 / (int)sizeof(T)), (int)(tile * R), &bars[s], pol);
   };
   // X of one tile by plain loads, in the layout the tensor copy would give
   auto load_direct = [&](int64_t tile, unsigned char* stage) {
@@ -233,14 +260,13 @@ __global__ void __launch_bounds__(MULTI_THREADS, 1)
 
   if (tma) {
     if (lane == 0) {
-      for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+      // one arrival with the byte count, plus one per lane for its weight copies
+      for (int s = 0; s < S; ++s) mbar_init(&bars[s], vmode ? 33u : 1u);
       fence_mbar_init();
     }
     __syncwarp();
     for (int s = 0; s < S && s < nt; ++s) issue(t0 + s, s);
   }
-  if (vmode && nt > 0) stage_v(t0, 0);
-  cp_async_commit();
 
   typename OuterAcc<T>::type acc[C];
   T tacc[C];
@@ -249,12 +275,8 @@ __global__ void __launch_bounds__(MULTI_THREADS, 1)
 
   for (int64_t k = 0; k < nt; ++k) {
     const int64_t tile = t0 + k;
-    if (vmode && k + 1 < nt) stage_v(tile + 1, (int)((k + 1) & 1));
-    cp_async_commit();
-    cp_async_wait<1>();  // this tile's weights have landed (this lane's copies)
-
     const int s = tma ? (int)(k % S) : 0;
-    unsigned char* stage = stages + (size_t)s * TILE;
+    unsigned char* stage = stages + (size_t)s * STAGE;
     if (tma) {
       const bool ok = mbar_wait_bounded(&bars[s], (uint32_t)((k / S) & 1));
       if (__any_sync(FULL_MASK, !ok)) {
@@ -264,44 +286,44 @@ __global__ void __launch_bounds__(MULTI_THREADS, 1)
       }
     } else {
       load_direct(tile, stage);
+      if (vmode) {
+        stage_v(tile, reinterpret_cast<T*>(stage + TILE));
+        cp_async_wait_all();
+      }
     }
-    __syncwarp();  // every lane's weights and (direct path) X are visible to the warp
-    const T* vb = vbuf + (int)(k & 1) * VB;
+    __syncwarp();  // zero fills and (direct path) plain stores are visible to the warp
+    const T* vb = reinterpret_cast<const T*>(stage + TILE);
 
 #pragma unroll 1
-    for (int it = 0; it < IT; ++it) {
-      const int r = tile_row<R, SH::LOGR, SH::ROT>(it * RS + rs);
-      T x[C];
+    for (int i0 = 0; i0 < IT; i0 += UNROLL) {
 #pragma unroll
-      for (int q = 0; q < Q; ++q) {
-        const uint4 u = *reinterpret_cast<const uint4*>(stage + chunk_offset<BOX>(r, jg + q * NB));
-        Chunk<T>::unpack(u, &x[q * NV]);
-      }
-      T d;
-      if constexpr (COMP) {
-        DotAcc<float, true> dacc;
+      for (int u = 0; u < UNROLL; ++u) {
+        const int r = (i0 + u) * RS + rs;
+        const unsigned char* rp = stage + (i0 + u) * RS * 128;
+        T x[C];
 #pragma unroll
-        for (int c = 0; c < C; ++c) dacc.add(x[c], yr[c]);
-        d = row_sum_comp<NB, KB>(dacc.s, dacc.c);
-      } else {
-        T d4[4] = {T(0), T(0), T(0), T(0)};
-#pragma unroll
-        for (int c = 0; c < C; ++c) d4[c & 3] = fma(x[c], yr[c], d4[c & 3]);
-        d = row_sum<T, NB, KB>((d4[0] + d4[1]) + (d4[2] + d4[3]));
-      }
-      const T t = vmode == 0 ? d : vb[vmode == 2 ? r * KB + cg : r] * d;
-#pragma unroll
-      for (int c = 0; c < C; ++c) tacc[c] = fma(t, x[c], tacc[c]);
-    }
-    if constexpr (sizeof(T) == 4) {
-      if ((k + 1) % FOLD == 0 || k + 1 == nt) {
-#pragma unroll
-        for (int c = 0; c < C; ++c) {
-          acc[c].add(tacc[c]);
-          tacc[c] = T(0);
+        for (int q = 0; q < Q; ++q) {
+          const uint4 w = *reinterpret_cast<const uint4*>(rp + off[q]);
+          Chunk<T>::unpack(w, &x[q * NV]);
         }
+        T d;
+        if constexpr (COMP) {
+          DotAcc<float, true> dacc;
+#pragma unroll
+          for (int c = 0; c < C; ++c) dacc.add(x[c], yr[c]);
+          d = row_sum_comp<NB, KB>(dacc.s, dacc.c);
+        } else {
+          T d4[4] = {T(0), T(0), T(0), T(0)};
+#pragma unroll
+          for (int c = 0; c < C; ++c) d4[c & 3] = fma(x[c], yr[c], d4[c & 3]);
+          d = row_sum<T, NB, KB>((d4[0] + d4[1]) + (d4[2] + d4[3]));
+        }
+        const T t = vmode == 0 ? d : vb[vmode == 2 ? r * KB + cg : r] * d;
+#pragma unroll
+        for (int c = 0; c < C; ++c) tacc[c] = fma(t, x[c], tacc[c]);
       }
-    } else {
+    }
+    if (sizeof(T) == 8 || (k + 1) % FOLD == 0 || k + 1 == nt) {
 #pragma unroll
       for (int c = 0; c < C; ++c) {
         acc[c].add(tacc[c]);
@@ -314,30 +336,22 @@ __global__ void __launch_bounds__(MULTI_THREADS, 1)
       issue(tile + S, s);
     }
   }
-  cp_async_wait<0>();
+  cp_async_wait_all();
 
-  // lane -> warp: lanes with the same (jg, cg) hold the same entries
-  double part[C];
-#pragma unroll
-  for (int c = 0; c < C; ++c) part[c] = acc[c].value();
-#pragma unroll
-  for (int o = KB * NB; o < 32; o <<= 1)
-#pragma unroll
-    for (int c = 0; c < C; ++c) part[c] += shfl_xor(part[c], o);
-
+  // per (warp, row slot) partials by column, then the CTA and grid reductions
   __syncthreads();
-  double* red = reinterpret_cast<double*>(smem);  // [nw][n][KB]
+  double* red = reinterpret_cast<double*>(smem);  // [nw * RS][n][KB]
   const int64_t N = n * KB;
-  if (rs == 0) {
 #pragma unroll
-    for (int q = 0; q < Q; ++q)
+  for (int q = 0; q < Q; ++q) {
+    const int ch = lane_chunk<NB>(rs, jg, q);
 #pragma unroll
-      for (int e = 0; e < NV; ++e) {
-        const int64_t col = (int64_t)(jg + q * NB) * NV + e;
-        if (col < n) red[warp * N + col * KB + cg] = part[q * NV + e];
-      }
+    for (int e = 0; e < NV; ++e) {
+      const int64_t col = (int64_t)ch * NV + e;
+      if (col < n) red[(warp * RS + rs) * N + col * KB + cg] = acc[q * NV + e].value();
+    }
   }
-  multi_finish<T, KB>(a, red, nw);
+  multi_finish<T, KB>(a, red, nw * RS, nw);
 }
 
 }  // namespace
@@ -364,15 +378,15 @@ MultiPlan plan_multi(const DeviceInfo& dev, int64_t m, int64_t n, int64_t k, int
   p.rows_per_tile = multi_rows(p.nb);
   // m == 0 runs the same kernel over no tiles (it writes beta Z); tensor maps need m > 0
   p.tma = tma_ok && m > 0 && m < (int64_t(1) << 31);
-  const size_t tile = (size_t)p.nb * p.rows_per_tile * 128;
+  // a stage holds R rows of X and their weights
   const size_t vb = full_v ? (size_t)p.rows_per_tile * p.kb_max : (has_v ? (size_t)p.rows_per_tile : 0);
-  const size_t vbytes = 2 * vb * elem;
+  const size_t tile = (size_t)p.nb * p.rows_per_tile * 128 + ((vb * elem + 127) & ~size_t(127));
   const size_t budget = std::min<size_t>(MULTI_SMEM_BUDGET, dev.smem_optin > 0 ? (size_t)dev.smem_optin : MULTI_SMEM_BUDGET);
   // eight warps with a pipeline of 2 to 4 tiles each; four warps where eight do not fit (16 KB tiles)
   p.warps = MULTI_THREADS / 32;
   if (p.tma) {
     for (;;) {
-      const size_t room = budget - 1024 - p.warps * vbytes;
+      const size_t room = budget - 1024;
       p.stages = (int)std::min<size_t>(4, room / (p.warps * (tile + 8)));
       if (p.stages >= 2 || p.warps == 4) break;
       p.warps = 4;
@@ -380,8 +394,9 @@ MultiPlan plan_multi(const DeviceInfo& dev, int64_t m, int64_t n, int64_t k, int
   } else {
     p.stages = 1;
   }
-  const size_t pipe = 1024 + p.warps * (p.stages * (tile + 8) + vbytes);
-  const size_t red = 1024 + (size_t)p.warps * n * p.kb_max * sizeof(double);
+  const size_t pipe = 1024 + p.warps * p.stages * (tile + 8);
+  // partials of every (warp, row slot) by column: row slots x right-hand sides = 32 / nb
+  const size_t red = 1024 + (size_t)p.warps * (32 / p.nb) * n * sizeof(double);
   p.smem = std::max(pipe, red);
   const int64_t tiles = (m + p.rows_per_tile - 1) / p.rows_per_tile;
   p.ctas = (int)std::max<int64_t>(1, std::min<int64_t>(dev.sm_count, (tiles + p.warps - 1) / p.warps));
@@ -407,7 +422,10 @@ static cudaError_t launch_kb(const MultiPlan& p, const CUtensorMap& map, const M
   const void* kern = (const void*)dense_multi_kernel<T, NB, KB>;
   cudaError_t e = ensure_smem(kern, p.smem);
   if (e != cudaSuccess) return e;
-  dense_multi_kernel<T, NB, KB><<<p.ctas, p.warps * 32, p.smem, st>>>(map, a, p.stages, p.tma ? 1 : 0, vmode);
+  // whole rows of weights in 16-byte copies: a full pass over 16-byte aligned rows
+  const int v16 = vmode == 2 && a.kb == KB && KB * sizeof(T) >= 16 && (reinterpret_cast<uintptr_t>(a.V) & 15u) == 0 &&
+                  (a.ldv * (int64_t)sizeof(T)) % 16 == 0;
+  dense_multi_kernel<T, NB, KB><<<p.ctas, p.warps * 32, p.smem, st>>>(map, a, p.stages, p.tma ? 1 : 0, vmode, v16);
   return cudaGetLastError();
 }
 
@@ -434,7 +452,7 @@ cudaError_t launch_multi(const MultiPlan& p, const MultiArgs<T>& a, cudaStream_t
   // a map the driver refuses sends the pass to the plain-load staging
   MultiPlan q = p;
   q.tma = p.tma && encode_rows_map(&map, Chunk<T>::MAP, a.X, a.m, a.n, a.ld * (int64_t)sizeof(T), (int)sizeof(T),
-                                   p.rows_per_tile, 128);
+                                   p.rows_per_tile, 128, 0);
   const int vmode = a.V == nullptr ? 0 : (a.ldv == 0 ? 1 : 2);
   switch (p.nb) {
     case 1: return launch_nb<T, 1>(q, map, a, vmode, st);
