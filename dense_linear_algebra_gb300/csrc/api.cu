@@ -202,6 +202,7 @@ fxtx_status_t csr_impl(int64_t m, int64_t n, int64_t nnz, const int64_t* row_ptr
   const size_t part_bytes = ((size_t)(plan.ctas + 1) * 8 + 127) / 128 * 128;
   a.part = reinterpret_cast<int64_t*>(w);
   a.queue = reinterpret_cast<int64_t*>(w + part_bytes);
+  a.queue_cap = plan.queue_cap;
   a.counters = reinterpret_cast<unsigned long long*>(w + plan.ws_bytes - 128);
   cudaError_t e = launch_csr<T>(plan, a, st);
   cudaFreeAsync(ws, st);

@@ -13,8 +13,9 @@
 //                         groups of LPR lanes x 8 entries per row, which spend
 //                         fewer fp64 operations per entry
 //   medium (<= WARP_LONG) one warp per row, two passes (the second from L1/L2)
-//   long   (> WARP_LONG)  deferred to a queue; a group of 4 warps takes each one
-//                         in the long-row kernel, two passes
+//   long   (> WARP_LONG)  deferred to queues bucketed by length; in the long-row
+//                         kernel a group of 4 warps takes each row, longest
+//                         buckets first, two passes
 // The y gathers of hot columns hit a copy of y[0, ylen) in shared memory.
 // Row dots of a packed batch are formed lane-locally per row segment, and each
 // segment's partial is added once into a per-warp fp64 buffer; t_i is then
@@ -23,9 +24,9 @@
 // atomic per column; columns outside the window go straight to out with
 // atomics. fp64 window updates fold the product into the atomic itself (a CAS
 // loop around one fused multiply-add).
-// The prologue writes out = beta z and splits rows among CTAs by equal shares
-// of nnz + row_cost * rows; inside a CTA, warps take 32-row windows from a
-// shared counter.
+// The prologue writes out = beta z and zeroes the counters. Warps of the packed
+// kernel take 32-row windows from one global counter; the fp64 lane-group kernel
+// splits rows among CTAs by equal shares of nnz + row_cost * rows.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -42,8 +43,13 @@ struct Pack {
 };
 constexpr int WARP_LONG = 1024;            // longest row a single warp takes
 constexpr int WARP_UNROLL = 8;             // loads in flight per lane for warp rows
-constexpr int LONG_UNROLL = 8;             // loads in flight per thread in the long-row kernel
+// entries per lane and batch in the long-row kernel (fp64 keeps fewer, to fit 64 registers)
+template <typename T>
+__host__ __device__ constexpr int long_unroll() {
+  return sizeof(T) == 4 ? 8 : 4;
+}
 constexpr int LONG_GROUP = 128;            // threads that share one long row
+constexpr int LONG_BUCKETS = 6;            // long-row queues: (1K, 2K], (2K, 4K], ... (16K, 32K], > 32K entries
 // per-warp scratch after the window: 32 row dots (double), 32 row scales (T), 33 row starts
 constexpr size_t WARP_SCRATCH = 32 * 8 + 32 * 8 + 33 * 8;
 
@@ -106,13 +112,17 @@ __device__ __forceinline__ void window_flush(const T* acc, int64_t c0, int64_t l
   }
 }
 
-// Named barrier over the `count` threads of one row group (ids 1..15; 0 is __syncthreads).
-__device__ __forceinline__ void group_barrier(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 __host__ __device__ constexpr size_t window_bytes(int64_t len, size_t elem) {
   return ((size_t)len * elem + 15) / 16 * 16;
+}
+
+// Defers row r (len > WARP_LONG entries) to the long-row queue of its length bucket.
+template <typename T>
+__device__ __forceinline__ void push_long(const CsrArgs<T>& a, int64_t r, int64_t len) {
+  const unsigned long long q = (unsigned long long)(len - 1) / WARP_LONG;  // >= 1
+  const int b = (int)tmin<unsigned long long>(LONG_BUCKETS - 1, 63 - __clzll((long long)q));
+  const unsigned long long k = atomicAdd(&a.counters[1 + b], 1ull);
+  a.queue[(int64_t)b * a.queue_cap + (int64_t)k] = r;
 }
 
 }  // namespace
@@ -124,6 +134,7 @@ size_t csr_rows_smem(int64_t win_len, int64_t ylen, int elem) {
 }
 int csr_pack_cap(int elem) { return elem == 4 ? Pack<float>::CAP : Pack<double>::CAP; }
 int csr_warp_long() { return WARP_LONG; }
+int csr_long_buckets() { return LONG_BUCKETS; }
 
 // out = beta z (or 0); row partition; counters.
 template <typename T>
@@ -150,17 +161,14 @@ __global__ void csr_prologue_kernel(const CsrArgs<T> a, const int nparts, const 
     }
     a.part[p] = r;
   }
-  if (tid == 0) {
-    a.counters[0] = 0ull;
-    a.counters[1] = 0ull;
-  }
+  if (tid < LONG_BUCKETS + 2) a.counters[tid] = 0ull;
 }
 
-// One row of up to WARP_LONG entries, taken by a whole warp: pass 1 forms the
+// One row of up to WARP_LONG entries (weight vi), taken by a whole warp: pass 1 forms the
 // dot with WARP_UNROLL loads in flight per lane, pass 2 re-reads the row (from
 // L1/L2) and scatters it.
 template <typename T>
-__device__ __forceinline__ void warp_row(const CsrArgs<T>& a, const Window<T>& win, int64_t r, int64_t st, int64_t en,
+__device__ __forceinline__ void warp_row(const CsrArgs<T>& a, const Window<T>& win, T vi, int64_t st, int64_t en,
                                          T alpha, int lane) {
   DotAcc<T, sizeof(T) == 4> d;
   for (int64_t b = st + lane; b < en; b += 32 * WARP_UNROLL) {
@@ -180,7 +188,6 @@ __device__ __forceinline__ void warp_row(const CsrArgs<T>& a, const Window<T>& w
     for (int k = 0; k < WARP_UNROLL; ++k) d.add(xv[k], yv[k]);
   }
   d.template group_reduce<32>();
-  const T vi = a.v ? ldg(a.v + r) : T(1);
   const T ts = alpha * (vi * d.value());
   for (int64_t b = st + lane; b < en; b += 32 * WARP_UNROLL) {
     T xv[WARP_UNROLL];
@@ -203,7 +210,6 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
     csr_rows_kernel(const CsrArgs<T> a, const int64_t win_c0, const int64_t win_len, const int64_t ylen) {
   constexpr int PACK_K = Pack<T>::K, PACK_CAP = Pack<T>::CAP;
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ unsigned long long s_next;
   T* wacc = reinterpret_cast<T*>(smem);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   T* ys = reinterpret_cast<T*>(smem + window_bytes(win_len, sizeof(T)));
@@ -214,7 +220,7 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
   T* tb = reinterpret_cast<T*>(scratch + 32 * 8);              // [32] row scales alpha * v_i * u_i
   int64_t* rsb = reinterpret_cast<int64_t*>(scratch + 64 * 8);  // [33] row starts of the window
   const Window<T> win{wacc, win_c0, win_len, a.out, ys, ylen, a.y};
-  const int64_t rb = a.part[blockIdx.x], re = a.part[blockIdx.x + 1];
+  const int64_t re = a.m;
   const T alpha = (T)a.alpha;
 
   // adds a lane's partial dot of one row segment into the warp's row-dot buffer: fp64 through a
@@ -230,19 +236,20 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
   };
   window_init(win);
   dotb[lane] = 0.0;
-  if (threadIdx.x == 0) s_next = (unsigned long long)rb;
   __syncthreads();
 
+  // 32-row windows from one global counter; the next window is claimed while this one runs
+  unsigned long long next = 0;
+  if (lane == 0) next = atomicAdd(&a.counters[LONG_BUCKETS + 1], 32ull);
   for (;;) {
-    unsigned long long r0u = 0;
-    if (lane == 0) r0u = atomicAdd(&s_next, 32ull);
-    r0u = __shfl_sync(FULL_MASK, r0u, 0);
-    const int64_t r0 = (int64_t)r0u;
+    const int64_t r0 = (int64_t)__shfl_sync(FULL_MASK, next, 0);
     if (r0 >= re) break;
+    if (lane == 0) next = atomicAdd(&a.counters[LONG_BUCKETS + 1], 32ull);
     const int nr = (int)tmin<int64_t>(32, re - r0);  // rows in this window
     const bool hasrow = lane < nr;
     const int64_t rs = hasrow ? a.row_ptr[r0 + lane] : 0;
     const int64_t rend = hasrow ? a.row_ptr[r0 + lane + 1] : 0;
+    const T vrow = (hasrow && a.v) ? ldg(a.v + r0 + lane) : T(1);  // this lane's row weight
     const int64_t len = rend - rs;
     const bool isshort = hasrow && len <= PACK_CAP;
     rsb[lane] = hasrow ? rs : INT64_MAX;
@@ -313,8 +320,7 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
           u = dotb[lane];
           dotb[lane] = 0.0;
         }
-        const T vi = a.v ? ldg(a.v + r0 + lane) : T(1);
-        tb[lane] = alpha * (vi * u);
+        tb[lane] = alpha * (vrow * u);
       }
       __syncwarp();
       // scatter, walking the same row boundaries again
@@ -337,10 +343,11 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
       const int j = __ffs(lm) - 1;
       lm &= lm - 1;
       const int64_t s2 = __shfl_sync(FULL_MASK, rs, j), e2 = __shfl_sync(FULL_MASK, rend, j);
+      const T vj = __shfl_sync(FULL_MASK, vrow, j);
       if (e2 - s2 > WARP_LONG) {
-        if (lane == 0) a.queue[atomicAdd(&a.counters[0], 1ull)] = r0 + j;
+        if (lane == 0) push_long(a, r0 + j, e2 - s2);
       } else {
-        warp_row(a, win, r0 + j, s2, e2, alpha, lane);
+        warp_row(a, win, vj, s2, e2, alpha, lane);
       }
     }
     __syncwarp();  // rsb reuse
@@ -409,9 +416,9 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
       const int64_t rr = __shfl_sync(FULL_MASK, r, src);
       const int64_t s2 = __shfl_sync(FULL_MASK, st, src), e2 = __shfl_sync(FULL_MASK, en, src);
       if (e2 - s2 > WARP_LONG) {
-        if (lane == 0) a.queue[atomicAdd(&a.counters[0], 1ull)] = rr;
+        if (lane == 0) push_long(a, rr, e2 - s2);
       } else {
-        warp_row(a, win, rr, s2, e2, alpha, lane);
+        warp_row(a, win, a.v ? ldg(a.v + rr) : T(1), s2, e2, alpha, lane);
       }
     }
   }
@@ -420,14 +427,39 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
 }
 
 // Rows longer than WARP_LONG: each group of LONG_GROUP threads takes queued rows
-// one at a time, with one group barrier per row. The next row's index is
-// claimed while the current one is processed, and the per-warp partial dots are
-// double-buffered by row parity, so the single barrier orders both.
+// one at a time, with one group barrier per row. Rows are claimed from one global
+// counter that walks the length buckets from the longest down, so the longest
+// rows start first and short ones fill in at the end. A group rather than a warp
+// per row keeps the rows in flight few enough that a row read by pass 1 is still
+// in L2 when pass 2 re-reads it. Both passes keep the next batch of entries loading
+// while the current batch is used. The next row's index is claimed while the
+// current one is processed, and the per-warp partial dots are double-buffered by
+// row parity, so the single barrier orders both.
+template <typename T>
+__device__ __forceinline__ void long_batch(const CsrArgs<T>& a, int64_t b, int64_t en, T* xv, int32_t* xc) {
+  constexpr int U = long_unroll<T>();
+#pragma unroll
+  for (int k = 0; k < U; ++k) {
+    const int64_t idx = b + (int64_t)k * LONG_GROUP;
+    const bool ok = idx < en;
+    xv[k] = ok ? ldg(a.vals + idx) : T(0);
+    xc[k] = ok ? ldg(a.col_idx + idx) : -1;
+  }
+}
+
+// Named barrier over the `count` threads of one row group (ids 1..15; 0 is __syncthreads).
+__device__ __forceinline__ void group_barrier(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 template <typename T>
 __global__ void __launch_bounds__(CSR_THREADS, 1)
     csr_long_kernel(const CsrArgs<T> a, const int64_t win_c0, const int64_t win_len, const int64_t ylen) {
-  constexpr int GW = LONG_GROUP / 32;  // warps per group
-  constexpr int NG = CSR_THREADS / LONG_GROUP;
+  constexpr int U = long_unroll<T>();
+  constexpr int GW = LONG_GROUP / 32;           // warps per group
+  constexpr int NG = CSR_THREADS / LONG_GROUP;  // groups per CTA (named barriers 1 .. NG)
+  static_assert(NG <= 15, "named barrier ids");
+  constexpr int64_t STEP = (int64_t)LONG_GROUP * U;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ long long s_row[NG][2];
   __shared__ double s_red[NG][2][GW];
@@ -438,14 +470,18 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
   const int grp = threadIdx.x / LONG_GROUP, gt = threadIdx.x % LONG_GROUP, gw = gt >> 5;
   const int bar = 1 + grp;
   const T alpha = (T)a.alpha;
-  const unsigned long long count = a.counters[0];
   auto claim = [&]() -> long long {
-    const unsigned long long k = atomicAdd(&a.counters[1], 1ull);
-    return k < count ? (long long)a.queue[k] : -1ll;
+    unsigned long long k = atomicAdd(&a.counters[0], 1ull);
+    for (int b = LONG_BUCKETS - 1; b >= 0; --b) {
+      const unsigned long long c = a.counters[1 + b];
+      if (k < c) return (long long)a.queue[(int64_t)b * a.queue_cap + (int64_t)k];
+      k -= c;
+    }
+    return -1ll;
   };
 
   window_init(win);
-  if (gt == 0) s_row[grp][0] = count > 0 ? claim() : -1ll;
+  if (gt == 0) s_row[grp][0] = claim();
   __syncthreads();
   for (int it = 0;; ++it) {
     const int cur = it & 1;
@@ -454,23 +490,24 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
     if (gt == 0) s_row[grp][cur ^ 1] = claim();
     const int64_t st = a.row_ptr[r], en = a.row_ptr[r + 1];
 
-    // pass 1: the dot, LONG_UNROLL independent loads in flight per thread
+    // pass 1: the dot
     DotAcc<T, sizeof(T) == 4> d;
-    for (int64_t b = st + gt; b < en; b += (int64_t)LONG_GROUP * LONG_UNROLL) {
-      T xv[LONG_UNROLL];
-      int32_t xc[LONG_UNROLL];
+    T xv[U];
+    int32_t xc[U];
+    long_batch(a, st + gt, en, xv, xc);
+    for (int64_t b = st + gt; b < en; b += STEP) {
+      T nv[U];
+      int32_t nc[U];
+      long_batch(a, b + STEP, en, nv, nc);
+      T yv[U];
 #pragma unroll
-      for (int k = 0; k < LONG_UNROLL; ++k) {
-        const int64_t idx = b + (int64_t)k * LONG_GROUP;
-        const bool ok = idx < en;
-        xv[k] = ok ? ldg(a.vals + idx) : T(0);
-        xc[k] = ok ? ldg(a.col_idx + idx) : -1;
+      for (int k = 0; k < U; ++k) yv[k] = xc[k] >= 0 ? win.yat(xc[k]) : T(0);
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        d.add(xv[k], yv[k]);
+        xv[k] = nv[k];
+        xc[k] = nc[k];
       }
-      T yv[LONG_UNROLL];
-#pragma unroll
-      for (int k = 0; k < LONG_UNROLL; ++k) yv[k] = xc[k] >= 0 ? win.yat(xc[k]) : T(0);
-#pragma unroll
-      for (int k = 0; k < LONG_UNROLL; ++k) d.add(xv[k], yv[k]);
     }
     d.template group_reduce<32>();
     if (lane == 0) s_red[grp][cur][gw] = d.value_f64();
@@ -482,19 +519,17 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
     const T ts = alpha * (vi * (T)u);
 
     // pass 2: the scatter, re-reading the row (served by L2)
-    for (int64_t b = st + gt; b < en; b += (int64_t)LONG_GROUP * LONG_UNROLL) {
-      T xv[LONG_UNROLL];
-      int32_t xc[LONG_UNROLL];
+    long_batch(a, st + gt, en, xv, xc);
+    for (int64_t b = st + gt; b < en; b += STEP) {
+      T nv[U];
+      int32_t nc[U];
+      long_batch(a, b + STEP, en, nv, nc);
 #pragma unroll
-      for (int k = 0; k < LONG_UNROLL; ++k) {
-        const int64_t idx = b + (int64_t)k * LONG_GROUP;
-        const bool ok = idx < en;
-        xv[k] = ok ? ldg(a.vals + idx) : T(0);
-        xc[k] = ok ? ldg(a.col_idx + idx) : -1;
-      }
-#pragma unroll
-      for (int k = 0; k < LONG_UNROLL; ++k)
+      for (int k = 0; k < U; ++k) {
         if (xc[k] >= 0) win.add(xc[k], ts, xv[k]);
+        xv[k] = nv[k];
+        xc[k] = nc[k];
+      }
     }
   }
   __syncthreads();

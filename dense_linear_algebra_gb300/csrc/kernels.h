@@ -47,8 +47,10 @@ struct CsrArgs {
   double alpha = 1.0, beta = 0.0;
   bool use_z = false;
   int64_t* part = nullptr;       // [ctas + 1] row partition of the row-group kernel
-  int64_t* queue = nullptr;      // rows deferred to the long-row kernel
-  unsigned long long* counters = nullptr;  // [0] queue length, [1] long-row work counter
+  int64_t* queue = nullptr;      // [buckets][queue_cap] rows deferred to the long-row kernel, by length
+  int64_t queue_cap = 0;
+  // [0] long-row claims, [1 .. buckets] bucket lengths, [buckets + 1] row windows handed out
+  unsigned long long* counters = nullptr;
 };
 
 template <typename T>

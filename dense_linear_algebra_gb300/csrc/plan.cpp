@@ -154,7 +154,8 @@ CsrPlan plan_csr(const DeviceInfo& dev, int64_t m, int64_t n, int64_t nnz, int e
   p.long_smem = csr_rows_smem(p.win_len, p.ylen, elem) - (size_t)csr_rows_smem(0, 0, elem);
   p.row_cost = 8;
   p.queue_cap = std::min<int64_t>(m, nnz / (p.warp_cap + 1) + 1);
-  p.ws_bytes = align128((size_t)(p.ctas + 1) * 8) + align128((size_t)std::max<int64_t>(p.queue_cap, 1) * 8) + 128;
+  p.ws_bytes = align128((size_t)(p.ctas + 1) * 8) +
+               align128((size_t)csr_long_buckets() * std::max<int64_t>(p.queue_cap, 1) * 8) + 128;
   return p;
 }
 
