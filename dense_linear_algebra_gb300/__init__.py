@@ -10,7 +10,7 @@ Raw C-ABI calls (pointers as ints, stream as a cudaStream_t int) carry the C nam
 ``fxtx_dense_f32``, ``fxtx_dense_f64``, ``fxtx_dense_bf16``, ``fxtx_dense_f32_noalloc``,
 ``fxtx_dense_multi_f32``, ``fxtx_dense_multi_f64``, ``fxtx_csr_f32``, ``fxtx_csr_f64``,
 ``fxtx_csr_validate``, ``fxtx_device_error``, ``fxtx_status_string``,
-``fxtx_plan_describe``, ``fxtx_multi_plan_describe``. ``dense``, ``dense_multi`` and
+``fxtx_plan_describe``, ``fxtx_multi_plan_describe`` and the ``fxtx_autotune_*`` calls. ``dense``, ``dense_multi`` and
 ``csr`` take torch CUDA tensors.
 """
 from ._lib import (  # noqa: F401
@@ -23,11 +23,25 @@ from ._lib import (  # noqa: F401
     FXTX_ERR_UNSUPPORTED,
     FXTX_OK,
     FxtxError,
+    autotune,
+    autotune_candidates,
+    autotune_clear,
+    autotune_entries,
+    autotune_load,
+    autotune_mode,
+    autotune_save,
     csr,
     csr_validate,
     dense,
     dense_multi,
     device_error,
+    fxtx_autotune_candidates,
+    fxtx_autotune_clear,
+    fxtx_autotune_entries,
+    fxtx_autotune_get,
+    fxtx_autotune_load,
+    fxtx_autotune_save,
+    fxtx_autotune_set,
     fxtx_csr_f32,
     fxtx_csr_f64,
     fxtx_csr_validate,

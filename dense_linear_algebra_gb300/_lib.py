@@ -39,9 +39,18 @@ def _load() -> ctypes.CDLL:
     lib.fxtx_status_string.restype = ctypes.c_char_p
     lib.fxtx_plan_describe.argtypes = [i32, i32, i64, i64, i64, i64, ctypes.c_char_p, i64]
     lib.fxtx_multi_plan_describe.argtypes = [i32, i64, i64, i64, i64, i32, ctypes.c_char_p, i64]
+    lib.fxtx_autotune_set.argtypes = [i32]
+    lib.fxtx_autotune_get.argtypes = []
+    lib.fxtx_autotune_entries.argtypes = []
+    lib.fxtx_autotune_entries.restype = i64
+    lib.fxtx_autotune_clear.argtypes = []
+    lib.fxtx_autotune_save.argtypes = [ctypes.c_char_p]
+    lib.fxtx_autotune_load.argtypes = [ctypes.c_char_p]
+    lib.fxtx_autotune_candidates.argtypes = [i32, i32, i64, i64, i64, i64, ctypes.c_char_p, i64]
     for name in ("fxtx_dense_f32", "fxtx_dense_f64", "fxtx_dense_f32_noalloc", "fxtx_dense_bf16", "fxtx_dense_multi_f32",
                  "fxtx_dense_multi_f64", "fxtx_csr_f32", "fxtx_csr_f64", "fxtx_csr_validate", "fxtx_device_error",
-                 "fxtx_plan_describe", "fxtx_multi_plan_describe"):
+                 "fxtx_plan_describe", "fxtx_multi_plan_describe", "fxtx_autotune_set", "fxtx_autotune_get",
+                 "fxtx_autotune_clear", "fxtx_autotune_save", "fxtx_autotune_load", "fxtx_autotune_candidates"):
         getattr(lib, name).restype = i32
     return lib
 
@@ -61,6 +70,13 @@ fxtx_csr_validate = _lib.fxtx_csr_validate
 fxtx_device_error = _lib.fxtx_device_error
 fxtx_plan_describe = _lib.fxtx_plan_describe
 fxtx_multi_plan_describe = _lib.fxtx_multi_plan_describe
+fxtx_autotune_set = _lib.fxtx_autotune_set
+fxtx_autotune_get = _lib.fxtx_autotune_get
+fxtx_autotune_entries = _lib.fxtx_autotune_entries
+fxtx_autotune_clear = _lib.fxtx_autotune_clear
+fxtx_autotune_save = _lib.fxtx_autotune_save
+fxtx_autotune_load = _lib.fxtx_autotune_load
+fxtx_autotune_candidates = _lib.fxtx_autotune_candidates
 
 
 def fxtx_status_string(status: int) -> str:
@@ -93,6 +109,39 @@ def multi_plan_describe(dtype: str, m: int, n: int, k: int, v_mode: str = "full"
     _check(fxtx_multi_plan_describe(1 if dtype in ("f64", "float64") else 0, m, n, k, n if ld is None else ld, vm,
                                     buf, 512), "fxtx_multi_plan_describe")
     return buf.value.decode()
+
+
+def autotune(mode: int) -> None:
+    """0: the launch model picks (default); 1: time the model's candidates once per call shape and cache the fastest."""
+    _check(fxtx_autotune_set(int(mode)), "fxtx_autotune_set")
+
+
+def autotune_mode() -> int:
+    return int(fxtx_autotune_get())
+
+
+def autotune_entries() -> int:
+    return int(fxtx_autotune_entries())
+
+
+def autotune_clear() -> None:
+    _check(fxtx_autotune_clear(), "fxtx_autotune_clear")
+
+
+def autotune_save(path: str) -> None:
+    _check(fxtx_autotune_save(os.fsencode(path)), "fxtx_autotune_save")
+
+
+def autotune_load(path: str) -> None:
+    _check(fxtx_autotune_load(os.fsencode(path)), "fxtx_autotune_load")
+
+
+def autotune_candidates(kind: str, dtype: str, m: int, n: int, nnz: int = 0, ld: int | None = None) -> list[str]:
+    """The candidate launches the tuner times for a shape, the model's plan first (host only)."""
+    buf = ctypes.create_string_buffer(4096)
+    _check(fxtx_autotune_candidates(1 if kind == "csr" else 0, 1 if dtype in ("f64", "float64") else 0, m, n, nnz,
+                                    n if ld is None else ld, buf, 4096), "fxtx_autotune_candidates")
+    return buf.value.decode().split("\n")
 
 
 # ---------------------------------------------------------------------------- torch tensors

@@ -3,13 +3,16 @@
 // on the caller's stream.
 #include <cstdio>
 #include <cstdlib>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "fxtx.h"
 #include "kernels.h"
 #include "multi.h"
 #include "plan.h"
+#include "tune.h"
 
 namespace fxtx {
 namespace {
@@ -72,37 +75,23 @@ bool aligned16(const T* p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
 }
 
-template <typename T>
-fxtx_status_t dense_impl(int64_t m, int64_t n, const T* X, int64_t ld, const T* y, const T* v, T alpha, T beta,
-                         const T* z, T* out, void* stream) {
-  if (m < 0 || n < 0) return FXTX_ERR_INVALID_ARG;
-  if (n == 0) return FXTX_OK;
-  if (ld < n || y == nullptr || out == nullptr) return FXTX_ERR_INVALID_ARG;
-  if (m > 0 && X == nullptr) return FXTX_ERR_INVALID_ARG;
-  const DeviceInfo* dev = nullptr;
-  fxtx_status_t s = current_device(&dev);
-  if (s != FXTX_OK) return s;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+// Compute type of the vectors for X stored as TX (bfloat16 X computes in fp32).
+template <typename TX>
+struct DenseT {
+  using T = TX;
+};
+template <>
+struct DenseT<__nv_bfloat16> {
+  using T = float;
+};
 
-  const int elem = (int)sizeof(T);
-  const bool tile_ok = aligned16(X) && (ld * elem) % 16 == 0;
-  const bool tma_ok = tile_ok && (n * elem) % 16 == 0;
-  const DensePlan plan = plan_dense(*dev, m, n, ld, elem, tma_ok, tile_ok);
-  if (log_enabled()) {
-    char buf[256];
-    describe(plan, buf, sizeof buf);
-    fprintf(stderr, "[fxtx] m=%lld n=%lld ld=%lld %s\n", (long long)m, (long long)n, (long long)ld, buf);
-  }
-
-  DenseArgs<T> a;
-  a.m = m; a.n = n; a.ld = ld;
-  a.X = X; a.y = y; a.v = v; a.z = z; a.out = out;
-  a.alpha = (double)alpha; a.beta = (double)beta;
-  a.use_z = (z != nullptr && beta != T(0));
-  a.tiles = plan.rows_per_tile > 0 ? (m + plan.rows_per_tile - 1) / plan.rows_per_tile : 0;
-
+// One dense launch with its own transient workspace (the column partials and the
+// ticket of the last-CTA reduction).
+template <typename TX>
+fxtx_status_t run_dense(const DensePlan& plan, DenseArgs<typename DenseT<TX>::T, TX> a, cudaStream_t st) {
+  a.tiles = plan.rows_per_tile > 0 ? (a.m + plan.rows_per_tile - 1) / plan.rows_per_tile : 0;
   void* ws = nullptr;
-  s = alloc_ws(&ws, plan.ws_bytes, st);
+  fxtx_status_t s = alloc_ws(&ws, plan.ws_bytes, st);
   if (s != FXTX_OK) return s;
   if (ws) {
     a.ws = static_cast<double*>(ws);
@@ -113,7 +102,11 @@ fxtx_status_t dense_impl(int64_t m, int64_t n, const T* X, int64_t ld, const T* 
       return FXTX_ERR_CUDA;
     }
   }
-  cudaError_t e = launch_dense<T>(plan, a, st);
+  cudaError_t e;
+  if constexpr (sizeof(TX) == 2)
+    e = launch_dense_bf16(plan, a, st);
+  else
+    e = launch_dense<TX>(plan, a, st);
   if (ws) cudaFreeAsync(ws, st);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -122,9 +115,82 @@ fxtx_status_t dense_impl(int64_t m, int64_t n, const T* X, int64_t ld, const T* 
   return FXTX_OK;
 }
 
-// bfloat16 X, fp32 everything else and fp32 arithmetic.
-fxtx_status_t dense_bf16_impl(int64_t m, int64_t n, const __nv_bfloat16* X, int64_t ld, const float* y,
-                              const float* v, float alpha, float beta, const float* z, float* out, void* stream) {
+// One CSR call (prologue, row kernel, long-row kernel) with its own workspace.
+template <typename T>
+fxtx_status_t run_csr(const CsrPlan& plan, CsrArgs<T> a, cudaStream_t st) {
+  void* ws = nullptr;
+  fxtx_status_t s = alloc_ws(&ws, plan.ws_bytes, st);
+  if (s != FXTX_OK) return s;
+  char* w = static_cast<char*>(ws);
+  const size_t part_bytes = ((size_t)(plan.ctas + 1) * 8 + 127) / 128 * 128;
+  a.part = reinterpret_cast<int64_t*>(w);
+  a.queue = reinterpret_cast<int64_t*>(w + part_bytes);
+  a.queue_cap = plan.queue_cap;
+  a.counters = reinterpret_cast<unsigned long long*>(w + plan.ws_bytes - 128);
+  cudaError_t e = launch_csr<T>(plan, a, st);
+  cudaFreeAsync(ws, st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FXTX_ERR_CUDA;
+  }
+  return FXTX_OK;
+}
+
+// The candidate to launch for `key`: the model's plan (index 0) unless autotuning is on.
+// On a cache miss outside stream capture, every candidate runs once to warm up and
+// then three times between events on the caller's stream (so the call synchronises),
+// and the fastest is cached. `run` enqueues one complete call with a candidate.
+template <typename P, typename Run>
+int choose(const TuneKey& key, const std::vector<P>& cands, Run run, cudaStream_t st) {
+  if (cands.size() < 2 || tune_mode() == 0) return 0;
+  int choice = 0;
+  if (tune_lookup(key, &choice)) return choice < (int)cands.size() ? choice : 0;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaEvent_t e0, e1;
+  if (cudaEventCreate(&e0) != cudaSuccess) return 0;
+  if (cudaEventCreate(&e1) != cudaSuccess) {
+    cudaEventDestroy(e0);
+    return 0;
+  }
+  double best = 0.0;
+  int bi = -1;
+  for (int i = 0; i < (int)cands.size(); ++i) {
+    if (run(cands[i]) != FXTX_OK) continue;
+    float t = 0.f, tmin = 0.f;
+    bool ok = true;
+    for (int rep = 0; rep < 3 && ok; ++rep) {
+      ok = cudaEventRecord(e0, st) == cudaSuccess && run(cands[i]) == FXTX_OK &&
+           cudaEventRecord(e1, st) == cudaSuccess && cudaEventSynchronize(e1) == cudaSuccess &&
+           cudaEventElapsedTime(&t, e0, e1) == cudaSuccess;
+      if (ok && (rep == 0 || t < tmin)) tmin = t;
+    }
+    if (ok && (bi < 0 || tmin * 1e3 < best)) {
+      best = tmin * 1e3;
+      bi = i;
+    }
+  }
+  cudaGetLastError();
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (bi < 0) return 0;
+  tune_store(key, bi, (int)cands.size(), best, cands[0].est_us);
+  if (log_enabled())
+    fprintf(stderr, "[fxtx] autotune kind=%d m=%lld n=%lld nnz=%lld: candidate %d of %d, %.1f us (model estimate %.1f us)\n",
+            key.kind, (long long)key.m, (long long)key.n, (long long)key.nnz, bi, (int)cands.size(), best,
+            cands[0].est_us);
+  return bi;
+}
+
+template <typename TX>
+fxtx_status_t dense_impl(int64_t m, int64_t n, const TX* X, int64_t ld, const typename DenseT<TX>::T* y,
+                         const typename DenseT<TX>::T* v, typename DenseT<TX>::T alpha,
+                         typename DenseT<TX>::T beta, const typename DenseT<TX>::T* z, typename DenseT<TX>::T* out,
+                         void* stream) {
+  using T = typename DenseT<TX>::T;
   if (m < 0 || n < 0) return FXTX_ERR_INVALID_ARG;
   if (n == 0) return FXTX_OK;
   if (ld < n || y == nullptr || out == nullptr) return FXTX_ERR_INVALID_ARG;
@@ -133,39 +199,33 @@ fxtx_status_t dense_bf16_impl(int64_t m, int64_t n, const __nv_bfloat16* X, int6
   fxtx_status_t s = current_device(&dev);
   if (s != FXTX_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const bool tile_ok = aligned16(X) && (ld * 2) % 16 == 0;
-  const DensePlan plan = plan_dense(*dev, m, n, ld, 2, false, tile_ok);
-  if (plan.kind == DENSE_WIDE || plan.kind == DENSE_NARROW_TMA) return FXTX_ERR_UNSUPPORTED;  // n > 512
-  if (log_enabled()) {
-    char buf[256];
-    describe(plan, buf, sizeof buf);
-    fprintf(stderr, "[fxtx] bf16 m=%lld n=%lld ld=%lld %s\n", (long long)m, (long long)n, (long long)ld, buf);
-  }
-  DenseArgs<float, __nv_bfloat16> a;
+
+  const int elem = (int)sizeof(TX);
+  const bool tile_ok = aligned16(X) && (ld * elem) % 16 == 0;
+  // bfloat16 X takes the tile kernel or the direct-load narrow kernel only
+  const bool tma_ok = elem != 2 && tile_ok && (n * elem) % 16 == 0;
+  const DensePlan model = plan_dense(*dev, m, n, ld, elem, tma_ok, tile_ok);
+  if (elem == 2 && (model.kind == DENSE_WIDE || model.kind == DENSE_NARROW_TMA)) return FXTX_ERR_UNSUPPORTED;
+
+  DenseArgs<T, TX> a;
   a.m = m; a.n = n; a.ld = ld;
   a.X = X; a.y = y; a.v = v; a.z = z; a.out = out;
   a.alpha = (double)alpha; a.beta = (double)beta;
-  a.use_z = (z != nullptr && beta != 0.0f);
-  a.tiles = plan.rows_per_tile > 0 ? (m + plan.rows_per_tile - 1) / plan.rows_per_tile : 0;
-  void* ws = nullptr;
-  s = alloc_ws(&ws, plan.ws_bytes, st);
-  if (s != FXTX_OK) return s;
-  if (ws) {
-    a.ws = static_cast<double*>(ws);
-    a.ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + plan.ws_bytes - 128);
-    if (cudaMemsetAsync(a.ticket, 0, sizeof(unsigned), st) != cudaSuccess) {
-      cudaGetLastError();
-      cudaFreeAsync(ws, st);
-      return FXTX_ERR_CUDA;
-    }
+  a.use_z = (z != nullptr && beta != T(0));
+
+  const std::vector<DensePlan> cands = dense_candidates(*dev, model, m, n, elem);
+  TuneKey key;
+  key.kind = 0; key.elem = elem; key.m = m; key.n = n; key.ld = ld;
+  key.flags = (tile_ok ? 1 : 0) | (tma_ok ? 2 : 0);
+  key.sm_count = dev->sm_count;
+  const DensePlan& plan = cands[choose(key, cands, [&](const DensePlan& p) { return run_dense<TX>(p, a, st); }, st)];
+  if (log_enabled()) {
+    char buf[320];
+    describe(plan, buf, sizeof buf);
+    fprintf(stderr, "[fxtx] %s m=%lld n=%lld ld=%lld %s\n", elem == 2 ? "bf16" : "dense", (long long)m, (long long)n,
+            (long long)ld, buf);
   }
-  cudaError_t e = launch_dense_bf16(plan, a, st);
-  if (ws) cudaFreeAsync(ws, st);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return FXTX_ERR_CUDA;
-  }
-  return FXTX_OK;
+  return run_dense<TX>(plan, a, st);
 }
 
 template <typename T>
@@ -181,13 +241,7 @@ fxtx_status_t csr_impl(int64_t m, int64_t n, int64_t nnz, const int64_t* row_ptr
   if (s != FXTX_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-  const CsrPlan plan = plan_csr(*dev, m, n, nnz, (int)sizeof(T));
-  if (log_enabled()) {
-    char buf[256];
-    describe(plan, buf, sizeof buf);
-    fprintf(stderr, "[fxtx] m=%lld n=%lld nnz=%lld %s\n", (long long)m, (long long)n, (long long)nnz, buf);
-  }
-
+  const CsrPlan model = plan_csr(*dev, m, n, nnz, (int)sizeof(T));
   CsrArgs<T> a;
   a.m = m; a.n = n; a.nnz = nnz;
   a.row_ptr = row_ptr; a.col_idx = col_idx; a.vals = vals;
@@ -195,22 +249,17 @@ fxtx_status_t csr_impl(int64_t m, int64_t n, int64_t nnz, const int64_t* row_ptr
   a.alpha = (double)alpha; a.beta = (double)beta;
   a.use_z = (z != nullptr && beta != T(0));
 
-  void* ws = nullptr;
-  s = alloc_ws(&ws, plan.ws_bytes, st);
-  if (s != FXTX_OK) return s;
-  char* w = static_cast<char*>(ws);
-  const size_t part_bytes = ((size_t)(plan.ctas + 1) * 8 + 127) / 128 * 128;
-  a.part = reinterpret_cast<int64_t*>(w);
-  a.queue = reinterpret_cast<int64_t*>(w + part_bytes);
-  a.queue_cap = plan.queue_cap;
-  a.counters = reinterpret_cast<unsigned long long*>(w + plan.ws_bytes - 128);
-  cudaError_t e = launch_csr<T>(plan, a, st);
-  cudaFreeAsync(ws, st);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return FXTX_ERR_CUDA;
+  const std::vector<CsrPlan> cands = csr_candidates(*dev, model, m, n, nnz, (int)sizeof(T));
+  TuneKey key;
+  key.kind = 1; key.elem = (int)sizeof(T); key.m = m; key.n = n; key.nnz = nnz;
+  key.sm_count = dev->sm_count;
+  const CsrPlan& plan = cands[choose(key, cands, [&](const CsrPlan& p) { return run_csr<T>(p, a, st); }, st)];
+  if (log_enabled()) {
+    char buf[320];
+    describe(plan, buf, sizeof buf);
+    fprintf(stderr, "[fxtx] m=%lld n=%lld nnz=%lld %s\n", (long long)m, (long long)n, (long long)nnz, buf);
   }
-  return FXTX_OK;
+  return run_csr<T>(plan, a, st);
 }
 
 // k right-hand sides: ceil(k / kb) passes over X, each for kb of them.
@@ -288,7 +337,8 @@ fxtx_status_t fxtx_dense_f64(int64_t m, int64_t n, const double* X, int64_t ld, 
 
 fxtx_status_t fxtx_dense_bf16(int64_t m, int64_t n, const uint16_t* X, int64_t ld, const float* y, const float* v,
                               float alpha, float beta, const float* z, float* out, void* stream) {
-  return dense_bf16_impl(m, n, reinterpret_cast<const __nv_bfloat16*>(X), ld, y, v, alpha, beta, z, out, stream);
+  return dense_impl<__nv_bfloat16>(m, n, reinterpret_cast<const __nv_bfloat16*>(X), ld, y, v, alpha, beta, z, out,
+                                   stream);
 }
 
 fxtx_status_t fxtx_dense_multi_f32(int64_t m, int64_t n, int64_t k, const float* X, int64_t ld, const float* Y,
@@ -391,6 +441,69 @@ fxtx_status_t fxtx_plan_describe(int is_csr, int is_f64, int64_t m, int64_t n, i
     const int64_t l = ld < n ? n : ld;
     const bool tile_ok = (l * elem) % 16 == 0;
     describe(plan_dense(*dev, m, n, l, elem, tile_ok && (n * elem) % 16 == 0, tile_ok), buf, (size_t)cap);
+  }
+  return FXTX_OK;
+}
+
+fxtx_status_t fxtx_autotune_set(int mode) {
+  if (mode != 0 && mode != 1) return FXTX_ERR_INVALID_ARG;
+  tune_set_mode(mode);
+  return FXTX_OK;
+}
+
+int fxtx_autotune_get(void) { return tune_mode(); }
+
+int64_t fxtx_autotune_entries(void) { return tune_entries(); }
+
+fxtx_status_t fxtx_autotune_clear(void) {
+  tune_clear();
+  return FXTX_OK;
+}
+
+fxtx_status_t fxtx_autotune_save(const char* path) {
+  if (path == nullptr) return FXTX_ERR_INVALID_ARG;
+  return tune_save(path) ? FXTX_OK : FXTX_ERR_INVALID_ARG;
+}
+
+fxtx_status_t fxtx_autotune_load(const char* path) {
+  if (path == nullptr) return FXTX_ERR_INVALID_ARG;
+  return tune_load(path) ? FXTX_OK : FXTX_ERR_INVALID_ARG;
+}
+
+fxtx_status_t fxtx_autotune_candidates(int is_csr, int is_f64, int64_t m, int64_t n, int64_t nnz, int64_t ld,
+                                       char* buf, int64_t cap) {
+  if (buf == nullptr || cap <= 0 || m < 0 || n < 0 || nnz < 0) return FXTX_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  DeviceInfo fallback;
+  if (current_device(&dev) != FXTX_OK) {
+    fallback.sm_count = 152;
+    fallback.cc_major = 10;
+    fallback.cc_minor = 3;
+    fallback.smem_optin = 232448;
+    fallback.smem_per_sm = 233472;
+    dev = &fallback;
+  }
+  const int elem = is_f64 ? 8 : 4;
+  size_t used = 0;
+  buf[0] = '\0';
+  auto put = [&](const char* line) {
+    const int w = snprintf(buf + used, (size_t)cap - used, "%s%s", used ? "\n" : "", line);
+    if (w > 0) used = std::min<size_t>((size_t)cap - 1, used + (size_t)w);
+  };
+  char line[320];
+  if (is_csr) {
+    for (const CsrPlan& p : csr_candidates(*dev, plan_csr(*dev, m, n, nnz, elem), m, n, nnz, elem)) {
+      describe(p, line, sizeof line);
+      put(line);
+    }
+  } else {
+    const int64_t l = ld < n ? n : ld;
+    const bool tile_ok = (l * elem) % 16 == 0;
+    const DensePlan model = plan_dense(*dev, m, n, l, elem, tile_ok && (n * elem) % 16 == 0, tile_ok);
+    for (const DensePlan& p : dense_candidates(*dev, model, m, n, elem)) {
+      describe(p, line, sizeof line);
+      put(line);
+    }
   }
   return FXTX_OK;
 }

@@ -64,16 +64,6 @@ __device__ __forceinline__ void smem_fma_add(double* p, double a, double b) {
   } while (old != assumed);
 }
 
-// *p += x in shared memory, fp64.
-__device__ __forceinline__ void smem_add_f64(double* p, double x) {
-  unsigned long long* q = reinterpret_cast<unsigned long long*>(p);
-  unsigned long long old = *q, assumed;
-  do {
-    assumed = old;
-    old = atomicCAS(q, assumed, __double_as_longlong(__longlong_as_double(assumed) + x));
-  } while (old != assumed);
-}
-
 // Shared-memory windows of one CTA: scatters into columns [c0, c0 + len) are
 // accumulated in `acc`, and y[0, ylen) is held in `ys` for the gathers.
 template <typename T>
@@ -216,24 +206,17 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
   unsigned char* scratch =
       smem + window_bytes(win_len, sizeof(T)) + window_bytes(ylen, sizeof(T)) + (size_t)warp * WARP_SCRATCH;
   double* dotb = reinterpret_cast<double*>(scratch);          // [32] row dots of the current batch (fp64)
-  float* dotf = reinterpret_cast<float*>(scratch);             // fp32: [32] sums and [32] compensations
   T* tb = reinterpret_cast<T*>(scratch + 32 * 8);              // [32] row scales alpha * v_i * u_i
   int64_t* rsb = reinterpret_cast<int64_t*>(scratch + 64 * 8);  // [33] row starts of the window
   const Window<T> win{wacc, win_c0, win_len, a.out, ys, ylen, a.y};
   const int64_t re = a.m;
   const T alpha = (T)a.alpha;
 
-  // adds a lane's partial dot of one row segment into the warp's row-dot buffer: fp64 through a
-  // CAS loop; fp32 as the compensated pair (sum and error term) with two native float atomics,
-  // which keeps fp64 units out of the fp32 path
-  auto flush = [&](int row, const DotAcc<T, sizeof(T) == 4>& part) {
-    if constexpr (sizeof(T) == 4) {
-      atomicAdd(&dotf[row], part.s);
-      atomicAdd(&dotf[32 + row], part.c);
-    } else {
-      smem_add_f64(&dotb[row], part.value_f64());
-    }
-  };
+  // adds a lane's partial dot of one row segment into the warp's row-dot buffer, in fp64 (the
+  // fp32 compensated pair converts exactly), with one native shared-memory atomic: segment sums
+  // of one row can cancel, and fp64 keeps their sum's rounding below the fp32 bound
+  auto flush = [&](int row, const DotAcc<T, sizeof(T) == 4>& part) { atomicAdd(&dotb[row], part.value_f64()); };
+
   window_init(win);
   dotb[lane] = 0.0;
   __syncthreads();
@@ -311,15 +294,8 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
       if (have) flush(cur, acc);
       __syncwarp();
       if (lane >= b0 && lane < b1) {
-        T u;
-        if constexpr (sizeof(T) == 4) {
-          u = __fadd_rn(dotf[lane], dotf[32 + lane]);
-          dotf[lane] = 0.f;
-          dotf[32 + lane] = 0.f;
-        } else {
-          u = dotb[lane];
-          dotb[lane] = 0.0;
-        }
+        const T u = (T)dotb[lane];
+        dotb[lane] = 0.0;
         tb[lane] = alpha * (vrow * u);
       }
       __syncwarp();

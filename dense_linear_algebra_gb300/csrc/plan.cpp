@@ -22,6 +22,44 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 size_t align128(size_t x) { return (x + 127) / 128 * 128; }
 
+// Rates of the cost model, per GB300 measurements: HBM copy bandwidth, FMA issue per
+// SM and clock (fp32 124.7, fp64 2), the SM clock, and L2 random-sector throughput.
+constexpr double kHbmBytesPerS = 6.8e12;
+constexpr double kClockHz = 2.07e9;
+constexpr double kFma32PerSmClk = 124.7;
+constexpr double kFma64PerSmClk = 2.0;
+constexpr double kL2SectorsPerS = 4.9e11;
+constexpr double kLaunchUs = 4.0;  // launch, grid reduction and epilogue of one call
+
+// Roofline estimate: the slowest of HBM bytes, FMAs and random L2 sectors, each at the
+// fraction of its peak the kernel kind reaches, plus the fixed cost of a call.
+double roofline_us(const DeviceInfo& dev, double bytes, double hbm_eff, double fmas, int elem, double fma_eff,
+                   double l2_sectors, double l2_eff) {
+  const double fma_rate = (elem == 8 ? kFma64PerSmClk : kFma32PerSmClk) * std::max(dev.sm_count, 1) * kClockHz;
+  double t = bytes / (kHbmBytesPerS * hbm_eff);
+  t = std::max(t, fmas / (fma_rate * fma_eff));
+  t = std::max(t, l2_sectors / (kL2SectorsPerS * l2_eff));
+  return t * 1e6 + kLaunchUs;
+}
+
+// Dense call: X once, v, y, z and out; two FMAs per element of X.
+double dense_est_us(const DeviceInfo& dev, const DensePlan& p, int64_t m, int64_t n, int elem) {
+  const int ce = elem == 2 ? 4 : elem;  // compute-type bytes of the vectors
+  const double bytes = (double)m * n * elem + (double)m * ce + 3.0 * n * ce;
+  static const double hbm_eff[] = {1.0, 1.0, 0.85, 0.5, 0.9, 0.95};  // by DenseKind
+  return roofline_us(dev, bytes, hbm_eff[p.kind], 2.0 * m * n, elem == 2 ? 4 : elem, 0.7, 0.0, 1.0);
+}
+
+// CSR call: vals and col_idx once, row_ptr, v, y, z and out; two FMAs per entry; a
+// random L2 sector for each gather and scatter outside the shared-memory copies,
+// with columns taken as uniform over [0, n).
+double csr_est_us(const DeviceInfo& dev, const CsrPlan& p, int64_t m, int64_t n, int64_t nnz, int elem) {
+  const double bytes = (double)nnz * (elem + 4) + (double)(m + 1) * 8 + (double)m * elem + 3.0 * n * elem;
+  const double nn = (double)std::max<int64_t>(n, 1);
+  const double miss = (1.0 - std::min(1.0, p.ylen / nn)) + (1.0 - std::min(1.0, p.win_len / nn));
+  return roofline_us(dev, bytes, 0.8, 2.0 * nnz, elem, 0.6, miss * nnz, 0.6);
+}
+
 }  // namespace
 
 bool narrow_shape(int64_t chunks, int* lpr, int* vpl) {
@@ -43,7 +81,8 @@ bool narrow_shape(int64_t chunks, int* lpr, int* vpl) {
   return true;
 }
 
-DensePlan plan_dense(const DeviceInfo& dev, int64_t m, int64_t n, int64_t ld, int elem, bool tma_ok, bool tile_ok) {
+static DensePlan plan_dense_model(const DeviceInfo& dev, int64_t m, int64_t n, int64_t ld, int elem, bool tma_ok,
+                                  bool tile_ok) {
   DensePlan p;
   if (n == 0) return p;  // nothing to write
   if (m == 0) {
@@ -128,6 +167,44 @@ DensePlan plan_dense(const DeviceInfo& dev, int64_t m, int64_t n, int64_t ld, in
   return p;
 }
 
+DensePlan plan_dense(const DeviceInfo& dev, int64_t m, int64_t n, int64_t ld, int elem, bool tma_ok, bool tile_ok) {
+  DensePlan p = plan_dense_model(dev, m, n, ld, elem, tma_ok, tile_ok);
+  if (p.kind != DENSE_NOOP) p.est_us = p.kind == DENSE_EMPTY_ROWS ? kLaunchUs : dense_est_us(dev, p, m, n, elem);
+  return p;
+}
+
+std::vector<DensePlan> dense_candidates(const DeviceInfo& dev, const DensePlan& model, int64_t m, int64_t n, int elem) {
+  std::vector<DensePlan> c{model};
+  const int64_t budget = std::min<int64_t>(kSmemBudget, dev.smem_optin > 0 ? dev.smem_optin : 48 * 1024);
+  if (model.kind == DENSE_TILE_TMA) {
+    // pipeline depth and warps per CTA
+    const int64_t tile = (int64_t)model.nb * model.rows_per_tile * model.box_bytes;
+    const int64_t tiles = cdiv(m, model.rows_per_tile);
+    for (int warps : {8, 4})
+      for (int S : {2, 3, 4, 6}) {
+        if (warps == model.warps && S == model.stages) continue;
+        const size_t smem =
+            1024 + std::max<size_t>((size_t)warps * S * (tile + 8), (size_t)warps * n * sizeof(double));
+        if ((int64_t)smem > budget) continue;
+        DensePlan q = model;
+        q.warps = warps;
+        q.stages = S;
+        q.smem = smem;
+        q.ctas = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)dev.sm_count, cdiv(tiles, warps)));
+        q.ws_bytes = align128((size_t)q.ctas * n * sizeof(double)) + 128;
+        q.est_us = dense_est_us(dev, q, m, n, elem);
+        c.push_back(q);
+      }
+  } else if (model.kind == DENSE_WIDE && model.smem_acc) {
+    // the column accumulator in global memory instead of shared memory
+    DensePlan q = model;
+    q.smem_acc = false;
+    q.smem = 0;
+    c.push_back(q);
+  }
+  return c;
+}
+
 CsrPlan plan_csr(const DeviceInfo& dev, int64_t m, int64_t n, int64_t nnz, int elem) {
   CsrPlan p;
   // fp64 short rows go to lane groups sized to the mean row (8 entries per lane); fp32 to packed batches
@@ -156,24 +233,55 @@ CsrPlan plan_csr(const DeviceInfo& dev, int64_t m, int64_t n, int64_t nnz, int e
   p.queue_cap = std::min<int64_t>(m, nnz / (p.warp_cap + 1) + 1);
   p.ws_bytes = align128((size_t)(p.ctas + 1) * 8) +
                align128((size_t)csr_long_buckets() * std::max<int64_t>(p.queue_cap, 1) * 8) + 128;
+  p.est_us = csr_est_us(dev, p, m, n, nnz, elem);
   return p;
+}
+
+std::vector<CsrPlan> csr_candidates(const DeviceInfo& dev, const CsrPlan& model, int64_t m, int64_t n, int64_t nnz,
+                                    int elem) {
+  std::vector<CsrPlan> c{model};
+  const int64_t budget = std::min<int64_t>(kSmemBudget, dev.smem_optin > 0 ? dev.smem_optin : 48 * 1024);
+  const int64_t fixed = (int64_t)csr_rows_smem(0, 0, elem) + 32;
+  const int64_t room = std::max<int64_t>(0, budget - fixed) / elem;
+  // the split of shared memory between the scatter window and the copy of y
+  if (n > room / 2) {
+    for (int eighths : {4, 7}) {
+      CsrPlan q = model;
+      q.win_len = std::min<int64_t>(n, room * eighths / 8);
+      q.ylen = std::min<int64_t>(n, room - q.win_len);
+      if (q.win_len == model.win_len) continue;
+      q.smem = csr_rows_smem(q.win_len, q.ylen, elem);
+      q.long_smem = q.smem - csr_rows_smem(0, 0, elem);
+      q.est_us = csr_est_us(dev, q, m, n, nnz, elem);
+      c.push_back(q);
+    }
+  }
+  // fp64 lane groups one size narrower and one wider
+  if (model.group_lpr > 0)
+    for (int lpr : {model.group_lpr / 2, model.group_lpr * 2}) {
+      if (lpr < 2 || lpr > 16) continue;
+      CsrPlan q = model;
+      q.group_lpr = lpr;
+      c.push_back(q);
+    }
+  return c;
 }
 
 int describe(const DensePlan& p, char* buf, size_t cap) {
   static const char* names[] = {"noop", "empty_rows", "narrow_tma", "narrow_direct", "wide", "tile_tma"};
   return snprintf(buf, cap,
                   "dense kind=%s lanes_per_row=%d chunks_per_lane=%d rows_per_tile=%d stages=%d warps=%d ctas=%d "
-                  "smem=%zu smem_acc=%d blocks=%d box=%d ws=%zu",
+                  "smem=%zu smem_acc=%d blocks=%d box=%d ws=%zu est_us=%.1f",
                   names[p.kind], p.lpr, p.vpl, p.rows_per_tile, p.stages, p.warps, p.ctas, p.smem, (int)p.smem_acc,
-                  p.nbr, p.box_bytes, p.ws_bytes);
+                  p.nbr, p.box_bytes, p.ws_bytes, p.est_us);
 }
 
 int describe(const CsrPlan& p, char* buf, size_t cap) {
   return snprintf(buf, cap,
                   "csr group_lanes=%d pack_k=%d pack_cap=%d warp_cap=%d ctas=%d threads=%d long_ctas=%d "
-                  "window=[%lld,+%lld) y_window=%lld smem=%zu queue_cap=%lld ws=%zu",
+                  "window=[%lld,+%lld) y_window=%lld smem=%zu queue_cap=%lld ws=%zu est_us=%.1f",
                   p.group_lpr, p.pack_k, p.pack_cap, p.warp_cap, p.ctas, p.threads, p.long_ctas, (long long)p.win_c0,
-                  (long long)p.win_len, (long long)p.ylen, p.smem, (long long)p.queue_cap, p.ws_bytes);
+                  (long long)p.win_len, (long long)p.ylen, p.smem, (long long)p.queue_cap, p.ws_bytes, p.est_us);
 }
 
 }  // namespace fxtx

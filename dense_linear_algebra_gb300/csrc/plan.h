@@ -12,6 +12,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <vector>
 
 namespace fxtx {
 
@@ -39,6 +40,7 @@ struct DensePlan {
   size_t smem = 0;        // dynamic shared memory per CTA
   bool smem_acc = false;  // wide: column accumulator kept in shared memory
   size_t ws_bytes = 0;    // device workspace
+  double est_us = 0.0;    // the model's estimate of the launch's duration
 };
 
 // lanes-per-row / chunks-per-lane table of the narrow kernel, keyed by the
@@ -63,6 +65,7 @@ struct CsrPlan {
   int row_cost = 0;         // nnz-equivalent cost of one row, for the partition
   size_t ws_bytes = 0;
   int64_t queue_cap = 0;    // capacity of the long-row queue
+  double est_us = 0.0;      // the model's estimate of the call's duration
 };
 
 // Constants of the CSR kernels (csr.cu): shared memory of the row kernel for an
@@ -77,5 +80,13 @@ CsrPlan plan_csr(const DeviceInfo& dev, int64_t m, int64_t n, int64_t nnz, int e
 
 int describe(const DensePlan& p, char* buf, size_t cap);
 int describe(const CsrPlan& p, char* buf, size_t cap);
+
+// The launches the tuner times for one call shape: the model's plan first, then the
+// variants of its free parameters that fit the device (pipeline depth and warps of
+// the tensor-copy kernels; the shared-memory split between the scatter window and
+// the copy of y, and the fp64 lane-group width, of the CSR kernels).
+std::vector<DensePlan> dense_candidates(const DeviceInfo& dev, const DensePlan& model, int64_t m, int64_t n, int elem);
+std::vector<CsrPlan> csr_candidates(const DeviceInfo& dev, const CsrPlan& model, int64_t m, int64_t n, int64_t nnz,
+                                    int elem);
 
 }  // namespace fxtx

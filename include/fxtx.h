@@ -197,6 +197,35 @@ fxtx_status_t fxtx_plan_describe(int is_csr, int is_f64, int64_t m, int64_t n, i
                                   int64_t ld, char* buf, int64_t cap);
 
 /*
+ * One-shot autotuning of the launch model ("On optimizing machine learning workloads
+ * via kernel fusion", abstract: the analytical model for launch parameters; the model
+ * picks by default). With mode 1, the first dense or CSR call of each shape (m, n,
+ * nnz, ld, element type, alignment class and SM count) runs each of the model's
+ * candidate launches once to warm up and three times timed, on the caller's stream,
+ * and caches the fastest; that call synchronises the stream and leaves the result of
+ * the chosen launch in out. Later calls of the shape, and calls during stream capture,
+ * launch without timing (the model's plan when the shape is not cached). The cache is
+ * process-wide and thread-safe. The initial mode is 1 when the environment variable
+ * FXTX_AUTOTUNE is "1", else 0. The multi-vector and no-allocation entry points always
+ * take the model's plan.
+ *
+ * fxtx_autotune_set: mode 0 or 1 (else FXTX_ERR_INVALID_ARG). fxtx_autotune_save /
+ * _load: a text file, one cached shape per line ("kind elem m n nnz ld flags sm_count
+ * choice candidates best_us model_us", '#' lines ignored); load replaces the cache and
+ * returns FXTX_ERR_INVALID_ARG, leaving it unchanged, for a missing file or a
+ * malformed line. fxtx_autotune_candidates writes the candidate plans of a shape, the
+ * model's first, one per line, as fxtx_plan_describe does (host only).
+ */
+fxtx_status_t fxtx_autotune_set(int mode);
+int fxtx_autotune_get(void);
+int64_t fxtx_autotune_entries(void);
+fxtx_status_t fxtx_autotune_clear(void);
+fxtx_status_t fxtx_autotune_save(const char* path);
+fxtx_status_t fxtx_autotune_load(const char* path);
+fxtx_status_t fxtx_autotune_candidates(int is_csr, int is_f64, int64_t m, int64_t n, int64_t nnz, int64_t ld,
+                                       char* buf, int64_t cap);
+
+/*
  * The launch plan of a multi-vector call (fxtx_dense_multi_*), for logging and
  * tests: v_mode 0 = no weights, 1 = one shared m-vector, 2 = an m x k matrix.
  * Host only; writes a NUL-terminated description of at most `cap` bytes.

@@ -1,0 +1,110 @@
+"""The autotune cache on the device: every candidate launch of a shape meets the oracle's
+bound, a tuned shape is timed once and then served from the cache, and a tuned call's
+result is that of the chosen launch (repeat calls are bitwise equal)."""
+import numpy as np
+import pytest
+import torch
+
+import dense_linear_algebra_gb300 as fx
+import inputgen
+import oracle
+from _gpu import DeviceProblem
+from _util import assert_within_bound
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _restore():
+    mode = fx.autotune_mode()
+    fx.autotune_clear()
+    yield
+    fx.autotune_clear()
+    fx.autotune(mode)
+
+
+def _key_line(kind, elem, m, n, nnz, ld, flags, choice, cands):
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    return f"{kind} {elem} {m} {n} {nnz} {ld} {flags} {sm} {choice} {cands} 1.0 1.0\n"
+
+
+def _run(dp):
+    out = dp.run()
+    torch.cuda.synchronize()
+    assert fx.device_error() == fx.FXTX_OK
+    return out.cpu().numpy().astype(np.float64)
+
+
+def test_every_dense_candidate_meets_the_bound(tmp_path):
+    p = inputgen.dense_tall(m=500_000, variant="b")
+    ref, S = oracle.solve(p)
+    dp = DeviceProblem(p)
+    cands = fx.autotune_candidates("dense", "f32", p.m, p.n, 0, p.ld)
+    fx.autotune(1)
+    for i in range(len(cands)):
+        f = tmp_path / f"c{i}.txt"
+        f.write_text(_key_line(0, 4, p.m, p.n, 0, p.ld, 3, i, len(cands)))
+        fx.autotune_load(str(f))
+        assert_within_bound(_run(dp), ref, S, 2e-5, f"candidate {i}: {cands[i]}")
+
+
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+def test_every_csr_candidate_meets_the_bound(tmp_path, dtype):
+    p = inputgen.csr_powerlaw(m=100_000) if dtype == np.float32 else inputgen.csr_uniform(m=200_000)
+    ref, S = oracle.solve(p)
+    dp = DeviceProblem(p)
+    tag = "f32" if dtype == np.float32 else "f64"
+    cands = fx.autotune_candidates("csr", tag, p.m, p.n, p.nnz)
+    assert len(cands) >= 2
+    fx.autotune(1)
+    for i in range(len(cands)):
+        f = tmp_path / f"c{i}.txt"
+        f.write_text(_key_line(1, p.itemsize, p.m, p.n, p.nnz, 0, 0, i, len(cands)))
+        fx.autotune_load(str(f))
+        assert_within_bound(_run(dp), ref, S, 2e-5 if dtype == np.float32 else 1e-12, f"candidate {i}: {cands[i]}")
+
+
+def test_tuned_once_then_cached(tmp_path):
+    fx.autotune(1)
+    p = inputgen.dense_tall(m=1_000_000, variant="b")
+    q = inputgen.csr_powerlaw(m=100_000)
+    dp, dq = DeviceProblem(p), DeviceProblem(q)
+    a = _run(dp)
+    assert fx.autotune_entries() == 1
+    b = _run(dp)
+    assert fx.autotune_entries() == 1 and np.array_equal(a, b)
+    ref, S = oracle.solve(p)
+    assert_within_bound(a, ref, S, 2e-5)
+    _run(dq)
+    assert fx.autotune_entries() == 2
+    path = tmp_path / "cache.txt"
+    fx.autotune_save(str(path))
+    lines = [ln.split() for ln in path.read_text().splitlines() if not ln.startswith("#")]
+    assert len(lines) == 2
+    for ln in lines:
+        choice, cands, best = int(ln[8]), int(ln[9]), float(ln[10])
+        assert 0 <= choice < cands and best > 0
+    fx.autotune_clear()
+    fx.autotune_load(str(path))
+    assert fx.autotune_entries() == 2
+    assert np.array_equal(_run(dp), a)
+
+
+def test_capture_uses_the_model_without_timing():
+    """Inside stream capture a cache miss launches the model's plan and records nothing."""
+    fx.autotune(1)
+    p = inputgen.dense_tall(m=200_000, variant="b")
+    dp = DeviceProblem(p)
+    out = torch.empty(p.n, dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    dp.run(out=out, stream=s)  # warm-up outside capture would tune: clear it again
+    torch.cuda.synchronize()
+    fx.autotune_clear()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        dp.run(out=out, stream=s)
+    assert fx.autotune_entries() == 0
+    g.replay()
+    torch.cuda.synchronize()
+    ref, S = oracle.solve(p)
+    assert_within_bound(out.cpu().numpy().astype(np.float64), ref, S, 2e-5)

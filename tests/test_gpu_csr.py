@@ -107,6 +107,28 @@ def test_duplicates_and_unsorted(dtype):
     check(p)
 
 
+@pytest.mark.parametrize("L", [40, 200, 700, 3000])
+def test_row_dots_that_cancel(L):
+    """Rows whose entries cancel to a small dot: the first half +a_k (integers in [64, 128)), the
+    second half -a_k + e_k with e_k a few units of 2^-17 (all exact in fp32), y = 1. Partial sums
+    reach thousands while the dot is ~1e-3, so a row's segments (across lanes, packed batches
+    or warps) must be summed without losing the small remainder: the bound is relative to |t_i|."""
+    m, n = 3000, 4 * L
+    lens = np.full(m, L, dtype=np.int64)
+    rp = inputgen.row_ptr_from_lengths(lens)
+    col = inputgen.csr_columns(5, n, rp, 0.0)
+    half = L // 2
+    a = (64.0 + (np.arange(m * half) % 61)).reshape(m, half)
+    e = ((np.arange(m * half) % 7) + 1).reshape(m, half) * 2.0 ** -17
+    vals = np.concatenate([a, -a + e], axis=1).astype(np.float32)
+    assert np.array_equal(vals[:, half:2 * half].astype(np.float64), -a + e)
+    if L % 2:
+        vals = np.concatenate([vals, np.zeros((m, 1), np.float32)], axis=1)
+    p = inputgen.Problem(f"csr_cancel_{L}", "csr", np.float32, m, n, 1.0, 0.0, y=np.ones(n, np.float32),
+                         v=None, z=None, row_ptr=rp, col_idx=col, vals=vals.ravel())
+    check(p)
+
+
 @pytest.mark.parametrize("dtype", [np.float32, np.float64])
 def test_integer_inputs_are_exact(dtype):
     rng = np.random.default_rng(12)
