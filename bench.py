@@ -93,6 +93,23 @@ def is_multi(p) -> bool:
     return p.kind == "dense" and p.y.ndim == 2
 
 
+def model_estimate(p):
+    """The launch model's plan for the call and its roofline estimate of the duration."""
+    import dense_linear_algebra_gb300 as fx
+
+    if is_multi(p):
+        vm = "none" if p.v is None else ("full" if p.v.ndim == 2 else "shared")
+        return {"plan": fx.multi_plan_describe(dtype_name(p), p.m, p.n, p.y.shape[1], vm, p.ld)}
+    if p.kind == "csr":
+        desc = fx.plan_describe("csr", dtype_name(p), p.m, p.n, p.nnz)
+    elif p.x_store == "bf16":
+        return {"plan": "bfloat16 X: the fp32 model's tile plan with 2-byte elements"}
+    else:
+        desc = fx.plan_describe("dense", dtype_name(p), p.m, p.n, 0, p.ld)
+    f = dict(kv.split("=") for kv in desc.split()[1:] if "=" in kv)
+    return {"plan": desc, "est_us": float(f.get("est_us", "nan"))}
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -502,6 +519,7 @@ def run_fused(args, name, desc, p, rank, world, dist):
                      "peak_source": f"{peak_kind} HBM copy bandwidth",
                      "kernel": kernel},
         "unfused_library": unfused,
+        "model": model_estimate(p),
     }
     if is_multi(p):
         # k right-hand sides: two FMAs (4 flops) per stored element per right-hand side, on the fp32 or fp64 pipe
