@@ -298,7 +298,6 @@ fxtx_status_t dense_multi_impl(int64_t m, int64_t n, int64_t k, const T* X, int6
   a.m = m; a.n = n; a.ld = ld; a.X = X;
   a.ldy = ldy; a.ldv = V != nullptr ? ldv : 0; a.ldz = ldz; a.ldo = ldo;
   a.alpha = (double)alpha; a.beta = (double)beta; a.use_z = use_z;
-  a.tiles = (m + plan.rows_per_tile - 1) / plan.rows_per_tile;
   a.ws = static_cast<double*>(ws);
   a.ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + plan.ws_bytes - 128);
   cudaError_t e = cudaMemsetAsync(a.ticket, 0, sizeof(unsigned), st);

@@ -51,6 +51,14 @@ struct Chunk<double> {
   }
 };
 
+// Rows per tile for rows of nb 128-byte blocks and kb right-hand sides of `elem` bytes:
+// 8-KB tiles of X (16 KB at nb = 16), which give each lane several independent rows per
+// tile; 4-KB tiles for one right-hand side (an HBM-bound pass) and where a tile's weights
+// would outgrow half its X (more than 64 bytes of weights a row).
+__host__ __device__ constexpr int multi_rows(int nb, int kb, int elem) {
+  return nb >= 8 ? 8 : ((kb == 1 || kb * elem > 64) ? 32 : 64) / nb;
+}
+
 // Geometry for rows of NB 128-byte blocks and KB right-hand sides per pass.
 template <typename T, int NB, int KB>
 struct MShape {
@@ -58,7 +66,7 @@ struct MShape {
   static constexpr int Q = 8;                     // chunks per lane
   static constexpr int C = Q * NV;                // columns per lane
   static constexpr int RS = 32 / (NB * KB);       // row slots of a warp
-  static constexpr int R = NB >= 4 ? 8 : 32 / NB; // rows per tile
+  static constexpr int R = multi_rows(NB, KB, (int)sizeof(T));  // rows per tile
   static constexpr int IT = R / RS;               // rows per lane per tile
   static constexpr int BOX = R * 128;             // bytes of one 128-byte column block of a tile
   static constexpr int TILE = NB * BOX;           // bytes of X in one pipeline stage
@@ -122,6 +130,54 @@ __device__ __forceinline__ float row_sum_comp(float s, float c) {
     c = __fadd_rn(__fadd_rn(c, c2), q);
   }
   return __fadd_rn(s, c);
+}
+
+// A lane's per-tile column sums tacc[c] += t * x[c]. fp32 keeps them as packed pairs and
+// updates two columns per instruction (fma.rn.f32x2); each element still rounds once.
+template <typename T, int C>
+struct ColSums {
+  T v[C];
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int c = 0; c < C; ++c) v[c] = T(0);
+  }
+  __device__ __forceinline__ void add(T t, const T* x) {
+#pragma unroll
+    for (int c = 0; c < C; ++c) v[c] = fma(t, x[c], v[c]);
+  }
+  __device__ __forceinline__ T get(int c) const { return v[c]; }
+};
+template <int C>
+struct ColSums<float, C> {
+  float2 v[C / 2];
+  __device__ __forceinline__ void zero() {
+#pragma unroll
+    for (int c = 0; c < C / 2; ++c) v[c] = make_float2(0.f, 0.f);
+  }
+  __device__ __forceinline__ void add(float t, const float* x) {
+    const float2 t2 = make_float2(t, t);
+#pragma unroll
+    for (int c = 0; c < C / 2; ++c) v[c] = __ffma2_rn(t2, make_float2(x[2 * c], x[2 * c + 1]), v[c]);
+  }
+  __device__ __forceinline__ float get(int c) const { return (c & 1) ? v[c >> 1].y : v[c >> 1].x; }
+};
+
+// A lane's partial dot x . y over its C columns in working precision: four independent
+// chains (fp32: two chains of packed pairs).
+template <typename T, int C>
+__device__ __forceinline__ T lane_dot(const T* x, const T* y) {
+  if constexpr (sizeof(T) == 4) {
+    float2 d[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+    for (int c = 0; c < C / 2; ++c)
+      d[c & 1] = __ffma2_rn(make_float2(x[2 * c], x[2 * c + 1]), make_float2(y[2 * c], y[2 * c + 1]), d[c & 1]);
+    return (d[0].x + d[0].y) + (d[1].x + d[1].y);
+  } else {
+    T d4[4] = {T(0), T(0), T(0), T(0)};
+#pragma unroll
+    for (int c = 0; c < C; ++c) d4[c & 3] = fma(x[c], y[c], d4[c & 3]);
+    return (d4[0] + d4[1]) + (d4[2] + d4[3]);
+  }
 }
 
 // CTA partials -> workspace; the last CTA to arrive sums them in a fixed order and
@@ -269,9 +325,8 @@ __global__ void __launch_bounds__(MULTI_THREADS, 1)
   }
 
   typename OuterAcc<T>::type acc[C];
-  T tacc[C];
-#pragma unroll
-  for (int c = 0; c < C; ++c) tacc[c] = T(0);
+  ColSums<T, C> tacc;
+  tacc.zero();
 
   for (int64_t k = 0; k < nt; ++k) {
     const int64_t tile = t0 + k;
@@ -313,22 +368,16 @@ __global__ void __launch_bounds__(MULTI_THREADS, 1)
           for (int c = 0; c < C; ++c) dacc.add(x[c], yr[c]);
           d = row_sum_comp<NB, KB>(dacc.s, dacc.c);
         } else {
-          T d4[4] = {T(0), T(0), T(0), T(0)};
-#pragma unroll
-          for (int c = 0; c < C; ++c) d4[c & 3] = fma(x[c], yr[c], d4[c & 3]);
-          d = row_sum<T, NB, KB>((d4[0] + d4[1]) + (d4[2] + d4[3]));
+          d = row_sum<T, NB, KB>(lane_dot<T, C>(x, yr));
         }
         const T t = vmode == 0 ? d : vb[vmode == 2 ? r * KB + cg : r] * d;
-#pragma unroll
-        for (int c = 0; c < C; ++c) tacc[c] = fma(t, x[c], tacc[c]);
+        tacc.add(t, x);
       }
     }
     if (sizeof(T) == 8 || (k + 1) % FOLD == 0 || k + 1 == nt) {
 #pragma unroll
-      for (int c = 0; c < C; ++c) {
-        acc[c].add(tacc[c]);
-        tacc[c] = T(0);
-      }
+      for (int c = 0; c < C; ++c) acc[c].add(tacc.get(c));
+      tacc.zero();
     }
     __syncwarp();
     if (tma && k + S < nt) {
@@ -365,7 +414,6 @@ static int pow2ceil(int64_t x) {
   return p;
 }
 
-static int multi_rows(int nb) { return nb >= 4 ? 8 : 32 / nb; }
 
 MultiPlan plan_multi(const DeviceInfo& dev, int64_t m, int64_t n, int64_t k, int elem, bool tma_ok, bool full_v,
                      bool has_v) {
@@ -375,19 +423,25 @@ MultiPlan plan_multi(const DeviceInfo& dev, int64_t m, int64_t n, int64_t k, int
   p.nb = pow2ceil((n * elem + 127) / 128);
   p.kb_max = (int)std::min<int64_t>(32 / p.nb, pow2ceil(k));
   p.passes = (int)((k + p.kb_max - 1) / p.kb_max);
-  p.rows_per_tile = multi_rows(p.nb);
+  p.rows_per_tile = multi_rows(p.nb, p.kb_max, elem);
   // m == 0 runs the same kernel over no tiles (it writes beta Z); tensor maps need m > 0
   p.tma = tma_ok && m > 0 && m < (int64_t(1) << 31);
-  // a stage holds R rows of X and their weights
-  const size_t vb = full_v ? (size_t)p.rows_per_tile * p.kb_max : (has_v ? (size_t)p.rows_per_tile : 0);
-  const size_t tile = (size_t)p.nb * p.rows_per_tile * 128 + ((vb * elem + 127) & ~size_t(127));
+  // a stage holds a tile of X and its weights; the widest pass (all kb_max, or the
+  // remainder's width) sets the stage size
+  auto stage_bytes = [&](int kb) {
+    const int64_t R = multi_rows(p.nb, kb, elem);
+    const int64_t vb = full_v ? R * kb : (has_v ? R : 0);
+    return (size_t)(p.nb * R * 128) + (size_t)((vb * elem + 127) & ~int64_t(127));
+  };
+  size_t tile = stage_bytes(p.kb_max);
+  if (k % p.kb_max != 0) tile = std::max(tile, stage_bytes(pow2ceil(k % p.kb_max)));
   const size_t budget = std::min<size_t>(MULTI_SMEM_BUDGET, dev.smem_optin > 0 ? (size_t)dev.smem_optin : MULTI_SMEM_BUDGET);
-  // eight warps with a pipeline of 2 to 4 tiles each; four warps where eight do not fit (16 KB tiles)
+  // eight warps with a pipeline of 2 to 8 stages each; four warps where eight do not fit
   p.warps = MULTI_THREADS / 32;
   if (p.tma) {
     for (;;) {
       const size_t room = budget - 1024;
-      p.stages = (int)std::min<size_t>(4, room / (p.warps * (tile + 8)));
+      p.stages = (int)std::min<size_t>(8, room / (p.warps * (tile + 8)));
       if (p.stages >= 2 || p.warps == 4) break;
       p.warps = 4;
     }
@@ -417,28 +471,35 @@ int describe_multi(const MultiPlan& p, char* buf, size_t cap) {
 int take_multi_device_error() { return take_device_error(); }
 
 template <typename T, int NB, int KB>
-static cudaError_t launch_kb(const MultiPlan& p, const CUtensorMap& map, const MultiArgs<T>& a, int vmode,
-                             cudaStream_t st) {
+static cudaError_t launch_kb(const MultiPlan& p, const MultiArgs<T>& a0, int vmode, cudaStream_t st) {
+  constexpr int R = MShape<T, NB, KB>::R;
+  MultiArgs<T> a = a0;
+  a.tiles = (a.m + R - 1) / R;
+  CUtensorMap map;
+  memset(&map, 0, sizeof map);
+  // a map the driver refuses sends the pass to the plain-load staging
+  MultiPlan q = p;
+  q.tma = p.tma && encode_rows_map(&map, Chunk<T>::MAP, a.X, a.m, a.n, a.ld * (int64_t)sizeof(T), (int)sizeof(T), R,
+                                   128, 0);
   const void* kern = (const void*)dense_multi_kernel<T, NB, KB>;
-  cudaError_t e = ensure_smem(kern, p.smem);
+  cudaError_t e = ensure_smem(kern, q.smem);
   if (e != cudaSuccess) return e;
   // whole rows of weights in 16-byte copies: a full pass over 16-byte aligned rows
   const int v16 = vmode == 2 && a.kb == KB && KB * sizeof(T) >= 16 && (reinterpret_cast<uintptr_t>(a.V) & 15u) == 0 &&
                   (a.ldv * (int64_t)sizeof(T)) % 16 == 0;
-  dense_multi_kernel<T, NB, KB><<<p.ctas, p.warps * 32, p.smem, st>>>(map, a, p.stages, p.tma ? 1 : 0, vmode, v16);
+  dense_multi_kernel<T, NB, KB><<<q.ctas, q.warps * 32, q.smem, st>>>(map, a, q.stages, q.tma ? 1 : 0, vmode, v16);
   return cudaGetLastError();
 }
 
 template <typename T, int NB>
-static cudaError_t launch_nb(const MultiPlan& p, const CUtensorMap& map, const MultiArgs<T>& a, int vmode,
-                             cudaStream_t st) {
+static cudaError_t launch_nb(const MultiPlan& p, const MultiArgs<T>& a, int vmode, cudaStream_t st) {
   switch (pow2ceil(a.kb)) {
-    case 1: return launch_kb<T, NB, 1>(p, map, a, vmode, st);
-    case 2: return launch_kb<T, NB, 2>(p, map, a, vmode, st);
-    case 4: if constexpr (NB <= 8) return launch_kb<T, NB, 4>(p, map, a, vmode, st); break;
-    case 8: if constexpr (NB <= 4) return launch_kb<T, NB, 8>(p, map, a, vmode, st); break;
-    case 16: if constexpr (NB <= 2) return launch_kb<T, NB, 16>(p, map, a, vmode, st); break;
-    case 32: if constexpr (NB == 1) return launch_kb<T, NB, 32>(p, map, a, vmode, st); break;
+    case 1: return launch_kb<T, NB, 1>(p, a, vmode, st);
+    case 2: return launch_kb<T, NB, 2>(p, a, vmode, st);
+    case 4: if constexpr (NB <= 8) return launch_kb<T, NB, 4>(p, a, vmode, st); break;
+    case 8: if constexpr (NB <= 4) return launch_kb<T, NB, 8>(p, a, vmode, st); break;
+    case 16: if constexpr (NB <= 2) return launch_kb<T, NB, 16>(p, a, vmode, st); break;
+    case 32: if constexpr (NB == 1) return launch_kb<T, NB, 32>(p, a, vmode, st); break;
     default: break;
   }
   return cudaErrorInvalidConfiguration;
@@ -447,19 +508,13 @@ static cudaError_t launch_nb(const MultiPlan& p, const CUtensorMap& map, const M
 template <typename T>
 cudaError_t launch_multi(const MultiPlan& p, const MultiArgs<T>& a, cudaStream_t st) {
   if (!p.ok || a.kb < 1 || a.kb > p.kb_max) return cudaErrorInvalidConfiguration;
-  CUtensorMap map;
-  memset(&map, 0, sizeof map);
-  // a map the driver refuses sends the pass to the plain-load staging
-  MultiPlan q = p;
-  q.tma = p.tma && encode_rows_map(&map, Chunk<T>::MAP, a.X, a.m, a.n, a.ld * (int64_t)sizeof(T), (int)sizeof(T),
-                                   p.rows_per_tile, 128, 0);
   const int vmode = a.V == nullptr ? 0 : (a.ldv == 0 ? 1 : 2);
   switch (p.nb) {
-    case 1: return launch_nb<T, 1>(q, map, a, vmode, st);
-    case 2: return launch_nb<T, 2>(q, map, a, vmode, st);
-    case 4: return launch_nb<T, 4>(q, map, a, vmode, st);
-    case 8: return launch_nb<T, 8>(q, map, a, vmode, st);
-    case 16: return launch_nb<T, 16>(q, map, a, vmode, st);
+    case 1: return launch_nb<T, 1>(p, a, vmode, st);
+    case 2: return launch_nb<T, 2>(p, a, vmode, st);
+    case 4: return launch_nb<T, 4>(p, a, vmode, st);
+    case 8: return launch_nb<T, 8>(p, a, vmode, st);
+    case 16: return launch_nb<T, 16>(p, a, vmode, st);
     default: return cudaErrorInvalidConfiguration;
   }
 }

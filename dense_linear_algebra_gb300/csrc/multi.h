@@ -35,7 +35,7 @@ struct MultiArgs {
   bool use_z = false;
   double* ws = nullptr;        // [ctas][n * KB] partials of each CTA
   unsigned* ticket = nullptr;  // arrival counter of the last-CTA reduction, zero at launch
-  int64_t tiles = 0;           // ceil(m / rows_per_tile)
+  int64_t tiles = 0;           // ceil(m / rows per tile), set by the launcher for the pass's kernel
 };
 
 // Launch shape of one multi-vector call. A call of k right-hand sides runs
@@ -46,7 +46,7 @@ struct MultiPlan {
   int nb = 0;           // 128-byte blocks per row (1, 2, 4, 8, 16)
   int kb_max = 0;       // right-hand sides per pass (a power of two, 32 / nb at most)
   int passes = 0;
-  int rows_per_tile = 0;
+  int rows_per_tile = 0;  // of a kb_max-wide pass (a narrower last pass may take taller tiles)
   int stages = 0;
   int warps = 0;
   int ctas = 0;

@@ -97,7 +97,8 @@ def test_launch_model_grid_and_smem_limits():
 @pytest.mark.parametrize(
     "args,expect",
     [
-        (("f32", 16_000_000, 32, 8), "tma=1 blocks=1 kb=8 passes=1 rows_per_tile=32 stages=4 warps=8 ctas=152"),
+        (("f32", 16_000_000, 32, 8), "tma=1 blocks=1 kb=8 passes=1 rows_per_tile=64 stages=2 warps=8 ctas=152"),
+        (("f32", 16_000_000, 32, 1), "kb=1 passes=1 rows_per_tile=32 stages=6"),
         (("f32", 16_000_000, 32, 40), "kb=32 passes=2"),
         (("f32", 1000, 32, 3), "kb=4 passes=1"),
         (("f64", 1000, 128, 8, "shared"), "blocks=8 kb=4 passes=2 rows_per_tile=8"),
