@@ -99,7 +99,8 @@ def model_estimate(p):
 
     if is_multi(p):
         vm = "none" if p.v is None else ("full" if p.v.ndim == 2 else "shared")
-        return {"plan": fx.multi_plan_describe(dtype_name(p), p.m, p.n, p.y.shape[1], vm, p.ld)}
+        desc = fx.multi_plan_describe(dtype_name(p), p.m, p.n, p.y.shape[1], vm, p.ld)
+        return {"plan": desc, "est_us": float(dict(kv.split("=") for kv in desc.split()[1:])["est_us"])}
     if p.kind == "csr":
         desc = fx.plan_describe("csr", dtype_name(p), p.m, p.n, p.nnz)
     elif p.x_store == "bf16":
@@ -587,12 +588,42 @@ def run_solver(args):
         torch.cuda.synchronize()
         out[name] = {"ms_per_iteration": round(e0.elapsed_time(e1) / info.iterations, 4),
                      "relative_residual": true_res}
+    # k = 8 targets: block CG with one multi-vector call per iteration, against the cuBLAS
+    # GEMM pair, per iteration of all eight solves
+    k = 8
+    B = torch.mm(X, torch.from_numpy(inputgen.normal(0, 9, (p.n, k), np.float32)).to(dev))
+    rhs_k = torch.mm(X.t(), B).contiguous()
+
+    def fused_multi_op(P):
+        return solvers.fused_multi(X, P.contiguous(), None, 1.0, lam, P.contiguous())
+
+    def unfused_multi_op(P):
+        return torch.mm(X.t(), torch.mm(X, P)) + lam * P
+
+    for name, op in (("fused_multi_k8", fused_multi_op), ("unfused_cublas_k8", unfused_multi_op)):
+        solvers.cg_block(op, rhs_k, tol=0.0, max_iter=3, check_every=3)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        W, info = solvers.cg_block(op, rhs_k, tol=0.0, max_iter=iters, check_every=iters)
+        true_res = float((torch.linalg.vector_norm(rhs_k - op(W), dim=0) / torch.linalg.vector_norm(rhs_k, dim=0)).max())
+        e1.record()
+        torch.cuda.synchronize()
+        out[name] = {"ms_per_iteration": round(e0.elapsed_time(e1) / info.iterations, 4),
+                     "relative_residual": true_res}
     rec = {"metric": "ridge regression by conjugate gradients: ms per CG iteration", "unit": "ms",
            "higher_is_better": False, "data": "synthetic",
            "config": {"workload": f"X {p.m} x {p.n} fp32 N(0,1), b = X w + 0.1 noise, lambda = 1, {iters} iterations",
                       "operator": "X^T (X p) + lambda p"},
            "fused": out["fused"], "unfused_cublas": out["unfused_cublas"],
-           "speedup": round(out["unfused_cublas"]["ms_per_iteration"] / out["fused"]["ms_per_iteration"], 3)}
+           "speedup": round(out["unfused_cublas"]["ms_per_iteration"] / out["fused"]["ms_per_iteration"], 3),
+           "k8": {"operator": "X^T (X P) + lambda P for 8 targets (block CG)", "fused_multi": out["fused_multi_k8"],
+                  "unfused_cublas": out["unfused_cublas_k8"],
+                  "speedup": round(out["unfused_cublas_k8"]["ms_per_iteration"] /
+                                   out["fused_multi_k8"]["ms_per_iteration"], 3),
+                  "vs_8_single_solves": round(8 * out["fused"]["ms_per_iteration"] /
+                                              out["fused_multi_k8"]["ms_per_iteration"], 3)}}
     print(json.dumps(rec), flush=True)
 
 

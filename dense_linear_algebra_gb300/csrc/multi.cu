@@ -455,6 +455,12 @@ MultiPlan plan_multi(const DeviceInfo& dev, int64_t m, int64_t n, int64_t k, int
   const int64_t tiles = (m + p.rows_per_tile - 1) / p.rows_per_tile;
   p.ctas = (int)std::max<int64_t>(1, std::min<int64_t>(dev.sm_count, (tiles + p.warps - 1) / p.warps));
   p.ws_bytes = (size_t)p.ctas * n * p.kb_max * sizeof(double) + 128;
+  // the model's estimate: every pass reads X; weights, Y, Z and OUT once; two FMAs per element
+  // of X and right-hand side, at the ~35 % of the FMA rate this kernel's issue rate allows
+  const double vbytes = full_v ? (double)m * k * elem : (has_v ? (double)m * elem * p.passes : 0.0);
+  const double bytes = (double)m * n * elem * p.passes + vbytes + 3.0 * n * k * elem;
+  p.est_us = roofline_us(dev, bytes, 0.9, 2.0 * m * n * k, elem, elem == 4 ? 0.35 : 0.8, 0.0, 1.0) +
+             4.0 * (p.passes - 1);
   return p;
 }
 
@@ -463,9 +469,11 @@ int multi_pass_kb(const MultiPlan& p, int64_t k, int64_t c0) {
 }
 
 int describe_multi(const MultiPlan& p, char* buf, size_t cap) {
-  return snprintf(buf, cap, "multi ok=%d tma=%d blocks=%d kb=%d passes=%d rows_per_tile=%d stages=%d warps=%d ctas=%d smem=%zu ws=%zu",
+  return snprintf(buf, cap,
+                  "multi ok=%d tma=%d blocks=%d kb=%d passes=%d rows_per_tile=%d stages=%d warps=%d ctas=%d smem=%zu "
+                  "ws=%zu est_us=%.1f",
                   (int)p.ok, (int)p.tma, p.nb, p.kb_max, p.passes, p.rows_per_tile, p.stages, p.warps, p.ctas, p.smem,
-                  p.ws_bytes);
+                  p.ws_bytes, p.est_us);
 }
 
 int take_multi_device_error() { return take_device_error(); }

@@ -52,6 +52,7 @@ struct MultiPlan {
   int ctas = 0;
   size_t smem = 0;
   size_t ws_bytes = 0;  // per-CTA partials of the widest pass, plus the ticket
+  double est_us = 0.0;  // the model's estimate of the call (all passes)
 };
 
 MultiPlan plan_multi(const DeviceInfo& dev, int64_t m, int64_t n, int64_t k, int elem, bool tma_ok, bool full_v,

@@ -31,6 +31,8 @@ constexpr double kFma64PerSmClk = 2.0;
 constexpr double kL2SectorsPerS = 4.9e11;
 constexpr double kLaunchUs = 4.0;  // launch, grid reduction and epilogue of one call
 
+}  // namespace
+
 // Roofline estimate: the slowest of HBM bytes, FMAs and random L2 sectors, each at the
 // fraction of its peak the kernel kind reaches, plus the fixed cost of a call.
 double roofline_us(const DeviceInfo& dev, double bytes, double hbm_eff, double fmas, int elem, double fma_eff,
@@ -41,6 +43,8 @@ double roofline_us(const DeviceInfo& dev, double bytes, double hbm_eff, double f
   t = std::max(t, l2_sectors / (kL2SectorsPerS * l2_eff));
   return t * 1e6 + kLaunchUs;
 }
+
+namespace {
 
 // Dense call: X once, v, y, z and out; two FMAs per element of X.
 double dense_est_us(const DeviceInfo& dev, const DensePlan& p, int64_t m, int64_t n, int elem) {

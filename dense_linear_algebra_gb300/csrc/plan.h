@@ -78,6 +78,13 @@ int csr_long_buckets();  // length buckets of the long-row queue
 
 CsrPlan plan_csr(const DeviceInfo& dev, int64_t m, int64_t n, int64_t nnz, int elem);
 
+// The cost model's roofline (in microseconds, one call): the slowest of `bytes` through
+// HBM at hbm_eff of 6.8 TB/s, `fmas` at fma_eff of the device's FMA rate for elements of
+// `elem` bytes, and `l2_sectors` random 32-byte L2 accesses at l2_eff of 4.9e11 per second,
+// plus the fixed cost of a call.
+double roofline_us(const DeviceInfo& dev, double bytes, double hbm_eff, double fmas, int elem, double fma_eff,
+                   double l2_sectors, double l2_eff);
+
 int describe(const DensePlan& p, char* buf, size_t cap);
 int describe(const CsrPlan& p, char* buf, size_t cap);
 

@@ -7,6 +7,8 @@ textbook consumers of ``alpha * X^T (v * (X p)) + beta * z``:
 * ``ridge_cg``: least squares with an L2 penalty, ``min ||X w - b||^2 + lam ||w||^2``,
   solved by conjugate gradients on ``(X^T X + lam I) w = X^T b``. Every operator
   application ``X^T (X p) + lam p`` is ONE fused call (v = 1, z = p, beta = lam).
+* ``ridge_cg_multi``: the same for k targets at once (block CG); every iteration applies
+  the operator to all k search directions in ONE multi-vector call, one pass over X.
 * ``logistic_newton_cg``: L2-regularised logistic regression by Newton's method;
   each Newton step solves ``(X^T D X + lam I) d = -g`` by conjugate gradients, where
   every Hessian-vector product ``X^T (D * (X p)) + lam p`` is ONE fused call with
@@ -114,6 +116,57 @@ def ridge_cg(X, b, lam: float, tol: float = 1e-6, max_iter: int = 200):
     m, n, dt, dev = _shape(X)
     rhs = rmatvec(X, b)
     return cg(lambda p: fused(X, p, None, 1.0, lam, p), rhs, tol=tol, max_iter=max_iter)
+
+
+def fused_multi(X, P, V, alpha: float, beta: float, Z, out=None):
+    """alpha * X^T (V * (X P)) + beta * Z for k right-hand sides (dense X): one pass over X."""
+    return _lib.dense_multi(X, P, V, alpha, beta, Z, out=out)
+
+
+def cg_block(apply, rhs, tol: float = 1e-6, max_iter: int = 100, check_every: int = 1):
+    """k independent conjugate-gradient solves in lockstep, one per column of `rhs` (n, k).
+
+    `apply` maps an (n, k) block to the operator applied to each column, so one call
+    serves all k solves. Each column has its own step sizes; a column whose residual
+    reaches zero stops moving. Converged when every column's relative residual is <= tol.
+    """
+    x = torch.zeros_like(rhs)
+    r = rhs.clone()
+    p = r.clone()
+    rs = (r * r).sum(dim=0)
+    bnorm = torch.linalg.vector_norm(rhs, dim=0)
+    info = CGInfo()
+    safe_b = torch.where(bnorm > 0, bnorm, torch.ones_like(bnorm))
+    if float(bnorm.max()) == 0.0:
+        info.converged = True
+        return x, info
+    for k in range(max_iter):
+        q = apply(p)
+        pq = (p * q).sum(dim=0)
+        a = torch.where(pq > 0, rs / torch.where(pq > 0, pq, torch.ones_like(pq)), torch.zeros_like(pq))
+        x.add_(a * p)
+        r.sub_(a * q)
+        rs_new = (r * r).sum(dim=0)
+        info.iterations = k + 1
+        if (k + 1) % check_every == 0 or k + 1 == max_iter:
+            res = float((torch.sqrt(rs_new) / safe_b).max())
+            info.residual = res
+            info.history.append(res)
+            if res <= tol:
+                info.converged = True
+                break
+        b = torch.where(rs > 0, rs_new / torch.where(rs > 0, rs, torch.ones_like(rs)), torch.zeros_like(rs))
+        p.mul_(b).add_(r)
+        rs = rs_new
+    return x, info
+
+
+def ridge_cg_multi(X, B, lam: float, tol: float = 1e-6, max_iter: int = 200):
+    """Ridge regression for k targets at once (B is (m, k)): block CG in which every
+    iteration applies X^T (X P) + lam P to all k directions in one multi-vector call."""
+    rhs = torch.mm(X.t(), B).contiguous()
+    return cg_block(lambda P: fused_multi(X, P.contiguous(), None, 1.0, lam, P.contiguous()), rhs, tol=tol,
+                    max_iter=max_iter)
 
 
 @dataclass

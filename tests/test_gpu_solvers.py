@@ -21,6 +21,19 @@ def test_cg_on_cpu_operator():
     assert np.allclose(x.numpy(), np.linalg.solve(A.numpy(), b.numpy()), rtol=1e-9, atol=1e-10)
 
 
+def test_cg_block_on_cpu_operator():
+    """The block CG driver alone (no GPU): k columns, an SPD matrix applied by torch."""
+    rng = np.random.default_rng(1)
+    A = rng.standard_normal((25, 25))
+    A = torch.from_numpy(A @ A.T + 25 * np.eye(25))
+    B = torch.from_numpy(rng.standard_normal((25, 4)))
+    B[:, 2] = 0.0  # a zero right-hand side stays at zero
+    x, info = solvers.cg_block(lambda P: A @ P, B, tol=1e-12, max_iter=200)
+    assert info.converged
+    assert np.allclose(x.numpy(), np.linalg.solve(A.numpy(), B.numpy()), rtol=1e-9, atol=1e-10)
+    assert np.all(x.numpy()[:, 2] == 0.0)
+
+
 def _ridge_ref(X, b, lam):
     return np.linalg.solve(X.T @ X + lam * np.eye(X.shape[1]), X.T @ b)
 
@@ -36,6 +49,23 @@ def test_ridge_cg_dense(dtype, m, n, rtol):
     Xd = torch.from_numpy(X.astype(dtype)).cuda()
     bd = torch.from_numpy(b.astype(dtype)).cuda()
     w, info = solvers.ridge_cg(Xd, bd, lam, tol=1e-10 if dtype == np.float64 else 1e-5, max_iter=200)
+    assert info.iterations <= 3 * n
+    assert np.linalg.norm(w.cpu().numpy() - ref) <= rtol * np.linalg.norm(ref)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("dtype,rtol", [(np.float64, 1e-9), (np.float32, 2e-3)])
+def test_ridge_cg_multi(dtype, rtol):
+    """k = 6 targets solved together with the multi-vector operator match six direct solves."""
+    m, n, k = 20_000, 32, 6
+    X = inputgen.normal(4, 1, (m, n), np.float64)
+    W = inputgen.normal(4, 2, (n, k), np.float64)
+    B = X @ W + 0.1 * inputgen.normal(4, 3, (m, k), np.float64)
+    lam = 0.5
+    ref = np.linalg.solve(X.T @ X + lam * np.eye(n), X.T @ B)
+    Xd = torch.from_numpy(X.astype(dtype)).cuda()
+    Bd = torch.from_numpy(B.astype(dtype)).cuda()
+    w, info = solvers.ridge_cg_multi(Xd, Bd, lam, tol=1e-10 if dtype == np.float64 else 1e-5, max_iter=200)
     assert info.iterations <= 3 * n
     assert np.linalg.norm(w.cpu().numpy() - ref) <= rtol * np.linalg.norm(ref)
 
