@@ -559,18 +559,20 @@ __global__ void __launch_bounds__(WIDE_THREADS) dense_wide_kernel(const DenseArg
     // in the reverse of pass 1's order, so it starts on the lines pass 1 brought into L2 last
     // and the re-read comes from L2 rather than HBM as far as L2 holds the CTAs' rows.
     for (int64_t j = nvec * NV + threadIdx.x; j < n; j += blockDim.x) {
-      T s = T(0);
+      // fp64: the FMA chain starts from the accumulator (no separate add); fp32: a step's
+      // products are summed in fp32 and added in fp64
+      T s = sizeof(T) == 8 ? (T)acc[j] : T(0);
 #pragma unroll
       for (int r = 0; r < WIDE_R; ++r)
         if (r < rows) s = fma(t[r], a.X[(i0 + r) * ld + j], s);
-      acc[j] += (double)s;
+      if constexpr (sizeof(T) == 8) acc[j] = (double)s; else acc[j] += (double)s;
     }
     const int64_t nk = threadIdx.x < nvec ? (nvec - 1 - threadIdx.x) / blockDim.x + 1 : 0;
     for (int64_t kk = nk - 1; kk >= 0; --kk) {
       const int64_t c = threadIdx.x + kk * blockDim.x;
       T s[NV];
 #pragma unroll
-      for (int e = 0; e < NV; ++e) s[e] = T(0);
+      for (int e = 0; e < NV; ++e) s[e] = sizeof(T) == 8 ? (T)acc[c * NV + e] : T(0);
 #pragma unroll
       for (int r = 0; r < WIDE_R; ++r) {
         if (r < rows) {
@@ -581,7 +583,9 @@ __global__ void __launch_bounds__(WIDE_THREADS) dense_wide_kernel(const DenseArg
         }
       }
 #pragma unroll
-      for (int e = 0; e < NV; ++e) acc[c * NV + e] += (double)s[e];
+      for (int e = 0; e < NV; ++e) {
+        if constexpr (sizeof(T) == 8) acc[c * NV + e] = (double)s[e]; else acc[c * NV + e] += (double)s[e];
+      }
     }
     __syncthreads();  // s_dot / s_t reuse
   }
