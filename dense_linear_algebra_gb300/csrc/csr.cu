@@ -215,7 +215,20 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
   // adds a lane's partial dot of one row segment into the warp's row-dot buffer, in fp64 (the
   // fp32 compensated pair converts exactly), with one native shared-memory atomic: segment sums
   // of one row can cancel, and fp64 keeps their sum's rounding below the fp32 bound
-  auto flush = [&](int row, const DotAcc<T, sizeof(T) == 4>& part) { atomicAdd(&dotb[row], part.value_f64()); };
+  auto flush = [&](int row, const DotAcc<T, sizeof(T) == 4>& part) {
+    if constexpr (sizeof(T) == 4) {
+      // float-float row dot: the atomic returns the old sum, so the rounding error of the
+      // addition it made is recovered exactly (TwoSum) and added, with the segment's own
+      // compensation, into the low word
+      float* dotf = reinterpret_cast<float*>(dotb);
+      const float old = atomicAdd(&dotf[row], part.s);
+      float sum, err;
+      two_sum(old, part.s, sum, err);
+      atomicAdd(&dotf[32 + row], __fadd_rn(err, part.c));
+    } else {
+      atomicAdd(&dotb[row], part.value_f64());
+    }
+  };
 
   window_init(win);
   dotb[lane] = 0.0;
@@ -294,8 +307,16 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
       if (have) flush(cur, acc);
       __syncwarp();
       if (lane >= b0 && lane < b1) {
-        const T u = (T)dotb[lane];
-        dotb[lane] = 0.0;
+        T u;
+        if constexpr (sizeof(T) == 4) {
+          float* dotf = reinterpret_cast<float*>(dotb);
+          u = __fadd_rn(dotf[lane], dotf[32 + lane]);
+          dotf[lane] = 0.f;
+          dotf[32 + lane] = 0.f;
+        } else {
+          u = (T)dotb[lane];
+          dotb[lane] = 0.0;
+        }
         tb[lane] = alpha * (vrow * u);
       }
       __syncwarp();
