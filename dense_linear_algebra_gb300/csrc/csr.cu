@@ -41,7 +41,7 @@ struct Pack {
   static constexpr int K = sizeof(T) == 4 ? 8 : 4;
   static constexpr int CAP = 32 * K;  // entries per packed batch
 };
-constexpr int WARP_LONG = 1024;            // longest row a single warp takes
+constexpr int WARP_LONG = 2048;            // longest row a single warp takes
 constexpr int WARP_UNROLL = 8;             // loads in flight per lane for warp rows
 // entries per lane and batch in the long-row kernel (fp64 keeps fewer, to fit 64 registers)
 template <typename T>
@@ -49,7 +49,7 @@ __host__ __device__ constexpr int long_unroll() {
   return sizeof(T) == 4 ? 8 : 4;
 }
 constexpr int LONG_GROUP = 128;            // threads that share one long row
-constexpr int LONG_BUCKETS = 6;            // long-row queues: (1K, 2K], (2K, 4K], ... (16K, 32K], > 32K entries
+constexpr int LONG_BUCKETS = 6;            // long-row queues: (2K, 4K], (4K, 8K], ... (32K, 64K], > 64K entries
 // per-warp scratch after the window: 32 row dots (double), 32 row scales (T), 33 row starts
 constexpr size_t WARP_SCRATCH = 32 * 8 + 32 * 8 + 33 * 8;
 
@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
   T* ys = reinterpret_cast<T*>(smem + window_bytes(win_len, sizeof(T)));
   unsigned char* scratch =
       smem + window_bytes(win_len, sizeof(T)) + window_bytes(ylen, sizeof(T)) + (size_t)warp * WARP_SCRATCH;
-  double* dotb = reinterpret_cast<double*>(scratch);          // [32] row dots of the current batch (fp64)
+  double* dotb = reinterpret_cast<double*>(scratch);  // [32] row dots of the batch (fp32: [64] float-float words)
   T* tb = reinterpret_cast<T*>(scratch + 32 * 8);              // [32] row scales alpha * v_i * u_i
   int64_t* rsb = reinterpret_cast<int64_t*>(scratch + 64 * 8);  // [33] row starts of the window
   const Window<T> win{wacc, win_c0, win_len, a.out, ys, ylen, a.y};
