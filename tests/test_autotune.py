@@ -29,10 +29,10 @@ def test_candidates_start_with_the_model_and_fit(args):
 
 
 def test_model_estimates_are_rooflines():
-    """The tall fp32 workload: 2.112 GB at 95 % of 6.8 TB/s plus the fixed call cost."""
+    """The tall fp32 workload: 2.112 GB at 99 % of 6.8 TB/s plus the fixed call cost."""
     d = fx.plan_describe("dense", "f32", 16_000_000, 32)
     est = float(dict(kv.split("=") for kv in d.split()[1:])["est_us"])
-    assert abs(est - (2_112_000_384 / (6.8e12 * 0.95) * 1e6 + 4.0)) < 1.0
+    assert abs(est - (2_112_000_384 / (6.8e12 * 0.99) * 1e6 + 4.0)) < 1.0
     # the fp64 wide workload is bound by its 8e8 fp64 FMAs at 2 per SM and clock (70 % of that rate)
     d = fx.plan_describe("dense", "f64", 20_000, 20_000)
     est = float(dict(kv.split("=") for kv in d.split()[1:])["est_us"])
