@@ -533,6 +533,14 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
   window_flush(wacc, win_c0, win_len, a.out);
 }
 
+template <typename T, int LPR, int KG>
+static cudaError_t launch_group(const CsrPlan& p, const CsrArgs<T>& a, cudaStream_t st) {
+  const cudaError_t e = ensure_smem((const void*)csr_group_kernel<T, LPR, KG>, p.long_smem);
+  if (e != cudaSuccess) return e;
+  csr_group_kernel<T, LPR, KG><<<p.ctas, p.threads, p.long_smem, st>>>(a, p.win_c0, p.win_len, p.ylen);
+  return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t launch_csr(const CsrPlan& p, const CsrArgs<T>& a, cudaStream_t st) {
   {
@@ -549,19 +557,18 @@ cudaError_t launch_csr(const CsrPlan& p, const CsrArgs<T>& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     csr_rows_kernel<T><<<p.ctas, p.threads, p.smem, st>>>(a, p.win_c0, p.win_len, p.ylen);
   } else {
-    const void* k = p.group_lpr == 4    ? (const void*)csr_group_kernel<T, 4, 8>
-                    : p.group_lpr == 8  ? (const void*)csr_group_kernel<T, 8, 8>
-                    : p.group_lpr == 16 ? (const void*)csr_group_kernel<T, 16, 8>
-                                        : (const void*)csr_group_kernel<T, 2, 8>;
-    e = ensure_smem(k, p.long_smem);
-    if (e != cudaSuccess) return e;
-    switch (p.group_lpr) {
-      case 2: csr_group_kernel<T, 2, 8><<<p.ctas, p.threads, p.long_smem, st>>>(a, p.win_c0, p.win_len, p.ylen); break;
-      case 4: csr_group_kernel<T, 4, 8><<<p.ctas, p.threads, p.long_smem, st>>>(a, p.win_c0, p.win_len, p.ylen); break;
-      case 8: csr_group_kernel<T, 8, 8><<<p.ctas, p.threads, p.long_smem, st>>>(a, p.win_c0, p.win_len, p.ylen); break;
-      case 16: csr_group_kernel<T, 16, 8><<<p.ctas, p.threads, p.long_smem, st>>>(a, p.win_c0, p.win_len, p.ylen); break;
+    switch (p.group_lpr * 100 + p.group_kg) {
+      case 208: e = launch_group<T, 2, 8>(p, a, st); break;
+      case 408: e = launch_group<T, 4, 8>(p, a, st); break;
+      case 808: e = launch_group<T, 8, 8>(p, a, st); break;
+      case 1608: e = launch_group<T, 16, 8>(p, a, st); break;
+      case 216: e = launch_group<T, 2, 16>(p, a, st); break;
+      case 416: e = launch_group<T, 4, 16>(p, a, st); break;
+      case 816: e = launch_group<T, 8, 16>(p, a, st); break;
+      case 1616: e = launch_group<T, 16, 16>(p, a, st); break;
       default: return cudaErrorInvalidConfiguration;
     }
+    if (e != cudaSuccess) return e;
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -53,7 +53,8 @@ bool narrow_shape(int64_t chunks, int* lpr, int* vpl);
 DensePlan plan_dense(const DeviceInfo& dev, int64_t m, int64_t n, int64_t ld, int elem, bool tma_ok, bool tile_ok);
 
 struct CsrPlan {
-  int group_lpr = 0;        // short rows in lane groups of this many lanes (x 8 entries); 0: packed batches
+  int group_lpr = 0;        // short rows in lane groups of this many lanes; 0: packed batches
+  int group_kg = 0;         // entries each lane of a group holds (8 or 16)
   int pack_k = 0;           // consecutive entries per lane in a packed batch of short rows
   int pack_cap = 0;         // entries per packed batch (32 * pack_k): longer rows are not packed
   int warp_cap = 0;         // longest row one warp takes; longer rows go to the long-row kernel

@@ -74,7 +74,7 @@ def test_no_device_is_reported_as_unsupported():
         (("dense", "f64", 20_000, 20_000), "kind=wide"),
         (("dense", "f32", 10, 3), "kind=narrow_direct"),
         (("dense", "f32", 0, 3), "kind=empty_rows"),
-        (("csr", "f64", 4_000_000, 10_000, 200_000_000), "csr group_lanes=8 pack_k=4 pack_cap=128 warp_cap=2048 ctas=152"),
+        (("csr", "f64", 4_000_000, 10_000, 200_000_000), "csr group_lanes=4 group_entries=16 pack_k=4 pack_cap=128 warp_cap=2048 ctas=152"),
         (("csr", "f32", 2_000_000, 1_000_000, 200_000_000), "window=[0,+"),
     ],
 )
