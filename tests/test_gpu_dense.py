@@ -209,3 +209,35 @@ def test_allocation_failure_is_reported():
     out = fx.dense(X, y)
     torch.cuda.synchronize()
     assert torch.isfinite(out).all() and fx.device_error() == fx.FXTX_OK
+
+
+def test_allocation_failure_is_reported_by_every_entry():
+    """The same hook through the multi-vector and CSR entry points, and through a tuned call
+    (a candidate whose workspace cannot be had is skipped; the call then reports the failure)."""
+    import os
+
+    X = torch.rand(2000, 32, device="cuda")
+    Y = torch.rand(32, 4, device="cuda")
+    rp = torch.arange(0, 2001 * 5, 5, dtype=torch.int64, device="cuda")
+    ci = (torch.arange(2000 * 5, device="cuda") % 32).to(torch.int32)
+    va = torch.rand(2000 * 5, device="cuda")
+    y = torch.rand(32, device="cuda")
+    mode = fx.autotune_mode()
+    os.environ["FXTX_FAIL_ALLOC"] = "1"
+    try:
+        for tuned in (0, 1):
+            fx.autotune(tuned)
+            fx.autotune_clear()
+            for call in (lambda: fx.dense_multi(X, Y), lambda: fx.csr(rp, ci, va, y, 32), lambda: fx.dense(X, y)):
+                with pytest.raises(fx.FxtxError) as ei:
+                    call()
+                assert ei.value.status == fx.FXTX_ERR_ALLOC
+            assert fx.autotune_entries() == 0
+    finally:
+        del os.environ["FXTX_FAIL_ALLOC"]
+        fx.autotune_clear()
+        fx.autotune(mode)
+    out = fx.dense_multi(X, Y)
+    o2 = fx.csr(rp, ci, va, y, 32)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all() and torch.isfinite(o2).all() and fx.device_error() == fx.FXTX_OK
