@@ -80,9 +80,15 @@ def dominant_kernel(p) -> str:
     if is_multi(p):
         return "dense_multi_kernel"
     if p.kind == "csr":
-        # rows longer than 256 entries go to the long-row kernel; it dominates when they hold most entries
+        # rows longer than the plan's one-warp limit go to the long-row kernel, which dominates
+        # when they hold most entries; otherwise the row kernel of the plan (lane groups for
+        # fp64, packed batches for fp32)
+        desc = fx.plan_describe("csr", dtype_name(p), p.m, p.n, p.nnz)
+        f = dict(kv.split("=") for kv in desc.split()[1:] if "=" in kv)
         lens = np.diff(p.row_ptr)
-        return "csr_long_kernel" if lens[lens > 256].sum() > 0.5 * p.nnz else "csr_rows_kernel"
+        if lens[lens > int(f["warp_cap"])].sum() > 0.5 * p.nnz:
+            return "csr_long_kernel"
+        return "csr_group_kernel" if int(f["group_lanes"]) > 0 else "csr_rows_kernel"
     desc = fx.plan_describe("dense", dtype_name(p), p.m, p.n, 0, p.ld)
     kind = dict(kv.split("=") for kv in desc.split()[1:] if "=" in kv)["kind"]
     return {"tile_tma": "dense_tile_kernel", "narrow_tma": "dense_narrow_kernel", "narrow_direct": "dense_narrow_kernel",
