@@ -24,7 +24,7 @@
  * Alongside out it returns the error scale
  *     S_j = |alpha| * sum_i |t_i| * |X_ij| + |beta * z_j|
  * in double, against which results computed in another summation order are
- * judged.
+ * checked.
  *
  * Sparse X is CSR: row_ptr (int64, m+1 entries, row_ptr[0] = 0, non-decreasing,
  * row_ptr[m] = nnz), col_idx (int32, 0 <= col < n) and vals. Column order inside
