@@ -17,10 +17,12 @@
  * `stream` is a cudaStream_t (NULL for the legacy default stream). Calls are
  * asynchronous with respect to the host, like cuBLAS: they return after the
  * work is enqueued on `stream`, and errors of execution surface at the caller's
- * next synchronisation (and through fxtx_device_error). The library allocates
- * only transient workspace, with cudaMallocAsync on `stream` and freed with
- * cudaFreeAsync on the same stream; it keeps no global cache, so concurrent
- * calls on different streams are safe.
+ * next synchronisation (and through fxtx_device_error). The one exception is the
+ * first call of a shape with autotuning switched on (fxtx_autotune_set), which
+ * times its candidates and synchronises `stream`. The library allocates only
+ * transient workspace, with cudaMallocAsync on `stream` and freed with
+ * cudaFreeAsync on the same stream; besides the opt-in autotune cache it keeps no
+ * global state between calls, so concurrent calls on different streams are safe.
  *
  * Aliasing: out may equal z (in place). Any other overlap of out with an input
  * is undefined.
