@@ -54,12 +54,22 @@ def test_csr_powerlaw_recipe_scaled():
 
 
 @pytest.mark.parametrize("dtype", [np.float32, np.float64])
-@pytest.mark.parametrize("L", [0, 1, 2, 3, 5, 8, 16, 17, 33, 63, 64, 65, 128, 255, 256, 257, 1000, 4097])
+@pytest.mark.parametrize("L", [0, 1, 2, 3, 5, 8, 16, 17, 33, 63, 64, 65, 128, 255, 256, 257, 1000, 2048, 2049, 4097,
+                               8193])
 def test_uniform_row_lengths(dtype, L):
     """Every row of the same length: short / medium / long bins and their boundaries."""
     n = max(8000, L)
     m = 3000 if L <= 256 else 200
     check(make_csr(dtype, np.full(m, L), n, seed=L))
+
+
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+def test_very_long_rows_every_bucket(dtype):
+    """Rows in every long-row length bucket, up to beyond 64K entries (the last bucket),
+    among short rows, so that the longest-first claim order spans all six buckets."""
+    lens = np.full(4000, 7)
+    lens[[5, 700, 1500, 2200, 3000, 3100, 3999]] = [2100, 5000, 9000, 17000, 33000, 70000, 100000]
+    check(make_csr(dtype, lens, 120_000, seed=9))
 
 
 @pytest.mark.parametrize("dtype", [np.float32, np.float64])
