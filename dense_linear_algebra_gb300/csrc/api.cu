@@ -139,9 +139,12 @@ fxtx_status_t run_csr(const CsrPlan& plan, CsrArgs<T> a, cudaStream_t st) {
 // The candidate to launch for `key`: the model's plan (index 0) unless autotuning is on.
 // On a cache miss outside stream capture, every candidate runs once to warm up and
 // then three times between events on the caller's stream (so the call synchronises),
-// and the fastest is cached. `run` enqueues one complete call with a candidate.
+// and the fastest is cached. `run(plan, o)` enqueues one complete call with a
+// candidate, writing to `o` instead of out when `o` is not NULL: the timed runs write
+// to a scratch vector of `out_bytes`, so out keeps its value (and z, which out may
+// equal, is read unchanged by every run).
 template <typename P, typename Run>
-int choose(const TuneKey& key, const std::vector<P>& cands, Run run, cudaStream_t st) {
+int choose(const TuneKey& key, const std::vector<P>& cands, Run run, size_t out_bytes, cudaStream_t st) {
   if (cands.size() < 2 || tune_mode() == 0) return 0;
   int choice = 0;
   if (tune_lookup(key, &choice)) return choice < (int)cands.size() ? choice : 0;
@@ -150,20 +153,28 @@ int choose(const TuneKey& key, const std::vector<P>& cands, Run run, cudaStream_
     cudaGetLastError();
     return 0;
   }
+  void* scratch = nullptr;
+  if (alloc_ws(&scratch, out_bytes, st) != FXTX_OK) return 0;
   cudaEvent_t e0, e1;
-  if (cudaEventCreate(&e0) != cudaSuccess) return 0;
+  if (cudaEventCreate(&e0) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFreeAsync(scratch, st);
+    return 0;
+  }
   if (cudaEventCreate(&e1) != cudaSuccess) {
+    cudaGetLastError();
     cudaEventDestroy(e0);
+    cudaFreeAsync(scratch, st);
     return 0;
   }
   double best = 0.0;
   int bi = -1;
   for (int i = 0; i < (int)cands.size(); ++i) {
-    if (run(cands[i]) != FXTX_OK) continue;
+    if (run(cands[i], scratch) != FXTX_OK) continue;
     float t = 0.f, tmin = 0.f;
     bool ok = true;
     for (int rep = 0; rep < 3 && ok; ++rep) {
-      ok = cudaEventRecord(e0, st) == cudaSuccess && run(cands[i]) == FXTX_OK &&
+      ok = cudaEventRecord(e0, st) == cudaSuccess && run(cands[i], scratch) == FXTX_OK &&
            cudaEventRecord(e1, st) == cudaSuccess && cudaEventSynchronize(e1) == cudaSuccess &&
            cudaEventElapsedTime(&t, e0, e1) == cudaSuccess;
       if (ok && (rep == 0 || t < tmin)) tmin = t;
@@ -176,6 +187,8 @@ int choose(const TuneKey& key, const std::vector<P>& cands, Run run, cudaStream_
   cudaGetLastError();
   cudaEventDestroy(e0);
   cudaEventDestroy(e1);
+  cudaFreeAsync(scratch, st);
+  cudaGetLastError();
   if (bi < 0) return 0;
   tune_store(key, bi, (int)cands.size(), best, cands[0].est_us);
   if (log_enabled())
@@ -218,7 +231,12 @@ fxtx_status_t dense_impl(int64_t m, int64_t n, const TX* X, int64_t ld, const ty
   key.kind = 0; key.elem = elem; key.m = m; key.n = n; key.ld = ld;
   key.flags = (tile_ok ? 1 : 0) | (tma_ok ? 2 : 0);
   key.sm_count = dev->sm_count;
-  const DensePlan& plan = cands[choose(key, cands, [&](const DensePlan& p) { return run_dense<TX>(p, a, st); }, st)];
+  auto run = [&](const DensePlan& p, void* o) {
+    DenseArgs<T, TX> b = a;
+    if (o) b.out = static_cast<T*>(o);
+    return run_dense<TX>(p, b, st);
+  };
+  const DensePlan& plan = cands[choose(key, cands, run, (size_t)n * sizeof(T), st)];
   if (log_enabled()) {
     char buf[320];
     describe(plan, buf, sizeof buf);
@@ -253,7 +271,12 @@ fxtx_status_t csr_impl(int64_t m, int64_t n, int64_t nnz, const int64_t* row_ptr
   TuneKey key;
   key.kind = 1; key.elem = (int)sizeof(T); key.m = m; key.n = n; key.nnz = nnz;
   key.sm_count = dev->sm_count;
-  const CsrPlan& plan = cands[choose(key, cands, [&](const CsrPlan& p) { return run_csr<T>(p, a, st); }, st)];
+  auto run = [&](const CsrPlan& p, void* o) {
+    CsrArgs<T> b = a;
+    if (o) b.out = static_cast<T*>(o);
+    return run_csr<T>(p, b, st);
+  };
+  const CsrPlan& plan = cands[choose(key, cands, run, (size_t)n * sizeof(T), st)];
   if (log_enabled()) {
     char buf[320];
     describe(plan, buf, sizeof buf);

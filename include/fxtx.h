@@ -205,11 +205,13 @@ fxtx_status_t fxtx_plan_describe(int is_csr, int is_f64, int64_t m, int64_t n, i
  * nnz, ld, element type, alignment class and SM count) runs each of the model's
  * candidate launches once to warm up and three times timed, on the caller's stream,
  * and caches the fastest; that call synchronises the stream and leaves the result of
- * the chosen launch in out. Later calls of the shape, and calls during stream capture,
- * launch without timing (the model's plan when the shape is not cached). The cache is
- * process-wide and thread-safe. The initial mode is 1 when the environment variable
- * FXTX_AUTOTUNE is "1", else 0. The multi-vector and no-allocation entry points always
- * take the model's plan.
+ * the chosen launch in out. The timed runs write to a scratch vector of n elements
+ * (cudaMallocAsync on the stream; if it cannot be had, the call takes the model's plan
+ * untimed), so out may equal z on that call too. Later calls of the shape, and calls
+ * during stream capture, launch without timing (the model's plan when the shape is not
+ * cached). The cache is process-wide and thread-safe. The initial mode is 1 when the
+ * environment variable FXTX_AUTOTUNE is "1", else 0. The multi-vector and no-allocation
+ * entry points always take the model's plan.
  *
  * fxtx_autotune_set: mode 0 or 1 (else FXTX_ERR_INVALID_ARG). fxtx_autotune_save /
  * _load: a text file, one cached shape per line ("kind elem m n nnz ld flags sm_count
