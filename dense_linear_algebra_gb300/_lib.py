@@ -1,6 +1,7 @@
 """ctypes binding over libfusedxtx's C ABI (argument marshalling only)."""
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -164,11 +165,17 @@ def _stream(stream, device):
     return stream.cuda_stream
 
 
+def _on(dev_index):
+    """The calls run on the current device: make it the tensors' device for the call."""
+    torch = _torch()
+    return torch.cuda.device(dev_index) if torch.cuda.current_device() != dev_index else contextlib.nullcontext()
+
+
 def _vec(t, dtype, length, name, dev_index):
     if t is None:
         return None
     if (t.dtype is not dtype or not t.is_cuda or t.get_device() != dev_index or t.dim() != 1
-            or t.shape[0] != length or t.stride(0) != 1):
+            or t.shape[0] != length or (length > 1 and t.stride(0) != 1)):
         raise ValueError(f"{name}: expected a contiguous {dtype} vector of length {length} on cuda:{dev_index}")
     return t
 
@@ -195,15 +202,16 @@ def dense(X, y, v=None, alpha: float = 1.0, beta: float = 0.0, z=None, out=None,
     if out is None:
         out = torch.empty(n, dtype=dt, device=X.device)
     _vec(out, dt, n, "out", di)
-    st = _stream(stream, X.device)
     if X.dtype == torch.bfloat16:
-        rc = fxtx_dense_bf16(m, n, _ptr(X), ld, _ptr(y), _ptr(v), alpha, beta, _ptr(z), _ptr(out), st)
+        fn = fxtx_dense_bf16
     elif dt == torch.float32:
-        rc = fxtx_dense_f32(m, n, _ptr(X), ld, _ptr(y), _ptr(v), alpha, beta, _ptr(z), _ptr(out), st)
+        fn = fxtx_dense_f32
     elif dt == torch.float64:
-        rc = fxtx_dense_f64(m, n, _ptr(X), ld, _ptr(y), _ptr(v), alpha, beta, _ptr(z), _ptr(out), st)
+        fn = fxtx_dense_f64
     else:
         raise TypeError(f"unsupported dtype {dt}")
+    with _on(di):
+        rc = fn(m, n, _ptr(X), ld, _ptr(y), _ptr(v), alpha, beta, _ptr(z), _ptr(out), _stream(stream, X.device))
     _check(rc, "fxtx_dense")
     return out
 
@@ -245,15 +253,15 @@ def dense_multi(X, Y, V=None, alpha: float = 1.0, beta: float = 0.0, Z=None, out
     if out is None:
         out = torch.empty((n, k), dtype=dt, device=X.device)
     ldo = _rows(out, dt, (n, k), "out", di)
-    st = _stream(stream, X.device)
     if dt == torch.float32:
         fn = fxtx_dense_multi_f32
     elif dt == torch.float64:
         fn = fxtx_dense_multi_f64
     else:
         raise TypeError(f"unsupported dtype {dt}")
-    rc = fn(m, n, k, _ptr(X), ld, _ptr(Y), max(ldy, k), _ptr(V), ldv, alpha, beta, _ptr(Z), max(ldz, k) if Z is not None else 0,
-            _ptr(out), max(ldo, k), st)
+    with _on(di):
+        rc = fn(m, n, k, _ptr(X), ld, _ptr(Y), max(ldy, k), _ptr(V), ldv, alpha, beta, _ptr(Z),
+                max(ldz, k) if Z is not None else 0, _ptr(out), max(ldo, k), _stream(stream, X.device))
     _check(rc, "fxtx_dense_multi")
     return out
 
@@ -262,34 +270,44 @@ def csr(row_ptr, col_idx, vals, y, n: int, v=None, alpha: float = 1.0, beta: flo
         stream=None):
     """The same pattern for CSR X: int64 row_ptr (m + 1), int32 col_idx and vals (nnz), n columns."""
     torch = _torch()
-    if row_ptr.dtype != torch.int64 or col_idx.dtype != torch.int32:
-        raise ValueError("row_ptr must be int64 and col_idx int32")
+    if row_ptr.dim() != 1 or row_ptr.shape[0] < 1 or vals.dim() != 1 or not vals.is_cuda:
+        raise ValueError("row_ptr (m + 1) and vals (nnz) must be 1-D, vals a CUDA tensor")
     m = row_ptr.shape[0] - 1
     nnz = vals.shape[0]
     dt, dev = vals.dtype, vals.device
     di = vals.get_device()
+    _vec(row_ptr, torch.int64, m + 1, "row_ptr", di)
+    _vec(col_idx, torch.int32, nnz, "col_idx", di)
+    _vec(vals, dt, nnz, "vals", di)
     y = _vec(y, dt, n, "y", di)
     v = _vec(v, dt, m, "v", di)
     z = _vec(z, dt, n, "z", di)
     if out is None:
         out = torch.empty(n, dtype=dt, device=dev)
     _vec(out, dt, n, "out", di)
-    st = _stream(stream, dev)
-    args = (m, n, nnz, _ptr(row_ptr), _ptr(col_idx), _ptr(vals), _ptr(y), _ptr(v), alpha, beta, _ptr(z), _ptr(out), st)
     if dt == torch.float32:
-        rc = fxtx_csr_f32(*args)
+        fn = fxtx_csr_f32
     elif dt == torch.float64:
-        rc = fxtx_csr_f64(*args)
+        fn = fxtx_csr_f64
     else:
         raise TypeError(f"unsupported dtype {dt}")
+    with _on(di):
+        rc = fn(m, n, nnz, _ptr(row_ptr), _ptr(col_idx), _ptr(vals), _ptr(y), _ptr(v), alpha, beta, _ptr(z), _ptr(out),
+                _stream(stream, dev))
     _check(rc, "fxtx_csr")
     return out
 
 
 def csr_validate(row_ptr, col_idx, n: int, stream=None) -> bool:
     """True if the CSR structure is well formed (synchronous device check)."""
-    m = row_ptr.shape[0] - 1
-    rc = fxtx_csr_validate(m, n, col_idx.shape[0], _ptr(row_ptr), _ptr(col_idx), _stream(stream, row_ptr.device))
+    torch = _torch()
+    if row_ptr.dim() != 1 or row_ptr.shape[0] < 1 or not row_ptr.is_cuda or col_idx.dim() != 1:
+        raise ValueError("row_ptr (m + 1) and col_idx (nnz) must be 1-D CUDA tensors")
+    m, di = row_ptr.shape[0] - 1, row_ptr.get_device()
+    _vec(row_ptr, torch.int64, m + 1, "row_ptr", di)
+    _vec(col_idx, torch.int32, col_idx.shape[0], "col_idx", di)
+    with _on(di):
+        rc = fxtx_csr_validate(m, n, col_idx.shape[0], _ptr(row_ptr), _ptr(col_idx), _stream(stream, row_ptr.device))
     if rc == FXTX_ERR_BAD_CSR:
         return False
     _check(rc, "fxtx_csr_validate")

@@ -54,6 +54,25 @@ def test_invalid_arguments_rejected_on_host():
     assert fx.fxtx_csr_validate(0, 3, 2, None, None, None) == fx.FXTX_ERR_BAD_CSR
 
 
+def test_binding_rejects_host_tensors():
+    """The torch binding hands only device pointers to the library: host tensors, wrong
+    dtypes and wrong lengths are refused in Python, before any C call."""
+    import torch
+
+    X, y = torch.zeros(8, 4), torch.zeros(4)
+    with pytest.raises(ValueError):
+        fx.dense(X, y)
+    with pytest.raises(ValueError):
+        fx.dense_multi(X, torch.zeros(4, 2))
+    rp, ci, va = torch.zeros(9, dtype=torch.int64), torch.zeros(0, dtype=torch.int32), torch.zeros(0)
+    with pytest.raises(ValueError):
+        fx.csr(rp, ci, va, y, 4)
+    with pytest.raises(ValueError):
+        fx.csr_validate(rp, ci, 4)
+    with pytest.raises(ValueError):
+        fx.csr(rp.view(3, 3), ci, va, y, 4)
+
+
 def test_no_device_is_reported_as_unsupported():
     import torch
 
