@@ -19,7 +19,8 @@
 // The y gathers of hot columns hit a copy of y[0, ylen) in shared memory.
 // Row dots of a packed batch are formed lane-locally per row segment, and each
 // segment's partial is added once into a per-warp fp64 buffer; t_i is then
-// computed once per row. Each CTA (one per SM, 1024 threads) accumulates
+// computed once per row. Each CTA (one per SM; 1024 threads, 768 for the fp64
+// lane groups) accumulates
 // scatters into a shared-memory window of columns and flushes it once with one
 // atomic per column; columns outside the window go straight to out with
 // atomics. fp64 window updates fold the product into the atomic itself (a CAS
@@ -35,6 +36,9 @@ namespace fxtx {
 namespace {
 
 constexpr int CSR_THREADS = 1024;
+// the lane-group kernel: 768 threads leave 80 registers a thread, so the 16-entry lane
+// buffers of fp64 rows stay in registers (at 1024 threads, 64 registers, they spill)
+constexpr int CSR_GROUP_THREADS = 768;
 // consecutive entries per lane in a packed batch (fp64 keeps fewer, to fit 64 registers)
 template <typename T>
 struct Pack {
@@ -124,6 +128,7 @@ size_t csr_rows_smem(int64_t win_len, int64_t ylen, int elem) {
 }
 int csr_pack_cap(int elem) { return elem == 4 ? Pack<float>::CAP : Pack<double>::CAP; }
 int csr_warp_long() { return WARP_LONG; }
+int csr_group_threads() { return CSR_GROUP_THREADS; }
 int csr_long_buckets() { return LONG_BUCKETS; }
 
 // out = beta z (or 0); row partition; counters.
@@ -359,7 +364,7 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
 // per-segment flushes), so the fp64 path uses it. Rows longer than LPR * KG go
 // to warp_row or to the long-row queue.
 template <typename T, int LPR, int KG>
-__global__ void __launch_bounds__(CSR_THREADS, 1)
+__global__ void __launch_bounds__(CSR_GROUP_THREADS, 1)
     csr_group_kernel(const CsrArgs<T> a, const int64_t win_c0, const int64_t win_len, const int64_t ylen) {
   constexpr int G = 32 / LPR;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -535,6 +540,7 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
 
 template <typename T, int LPR, int KG>
 static cudaError_t launch_group(const CsrPlan& p, const CsrArgs<T>& a, cudaStream_t st) {
+  if (p.threads != CSR_GROUP_THREADS) return cudaErrorInvalidConfiguration;
   const cudaError_t e = ensure_smem((const void*)csr_group_kernel<T, LPR, KG>, p.long_smem);
   if (e != cudaSuccess) return e;
   csr_group_kernel<T, LPR, KG><<<p.ctas, p.threads, p.long_smem, st>>>(a, p.win_c0, p.win_len, p.ylen);

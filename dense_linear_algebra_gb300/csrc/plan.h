@@ -75,6 +75,7 @@ struct CsrPlan {
 size_t csr_rows_smem(int64_t win_len, int64_t ylen, int elem);
 int csr_pack_cap(int elem);
 int csr_warp_long();
+int csr_group_threads();  // block size of the lane-group kernel
 int csr_long_buckets();  // length buckets of the long-row queue
 
 CsrPlan plan_csr(const DeviceInfo& dev, int64_t m, int64_t n, int64_t nnz, int elem);
