@@ -117,17 +117,41 @@ def model_estimate(p):
     return {"plan": desc, "est_us": float(f.get("est_us", "nan"))}
 
 
-def measured_peaks():
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+def _num(v):
+    """A positive number from a peak entry: a number, or a record holding one."""
+    if isinstance(v, dict):
+        for k in ("value", "burst", "gbs", "GBs", "measured"):
+            if k in v:
+                return _num(v[k])
+        return None
+    try:
+        f = float(v)
+    except (TypeError, ValueError):
+        return None
+    return f if f > 0 and f == f and f != float("inf") else None
+
+
+def measured_peaks(path=None):
+    """(HBM GB/s, "measured" | "fallback", the file's records) from the measured-peaks file."""
+    path = path or os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         try:
             d = json.load(open(path))
-            for k in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs"):
-                if k in d:
-                    return float(d[k]), "measured", d
         except Exception:
-            pass
+            d = None
+        if isinstance(d, dict):
+            keys = ["hbm_gbs", "hbm_GBs", "hbm_copy_gbs"]
+            keys += sorted(k for k in d if "hbm" in k.lower() and k not in keys)
+            for k in keys:
+                f = _num(d.get(k))
+                if f is not None:
+                    return f, "measured", d
     return FALLBACK_HBM_GBS, "fallback", {}
+
+
+def fp64_peak_tflops(peaks):
+    f = _num(peaks.get("fp64_tflops"))
+    return FP64_PEAK_TFLOPS if f is None else f
 
 
 class ClockSampler:
@@ -531,7 +555,7 @@ def run_fused(args, name, desc, p, rank, world, dist):
     if is_multi(p):
         # k right-hand sides: two FMAs (4 flops) per stored element per right-hand side, on the fp32 or fp64 pipe
         flops = 4.0 * p.m * p.n * p.y.shape[1]
-        alu_peak = FP32_PEAK_TFLOPS if dtype_name(p) == "f32" else float(peaks.get("fp64_tflops", FP64_PEAK_TFLOPS))
+        alu_peak = FP32_PEAK_TFLOPS if dtype_name(p) == "f32" else fp64_peak_tflops(peaks)
         rec["roofline_alu"] = {"bound": "alu", "achieved": round(flops / (kernel_ms * 1e-3) / 1e12, 4),
                                "peak": alu_peak, "unit": "TFLOP/s",
                                "frac": round(flops / (kernel_ms * 1e-3) / 1e12 / alu_peak, 4),
@@ -545,7 +569,7 @@ def run_fused(args, name, desc, p, rank, world, dist):
         # fp64 runs on GB300's fp64 units: 2 DFMA per clock per SM (measured 1.254 TFLOP/s), and the
         # pattern needs two FMAs (4 flops) per stored element, so the fp64 rate can bind before HBM
         flops = 4.0 * (p.m * p.n if p.kind == "dense" else p.nnz)
-        fp64_peak = float(peaks.get("fp64_tflops", FP64_PEAK_TFLOPS))
+        fp64_peak = fp64_peak_tflops(peaks)
         rec["roofline_alu"] = {"bound": "alu", "achieved": round(flops / (kernel_ms * 1e-3) / 1e12, 4),
                                "peak": fp64_peak, "unit": "TFLOP/s",
                                "frac": round(flops / (kernel_ms * 1e-3) / 1e12 / fp64_peak, 4),

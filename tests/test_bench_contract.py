@@ -58,3 +58,25 @@ def test_model_estimate_is_reported():
     assert "kind=tile_tma" in m["plan"] and m["est_us"] > 4.0
     m = bench.model_estimate(inputgen.dense_multi(m=1000, k=8))
     assert m["plan"].startswith("multi ok=1") and m["est_us"] > 0
+
+
+@pytest.mark.parametrize("content,expect", [
+    ('{"hbm_gbs": 7012.5}', (7012.5, "measured")),
+    ('{"hbm_gbs": {"value": 7012.5, "unit": "GB/s"}}', (7012.5, "measured")),
+    ('{"hbm_copy_gbs": "6950"}', (6950.0, "measured")),
+    ('{"hbm_stream_copy_GBps": 7100}', (7100.0, "measured")),
+    ('{"bf16_tflops": 1900}', (bench.FALLBACK_HBM_GBS, "fallback")),
+    ('{"hbm_gbs": null}', (bench.FALLBACK_HBM_GBS, "fallback")),
+    ('not json', (bench.FALLBACK_HBM_GBS, "fallback")),
+])
+def test_measured_peaks_file(tmp_path, content, expect):
+    f = tmp_path / "peaks.json"
+    f.write_text(content)
+    peak, kind, _ = bench.measured_peaks(str(f))
+    assert (peak, kind) == expect
+
+
+def test_fp64_peak_from_file():
+    assert bench.fp64_peak_tflops({}) == bench.FP64_PEAK_TFLOPS
+    assert bench.fp64_peak_tflops({"fp64_tflops": {"value": 1.3}}) == 1.3
+    assert bench.fp64_peak_tflops({"fp64_tflops": "n/a"}) == bench.FP64_PEAK_TFLOPS
