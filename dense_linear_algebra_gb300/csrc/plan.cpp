@@ -61,9 +61,9 @@ double csr_est_us(const DeviceInfo& dev, const CsrPlan& p, int64_t m, int64_t n,
   const double bytes = (double)nnz * (elem + 4) + (double)(m + 1) * 8 + (double)m * elem + 3.0 * n * elem;
   const double nn = (double)std::max<int64_t>(n, 1);
   const double miss = (1.0 - std::min(1.0, p.ylen / nn)) + (1.0 - std::min(1.0, p.win_len / nn));
-  // fp64 lane groups reach 44 % of the fp64 FMA rate (padding slots, reductions, the CAS
+  // fp64 lane groups reach 45 % of the fp64 FMA rate (padding slots, reductions, the CAS
   // loop); fp32 packed rows are bound by memory and L2, not FMAs
-  return roofline_us(dev, bytes, 0.8, 2.0 * nnz, elem, elem == 8 ? 0.44 : 0.6, miss * nnz, 0.6);
+  return roofline_us(dev, bytes, 0.8, 2.0 * nnz, elem, elem == 8 ? 0.45 : 0.6, miss * nnz, 0.6);
 }
 
 }  // namespace
