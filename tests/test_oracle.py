@@ -26,8 +26,6 @@ from __future__ import annotations
 
 import json
 import os
-import subprocess
-import tempfile
 from fractions import Fraction
 
 import numpy as np
