@@ -12,15 +12,21 @@
 // process exits. The caller still passes every input and output.
 //
 // Set-up: the first call on a device, with that device current, looks up the
-// array's device address (cudaGetSymbolAddress) and caches it for that device.
-// That first call should therefore come before any stream capture. Later calls
-// make no allocation, look-up or synchronisation.
+// array's device address (cudaGetSymbolAddress) and caches it for that device,
+// together with the unique id of the device's current context. That first call
+// should therefore come before any stream capture. Later calls compare the
+// context id (one driver query, no allocation or synchronisation) and look the
+// address up again only when the context has changed: after cudaDeviceReset, or
+// a release and re-creation of the primary context, the library's device code is
+// loaded anew and the array has a new address.
 //
 // Sharing: every call on a device uses the same array and finds it as the last
 // call left it. The arrival ticket, which must start at zero, is cleared on the
 // caller's stream before each launch. Calls whose executions overlap on the GPU
 // (different streams, no ordering between them) race on the array and give
 // wrong results; order them on one stream or with events.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "fxtx.h"
@@ -38,14 +44,43 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 struct NoallocDevice {
   std::once_flag once;
-  cudaError_t err = cudaSuccess;
+  std::mutex mu;                   // guards scratch and ctx_id
   unsigned char* scratch = nullptr;
+  unsigned long long ctx_id = 0;   // unique id of the context the address belongs to
   DeviceInfo info;
 };
 NoallocDevice g_devs[kMaxDevices];
 
-// Device properties and the scratch address for the current device, looked up once.
-fxtx_status_t setup(NoallocDevice** out) {
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// The unique id of the calling thread's current context (0 if it cannot be had).
+unsigned long long current_ctx_id() {
+  static std::once_flag once;
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+    cudaGetLastError();
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device properties and the scratch address for the current device and context.
+fxtx_status_t setup(NoallocDevice** out, unsigned char** scratch) {
   int d = -1;
   if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) {
     cudaGetLastError();
@@ -61,16 +96,25 @@ fxtx_status_t setup(NoallocDevice** out) {
     cudaDeviceGetAttribute(&di.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d);
     cudaDeviceGetAttribute(&di.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, d);
     cudaGetLastError();
-    if (di.cc_major == 10 && di.cc_minor == 3) {
-      void* p = nullptr;
-      nd.err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-      if (nd.err == cudaSuccess) nd.scratch = static_cast<unsigned char*>(p);
-      cudaGetLastError();
-    }
   });
   if (nd.info.cc_major != 10 || nd.info.cc_minor != 3 || nd.info.sm_count <= 0) return FXTX_ERR_UNSUPPORTED;
-  if (nd.err != cudaSuccess || nd.scratch == nullptr) return FXTX_ERR_CUDA;
+  // the first cudaGetSymbolAddress on a device also makes its primary context current,
+  // so the context id is read after it
+  std::lock_guard<std::mutex> lock(nd.mu);
+  const unsigned long long id = nd.scratch ? current_ctx_id() : 0;
+  if (nd.scratch == nullptr || id == 0 || id != nd.ctx_id) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      nd.scratch = nullptr;
+      return FXTX_ERR_CUDA;
+    }
+    nd.scratch = static_cast<unsigned char*>(p);
+    nd.ctx_id = current_ctx_id();
+  }
   *out = &nd;
+  *scratch = nd.scratch;
   return FXTX_OK;
 }
 
@@ -87,7 +131,8 @@ extern "C" fxtx_status_t fxtx_dense_f32_noalloc(int64_t m, int64_t n, const floa
   if (ld < n || y == nullptr || out == nullptr) return FXTX_ERR_INVALID_ARG;
   if (m > 0 && X == nullptr) return FXTX_ERR_INVALID_ARG;
   NoallocDevice* nd = nullptr;
-  fxtx_status_t s = setup(&nd);
+  unsigned char* scratch = nullptr;
+  fxtx_status_t s = setup(&nd, &scratch);
   if (s != FXTX_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
@@ -109,8 +154,8 @@ extern "C" fxtx_status_t fxtx_dense_f32_noalloc(int64_t m, int64_t n, const floa
   a.alpha = (double)alpha; a.beta = (double)beta;
   a.use_z = (z != nullptr && beta != 0.0f);
   a.tiles = plan.rows_per_tile > 0 ? (m + plan.rows_per_tile - 1) / plan.rows_per_tile : 0;
-  a.ws = reinterpret_cast<double*>(nd->scratch);
-  a.ticket = reinterpret_cast<unsigned*>(nd->scratch + kTicketOffset);
+  a.ws = reinterpret_cast<double*>(scratch);
+  a.ticket = reinterpret_cast<unsigned*>(scratch + kTicketOffset);
   if (partials) {
     if (cudaMemsetAsync(a.ticket, 0, sizeof(unsigned), st) != cudaSuccess) {
       cudaGetLastError();

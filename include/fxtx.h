@@ -135,8 +135,10 @@ fxtx_status_t fxtx_dense_multi_f64(int64_t m, int64_t n, int64_t k, const double
  * Scratch: one library-wide device array of FXTX_NOALLOC_SCRATCH_BYTES (1 MiB),
  * which every GPU that loads the library holds until the process exits. The
  * first call on a device (with that device current) looks up the array's address
- * and caches it; make that first call before any stream capture. No call
- * allocates or frees memory.
+ * and caches it; make that first call before any stream capture. A later call
+ * that finds a different context current on the device (after cudaDeviceReset,
+ * which reloads the library's device code at a new address) looks it up again.
+ * No call allocates or frees memory.
  *
  * Limits: rows of at most 512 fp32 columns (the narrow kernel); n > 512 returns
  * FXTX_ERR_TOO_LARGE. The grid is capped so that the per-CTA partials fit the

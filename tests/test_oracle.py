@@ -312,6 +312,14 @@ def pin_special_cases(lib):
         oracle.csr(np.array([0, 2, 1], np.int64), np.zeros(1, np.int32), np.zeros(1), y, None, 1.0, 0.0, None, n, lib=lib)
     with pytest.raises(ValueError):
         oracle.csr(np.array([0, 1], np.int64), np.array([n], np.int32), np.zeros(1), y, None, 1.0, 0.0, None, n, lib=lib)
+    # row_ptr must start at 0 and end at nnz, even when it is non-decreasing and every column is in range
+    with pytest.raises(ValueError):
+        oracle.csr(np.array([1, 2], np.int64), np.zeros(2, np.int32), np.ones(2), y, None, 1.0, 0.0, None, n, lib=lib)
+    with pytest.raises(ValueError):
+        oracle.csr(np.array([0, 1, 1], np.int64), np.zeros(2, np.int32), np.ones(2), y, None, 1.0, 0.0, None, n,
+                   lib=lib)
+    assert not oracle.csr_is_valid(np.array([0, 1, 1], np.int64), np.zeros(2, np.int32), n, lib=lib)
+    assert oracle.csr_is_valid(np.array([0, 1, 2], np.int64), np.zeros(2, np.int32), n, lib=lib)
 
 
 PINS = [pin_worked_example, pin_gram_identity, pin_quadratic_form, pin_linearity_and_permutations,
@@ -464,6 +472,9 @@ MUTANTS = [
     ("z read when beta is zero", "int use_z = (z != NULL && beta != 0.0);", "int use_z = (z != NULL);"),
     ("dot drops the last column", "for (int64_t j = 0; j < n; ++j) u +=", "for (int64_t j = 0; j + 1 < n; ++j) u +="),
     ("S omits beta z", "sj += fabs(beta * atd(z, dtype, j));", "sj += 0;"),
+    ("CSR row_ptr ends unchecked", "if (row_ptr[0] != 0 || row_ptr[m] != nnz) return ORACLE_BAD_CSR;", ""),
+    ("CSR row_ptr end checked only", "if (row_ptr[0] != 0 || row_ptr[m] != nnz) return ORACLE_BAD_CSR;",
+     "if (row_ptr[m] != nnz) return ORACLE_BAD_CSR;"),
 ]
 
 
@@ -482,6 +493,6 @@ def test_planted_mistakes(mutant, tmp_path):
     for pin in PINS:
         try:
             pin(lib)
-        except (AssertionError, ValueError) as e:
+        except (AssertionError, ValueError, pytest.fail.Exception):  # pytest.raises that saw no error fails so
             failures.append(pin.__name__)
     assert failures, f"mutant '{desc}' passed every pin"

@@ -19,6 +19,8 @@ from _util import assert_within_bound
 
 pytestmark = pytest.mark.gpu
 
+SCRATCH = 1 << 20  # FXTX_NOALLOC_SCRATCH_BYTES
+
 
 def _noalloc(dp, out):
     p = dp.p
@@ -29,18 +31,38 @@ def _noalloc(dp, out):
                                      ptr(dp.z), out.data_ptr(), stream)
 
 
-@pytest.mark.parametrize("m,n,variant", [(1_000_000, 32, "b"), (200_000, 32, "c"), (50_000, 100, "a")])
-def test_noalloc_matches_allocating_entry_point(m, n, variant):
-    p = inputgen.dense_tall(m=m, n=n, variant=variant)
+def _check_two_calls(p):
+    """Two calls in a row (sharing the scratch array) against the oracle, and against the allocating entry."""
     dp = DeviceProblem(p)
-    ref = dp.run().cpu().numpy().astype(np.float64)  # the allocating entry point
-    _, S = oracle.solve(p, acc="d")
-    for call in range(2):  # two calls in a row share the same scratch array
+    ref, S = oracle.solve(p, acc="d")
+    alloc = dp.run().cpu().numpy().astype(np.float64)
+    for call in range(2):
         out = torch.full((p.n,), float("nan"), dtype=torch.float32, device="cuda")
         assert _noalloc(dp, out) == fx.FXTX_OK
         torch.cuda.synchronize()
         got = out.cpu().numpy().astype(np.float64)
-        assert_within_bound(got, ref, S, 2e-5, f"noalloc call {call}")
+        assert_within_bound(got, ref, S, 2e-5, f"noalloc call {call} against the oracle")
+        assert_within_bound(got, alloc, S, 4e-5, f"noalloc call {call} against fxtx_dense_f32")
+    assert fx.device_error() == fx.FXTX_OK
+
+
+@pytest.mark.parametrize("m,n,variant", [(1_000_000, 32, "b"), (200_000, 32, "c"), (50_000, 100, "a")])
+def test_noalloc_matches_oracle(m, n, variant):
+    _check_two_calls(inputgen.dense_tall(m=m, n=n, variant=variant))
+
+
+def test_noalloc_capped_grid_matches_oracle():
+    """Rows of 500 columns with pitch 501 take the direct-load narrow kernel, whose planned grid holds
+    more CTA partials than the scratch array: the entry point caps the grid to fit."""
+    m, n, ld = 200_000, 500, 501
+    X = inputgen.normal(0, 1, (m, ld), np.float32)
+    p = inputgen.Problem("dense_f32_%dx%d_ld%d" % (m, n, ld), "dense", np.float32, m, n, 2.0, -1.0,
+                         X=X, ld=ld, y=inputgen.normal(0, 2, n, np.float32),
+                         v=inputgen.uniform(0, 3, m, 0.1, 2.0, np.float32), z=inputgen.normal(0, 4, n, np.float32))
+    plan = dict(kv.split("=") for kv in fx.plan_describe("dense", "f32", m, n, 0, ld).split()[1:] if "=" in kv)
+    assert plan["kind"] == "narrow_direct"
+    assert int(plan["ctas"]) * n * 8 > SCRATCH - 256, "the planned grid must exceed the scratch, so the cap fires"
+    _check_two_calls(p)
 
 
 def test_noalloc_rejects_rows_beyond_its_scratch():
