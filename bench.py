@@ -13,9 +13,17 @@ kernel to the measured HBM copy bandwidth; ``cpu_baseline`` is the C oracle time
 this host's cores; ``unfused_library`` is the three-call cuBLAS sequence
 (gemv, scale, transposed gemv) on the same GPU.
 
+The default run also measures every other configuration of the workload list (dense f64
+1000 x 64; the three variants of the tall fp32 X; dense f64 20,000 x 20,000; CSR f64
+uniform; CSR f32 power-law) in the same process and nests their figures in the same
+line under ``configs``: back-to-back microseconds per call, isolated calls after an L2
+flush (p10/p50/p90; hot-L2 too for the small case), GB/s against the measured HBM copy
+bandwidth, the fp64 ALU roof where it binds, e2e, the unfused library sequence and the
+oracle on a bounded sample. --headline-only skips them.
+
 --impl reference times the oracle (the CPU reference of this pattern) instead, on a
 bounded sample of the same workload, and prints the same line with "impl": "reference".
---workload picks another configuration; --all prints one line per configuration.
+--workload picks one other configuration; --all prints one line per configuration.
 """
 from __future__ import annotations
 
@@ -439,6 +447,42 @@ def time_unfused(args, p, d, X, out, dev, stream, ideal, ms_step):
     return unfused
 
 
+L2_FLUSH_BYTES = 256 << 20  # larger than GB300's 129 MB L2
+
+
+GATE_CYCLES = 2_000_000  # a ~1 ms spin on the device that holds the stream while a call is enqueued
+
+
+def time_isolated(call, stream, reps: int, flush=None):
+    """Per-call device times (us) of `reps` isolated calls, one CUDA-event pair each. With
+    `flush`, a write of L2_FLUSH_BYTES before every call evicts L2 (cold-cache calls).
+
+    Each call is enqueued behind a device-side spin, so the first event and the call are both
+    queued before the device reaches them: the pair then times the call alone, not the host's
+    enqueue latency (which an idle device would otherwise wait out between the two events)."""
+    import torch
+
+    ts = []
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    for _ in range(reps):
+        torch.cuda._sleep(GATE_CYCLES)
+        if flush is not None:
+            flush.fill_(1)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e3)
+    return ts
+
+
+def percentiles(ts):
+    q = np.percentile(np.asarray(ts, dtype=np.float64), [10, 50, 90])
+    return {"p10": round(float(q[0]), 2), "p50": round(float(q[1]), 2), "p90": round(float(q[2]), 2),
+            "calls": len(ts)}
+
+
 def run_fused(args, name, desc, p, rank, world, dist):
     import torch
 
@@ -509,6 +553,12 @@ def run_fused(args, name, desc, p, rank, world, dist):
                 call()
             extra += 20
             torch.cuda.synchronize()
+    # the same call in isolation, one event pair per call: after an L2 flush (cold cache, as ncu's
+    # serialised launch list sees it), and for inputs that fit in L2 also hot
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    iso_cold = time_isolated(call, stream, max(args.steps, 5), flush)
+    del flush
+    iso_hot = time_isolated(call, stream, max(args.steps, 5)) if p.ideal_bytes() <= 64e6 else None
     if dist:
         dist.barrier()
     # one event pair around the K back-to-back calls: events between calls would stop
@@ -539,6 +589,8 @@ def run_fused(args, name, desc, p, rank, world, dist):
                          "inputs fit in L2: hot-L2 figure",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "us_per_call": round(kernel_ms * 1e3, 2),
+        "isolated_call_us": dict({"l2_flushed": percentiles(iso_cold)},
+                                 **({"hot_l2": percentiles(iso_hot)} if iso_hot is not None else {})),
         "hbm_pct_of_peak": round(100 * value / world / peak, 2),
         "hbm_pct_of_nominal_7900": round(100 * value / world / 7900.0, 2),
         "clocks": dict(clk.summary(), window=f"{args.steps} timed steps + {extra} identical steps (>= 1 s)"),
@@ -581,6 +633,71 @@ def run_fused(args, name, desc, p, rank, world, dist):
     if p.kind == "csr":
         rec["config"]["nnz"] = p.nnz
     return rec
+
+
+def run_split(args, name, desc, p, rank, world, dist):
+    """--split rows: one problem split by rows across the ranks (strong scaling). Each rank
+    holds its row block; a step is its partial (one fused call at alpha = 1, beta = 0), one
+    all-reduce of the n-vector and the epilogue kernel, on every rank."""
+    import torch
+
+    from dense_linear_algebra_gb300 import distributed as sp
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream(dev)
+
+    def to(a):
+        return None if a is None else torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    if p.kind == "dense":
+        b = sp.row_bounds(p.m, world)
+        shard = sp.shard_dense(to(p.X[b[rank]:b[rank + 1], : p.n]), to(p.v[b[rank]:b[rank + 1]])
+                               if p.v is not None else None, [0, b[rank + 1] - b[rank]], 0)
+    else:
+        b = sp.row_bounds(p.m, world, p.row_ptr)
+        hs = sp.shard_csr(p.row_ptr, p.col_idx, p.vals, p.v, p.n, b, rank)
+        shard = sp.RowShard("csr", p.n, hs.r0, hs.r1, v=to(hs.v), row_ptr=to(hs.row_ptr), col_idx=to(hs.col_idx),
+                            vals=to(hs.vals))
+    y, z = to(p.y), to(p.z)
+
+    def step():
+        return sp.sharded_call(shard, y, p.alpha, p.beta, z)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ms_rank = e0.elapsed_time(e1) / args.steps
+    ms_step = ms_rank
+    if dist is not None and world > 1:
+        tt = torch.tensor([ms_step], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_step = float(tt.item())
+    ideal = p.ideal_bytes()
+    peak, peak_kind, _ = measured_peaks()
+    value = ideal / (ms_step * 1e-3) / 1e9
+    per_call = 1 if p.kind == "dense" else 3
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+        "scaling": "strong", "vs_baseline": None, "dtype": dtype_name(p), "data": "synthetic",
+        "config": {"workload": desc, "name": name, "algorithmic_bytes_per_step": ideal,
+                   "parallelism": f"rows split over {world} rank(s): fused partial, all-reduce of n values, epilogue",
+                   "rows_this_rank": shard.rows},
+        "hbm_pct_of_peak_per_gpu": round(100 * value / world / peak, 2), "peak_source": f"{peak_kind} HBM copy",
+        "gpu_launches": (per_call + 1) * args.steps,
+    }
 
 
 def run_solver(args):
@@ -657,24 +774,80 @@ def run_solver(args):
     print(json.dumps(rec), flush=True)
 
 
+# BASELINE's configurations in order: (label, workload, HBM-fraction target or None)
+BASELINE_CONFIGS = [("1", "dense_small", None), ("2a", "dense_tall_a", 0.75), ("2b", "dense_tall_b", 0.75),
+                    ("2c", "dense_tall_c", 0.75), ("3", "dense_wide", 0.75), ("4", "csr_uniform", 0.5),
+                    ("5", "csr_powerlaw", 0.5)]
+HEADLINE = "dense_tall_b"
+CPU_SAMPLE_BYTES = 256e6  # algorithmic bytes of the oracle's sample for a configuration's cpu_baseline
+
+
+def cpu_baseline_sample(p, budget_s: float = 3.0):
+    """The oracle (double accumulator, one thread) on the first rows of p, about CPU_SAMPLE_BYTES of them."""
+    rows = max(1, min(p.m, int(p.m * CPU_SAMPLE_BYTES / max(p.ideal_bytes(), 1))))
+    sp = sample_problem(p, rows)
+    t, reps = cpu_oracle_time(sp, budget_s=budget_s, min_reps=1, max_reps=3)
+    return {"value": round(sp.ideal_bytes() / t / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {rows} of {p.m} rows ({sp.ideal_bytes()} algorithmic bytes), double accumulator, "
+                      f"single thread, median of {reps} runs of {t:.3f} s",
+            "host_cores": os.cpu_count()}
+
+
+def config_summary(label, target, rec):
+    """The figures of one configuration's measurement, for the headline line's `configs` object."""
+    peak = rec["roofline"]["peak"]
+    frac = rec["roofline"]["achieved"] / peak
+    d = {"workload": rec["config"]["workload"], "name": rec["config"]["name"], "dtype": rec["dtype"],
+         "us_per_call": rec["us_per_call"], "isolated_call_us": rec["isolated_call_us"],
+         "value": rec["roofline"]["achieved"], "unit": "GB/s", "hbm_frac_of_measured": round(frac, 4),
+         "hbm_pct_of_nominal_7900": round(100 * rec["roofline"]["achieved"] / 7900.0, 2),
+         "algorithmic_bytes_per_call": rec["config"]["algorithmic_bytes_per_step"],
+         "roofline": rec["roofline"], "e2e": rec["e2e"], "clocks": rec["clocks"], "model": rec["model"]}
+    if "roofline_alu" in rec:
+        d["roofline_alu"] = rec["roofline_alu"]
+    if "nnz" in rec["config"]:
+        d["nnz"] = rec["config"]["nnz"]
+    u = rec.get("unfused_library") or {}
+    if "ms_per_step" in u:
+        d["unfused_library"] = {"what": u["what"], "us_per_call": round(u["ms_per_step"] * 1e3, 2),
+                                "fused_speedup": u["fused_speedup"]}
+    elif u:
+        d["unfused_library"] = u
+    if "cpu_baseline" in rec:
+        d["cpu_baseline"] = rec["cpu_baseline"]
+    if target is None:
+        d["target"] = "parity; launch-bound and L2-resident, so microseconds per call (hot and L2-flushed)"
+    else:
+        d["target"] = f">= {int(target * 100)} % of HBM peak"
+        d["meets_target"] = bool(frac >= target)
+    return d
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="fused", choices=["fused", "reference"])
-    ap.add_argument("--workload", default="dense_tall_b", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=None, choices=sorted(WORKLOADS),
+                    help="one workload only (default: the headline, with every BASELINE configuration nested)")
+    ap.add_argument("--headline-only", action="store_true", help="skip the nested configurations")
     ap.add_argument("--all", action="store_true", help="one line per workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rows", type=int, default=0, help="override the row count (same recipe), for profiling")
     ap.add_argument("--no-extras", action="store_true", help="skip the e2e and unfused-library legs")
     ap.add_argument("--solver", action="store_true", help="time ridge-regression CG on the tall X instead")
+    ap.add_argument("--split", default=None, choices=["rows"],
+                    help="rows: split one problem by rows across the ranks (all-reduce of n values) "
+                         "instead of running independent replicas")
     args = ap.parse_args()
 
     import inputgen
 
     rank, world, local = dist_env()
-    names = sorted(WORKLOADS) if args.all else [args.workload]
+    names = sorted(WORKLOADS) if args.all else [args.workload or HEADLINE]
+    # the default run nests every BASELINE configuration in the headline's line
+    nest = not args.all and args.workload is None and not args.headline_only and args.impl == "fused"
     if args.solver:
         if rank == 0:
             run_solver(args)
@@ -700,6 +873,20 @@ def main():
     else:
         torch.cuda.set_device(0)
 
+    if args.split == "rows":
+        for name in names:
+            desc, mk = WORKLOADS[name]
+            p = mk(inputgen, args.rows or None)
+            if is_multi(p) or p.x_store == "bf16":
+                raise SystemExit("--split rows takes the single-vector fp32/fp64 workloads")
+            rec = run_split(args, name, desc, p, rank, world, dist)
+            if rank == 0:
+                print(json.dumps(rec), flush=True)
+        if dist:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
     for name in names:
         desc, mk = WORKLOADS[name]
         p = mk(inputgen, args.rows or None)
@@ -713,9 +900,26 @@ def main():
                                    "sample": f"the whole workload ({p.ideal_bytes()} algorithmic bytes), double "
                                              f"accumulator, single thread, median of {reps} runs of {t:.2f} s",
                                    "host_cores": os.cpu_count()}
+        del p
+        if nest:
+            rec["configs"] = {}
+            for label, wl, target in BASELINE_CONFIGS:
+                if wl == name:
+                    rec["configs"][label] = config_summary(label, target, rec)
+                    continue
+                wdesc, wmk = WORKLOADS[wl]
+                q = wmk(inputgen, None)
+                r = run_fused(args, wl, wdesc, q, rank, world, dist)
+                if rank == 0 and world == 1 and not args.no_cpu_baseline:
+                    r["cpu_baseline"] = cpu_baseline_sample(q)
+                rec["configs"][label] = config_summary(label, target, r)
+                del q, r
+                torch.cuda.empty_cache()
+            rec["config"]["configs_note"] = ("headline: BASELINE configuration 2 (dense f32 16,000,000 x 32, "
+                                             "alpha=2, beta=-1); every configuration, the headline included, "
+                                             "under `configs`, each measured in this run")
         if rank == 0:
             print(json.dumps(rec), flush=True)
-        del p
     if dist:
         dist.barrier()
         dist.destroy_process_group()

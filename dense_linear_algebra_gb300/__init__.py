@@ -9,9 +9,11 @@ fallback: if the library cannot be loaded, importing the binding fails.
 Raw C-ABI calls (pointers as ints, stream as a cudaStream_t int) carry the C names:
 ``fxtx_dense_f32``, ``fxtx_dense_f64``, ``fxtx_dense_bf16``, ``fxtx_dense_f32_noalloc``,
 ``fxtx_dense_multi_f32``, ``fxtx_dense_multi_f64``, ``fxtx_csr_f32``, ``fxtx_csr_f64``,
-``fxtx_csr_validate``, ``fxtx_device_error``, ``fxtx_status_string``,
+``fxtx_csr_validate``, ``fxtx_epilogue_f32``, ``fxtx_epilogue_f64``, ``fxtx_device_error``,
+``fxtx_status_string``,
 ``fxtx_plan_describe``, ``fxtx_multi_plan_describe`` and the ``fxtx_autotune_*`` calls. ``dense``, ``dense_multi`` and
-``csr`` take torch CUDA tensors.
+``csr`` take torch CUDA tensors; ``epilogue`` applies alpha * w + beta * z. The module
+``distributed`` runs one call across ranks, each holding a block of X's rows.
 """
 from ._lib import (  # noqa: F401
     FXTX_ERR_ALLOC,
@@ -35,6 +37,7 @@ from ._lib import (  # noqa: F401
     dense,
     dense_multi,
     device_error,
+    epilogue,
     fxtx_autotune_candidates,
     fxtx_autotune_clear,
     fxtx_autotune_entries,
@@ -52,6 +55,8 @@ from ._lib import (  # noqa: F401
     fxtx_dense_multi_f32,
     fxtx_dense_multi_f64,
     fxtx_device_error,
+    fxtx_epilogue_f32,
+    fxtx_epilogue_f64,
     fxtx_multi_plan_describe,
     fxtx_plan_describe,
     fxtx_status_string,

@@ -35,6 +35,8 @@ def _load() -> ctypes.CDLL:
     lib.fxtx_csr_f32.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, f32, f32, vp, vp, vp]
     lib.fxtx_csr_f64.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, f64, f64, vp, vp, vp]
     lib.fxtx_csr_validate.argtypes = [i64, i64, i64, vp, vp, vp]
+    lib.fxtx_epilogue_f32.argtypes = [i64, vp, f32, f32, vp, vp, vp]
+    lib.fxtx_epilogue_f64.argtypes = [i64, vp, f64, f64, vp, vp, vp]
     lib.fxtx_device_error.argtypes = [vp]
     lib.fxtx_status_string.argtypes = [i32]
     lib.fxtx_status_string.restype = ctypes.c_char_p
@@ -50,6 +52,7 @@ def _load() -> ctypes.CDLL:
     lib.fxtx_autotune_candidates.argtypes = [i32, i32, i64, i64, i64, i64, ctypes.c_char_p, i64]
     for name in ("fxtx_dense_f32", "fxtx_dense_f64", "fxtx_dense_f32_noalloc", "fxtx_dense_bf16", "fxtx_dense_multi_f32",
                  "fxtx_dense_multi_f64", "fxtx_csr_f32", "fxtx_csr_f64", "fxtx_csr_validate", "fxtx_device_error",
+                 "fxtx_epilogue_f32", "fxtx_epilogue_f64",
                  "fxtx_plan_describe", "fxtx_multi_plan_describe", "fxtx_autotune_set", "fxtx_autotune_get",
                  "fxtx_autotune_clear", "fxtx_autotune_save", "fxtx_autotune_load", "fxtx_autotune_candidates"):
         getattr(lib, name).restype = i32
@@ -68,6 +71,8 @@ fxtx_dense_multi_f64 = _lib.fxtx_dense_multi_f64
 fxtx_csr_f32 = _lib.fxtx_csr_f32
 fxtx_csr_f64 = _lib.fxtx_csr_f64
 fxtx_csr_validate = _lib.fxtx_csr_validate
+fxtx_epilogue_f32 = _lib.fxtx_epilogue_f32
+fxtx_epilogue_f64 = _lib.fxtx_epilogue_f64
 fxtx_device_error = _lib.fxtx_device_error
 fxtx_plan_describe = _lib.fxtx_plan_describe
 fxtx_multi_plan_describe = _lib.fxtx_multi_plan_describe
@@ -295,6 +300,31 @@ def csr(row_ptr, col_idx, vals, y, n: int, v=None, alpha: float = 1.0, beta: flo
         rc = fn(m, n, nnz, _ptr(row_ptr), _ptr(col_idx), _ptr(vals), _ptr(y), _ptr(v), alpha, beta, _ptr(z), _ptr(out),
                 _stream(stream, dev))
     _check(rc, "fxtx_csr")
+    return out
+
+
+def epilogue(w, alpha: float = 1.0, beta: float = 0.0, z=None, out=None, stream=None):
+    """out = alpha * w + beta * z on the GPU (the last step of a row-sharded call, after the
+    partials w_g = X_g^T (v_g * (X_g y)) of the row blocks are summed). ``z=None`` or beta = 0
+    drops the beta z term; ``out`` may be ``w`` or ``z``."""
+    torch = _torch()
+    if w.dim() != 1 or not w.is_cuda:
+        raise ValueError("w: expected a 1-D CUDA tensor")
+    n, dt, di = w.shape[0], w.dtype, w.get_device()
+    _vec(w, dt, n, "w", di)
+    z = _vec(z, dt, n, "z", di)
+    if out is None:
+        out = torch.empty(n, dtype=dt, device=w.device)
+    _vec(out, dt, n, "out", di)
+    if dt == torch.float32:
+        fn = fxtx_epilogue_f32
+    elif dt == torch.float64:
+        fn = fxtx_epilogue_f64
+    else:
+        raise TypeError(f"unsupported dtype {dt}")
+    with _on(di):
+        rc = fn(n, _ptr(w), alpha, beta, _ptr(z), _ptr(out), _stream(stream, w.device))
+    _check(rc, "fxtx_epilogue")
     return out
 
 

@@ -340,6 +340,23 @@ fxtx_status_t dense_multi_impl(int64_t m, int64_t n, int64_t k, const T* X, int6
   return FXTX_OK;
 }
 
+template <typename T>
+fxtx_status_t epilogue_impl(int64_t n, const T* w, T alpha, T beta, const T* z, T* out, void* stream) {
+  if (n < 0) return FXTX_ERR_INVALID_ARG;
+  if (n == 0) return FXTX_OK;
+  if (w == nullptr || out == nullptr) return FXTX_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  fxtx_status_t s = current_device(&dev);
+  if (s != FXTX_OK) return s;
+  const bool use_z = z != nullptr && beta != T(0);
+  if (launch_epilogue<T>(n, w, (double)alpha, (double)beta, z, use_z, out, dev->sm_count,
+                         static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return FXTX_ERR_CUDA;
+  }
+  return FXTX_OK;
+}
+
 }  // namespace
 }  // namespace fxtx
 
@@ -385,6 +402,16 @@ fxtx_status_t fxtx_csr_f64(int64_t m, int64_t n, int64_t nnz, const int64_t* row
                            const double* vals, const double* y, const double* v, double alpha, double beta,
                            const double* z, double* out, void* stream) {
   return csr_impl<double>(m, n, nnz, row_ptr, col_idx, vals, y, v, alpha, beta, z, out, stream);
+}
+
+fxtx_status_t fxtx_epilogue_f32(int64_t n, const float* w, float alpha, float beta, const float* z, float* out,
+                                void* stream) {
+  return epilogue_impl<float>(n, w, alpha, beta, z, out, stream);
+}
+
+fxtx_status_t fxtx_epilogue_f64(int64_t n, const double* w, double alpha, double beta, const double* z, double* out,
+                                void* stream) {
+  return epilogue_impl<double>(n, w, alpha, beta, z, out, stream);
 }
 
 fxtx_status_t fxtx_csr_validate(int64_t m, int64_t n, int64_t nnz, const int64_t* row_ptr, const int32_t* col_idx,

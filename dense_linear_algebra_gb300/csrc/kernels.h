@@ -59,6 +59,12 @@ cudaError_t launch_csr(const CsrPlan& p, const CsrArgs<T>& a, cudaStream_t st);
 cudaError_t launch_csr_validate(int64_t m, int64_t n, int64_t nnz, const int64_t* row_ptr,
                                 const int32_t* col_idx, int* flag, cudaStream_t st);
 
+// out = alpha * w + beta * z (z read only when use_z): the epilogue of a row-sharded call,
+// applied once after the devices' partials are summed.
+template <typename T>
+cudaError_t launch_epilogue(int64_t n, const T* w, double alpha, double beta, const T* z, bool use_z, T* out,
+                            int sm_count, cudaStream_t st);
+
 // Read and clear the device-side error word of each kernel file (synchronous;
 // -1 if the read itself failed).
 int take_dense_device_error();

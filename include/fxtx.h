@@ -174,6 +174,30 @@ fxtx_status_t fxtx_csr_f64(int64_t m, int64_t n, int64_t nnz, const int64_t* row
                            void* stream);
 
 /*
+ * The epilogue of a row-sharded call: out = alpha * w + beta * z.
+ * ("On optimizing machine learning workloads via kernel fusion", abstract: the
+ * generic pattern, whose X^T (v * (X y)) is a sum over the rows of X.)
+ *
+ * Row sharding: split X by rows into blocks X_g (for CSR, the row_ptr range of the
+ * block rebased to start at 0, with its col_idx and vals entries) and v into the
+ * matching v_g. Each device computes its partial w_g = X_g^T (v_g * (X_g y)) with
+ * the fused entry points above at alpha = 1, beta = 0, z = NULL; the partials are
+ * summed across devices (one all-reduce of n values); this call then applies
+ * alpha * w + beta * z once. The result meets the bound of a single call up to
+ * the rounding of the partials and of their sum (a few units of the working
+ * precision times S_j).
+ *
+ * n >= 0 (n == 0 does nothing); w and out are device pointers of n entries, z of
+ * n entries or NULL. z is read only when z != NULL and beta != 0. out may equal w
+ * or z (element j is read before it is written); other overlaps are undefined.
+ * Asynchronous on `stream`; allocates nothing.
+ */
+fxtx_status_t fxtx_epilogue_f32(int64_t n, const float* w, float alpha, float beta, const float* z, float* out,
+                                void* stream);
+fxtx_status_t fxtx_epilogue_f64(int64_t n, const double* w, double alpha, double beta, const double* z, double* out,
+                                void* stream);
+
+/*
  * Checks a CSR structure on the device (row_ptr[0] == 0, non-decreasing,
  * row_ptr[m] == nnz, 0 <= col_idx < n). Synchronous: it waits for `stream`.
  * Returns FXTX_OK or FXTX_ERR_BAD_CSR (or an argument/CUDA error).
