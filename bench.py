@@ -76,6 +76,9 @@ WORKLOADS = {
     "csr_powerlaw": ("CSR f32 2,000,000 x 1,000,000, Zipf(1.5) row lengths (mean 100, cap 50,000), Zipf(1.1) "
                      "columns, N(0,1) vals/y, v U[0,1], alpha=1, beta=0",
                      lambda g, m=None: g.csr_powerlaw(**_m({}, m))),
+    "csr_powerlaw_rotated": ("CSR f32 2,000,000 x 1,000,000 as csr_powerlaw with every column index rotated by "
+                             "500,000 (the hot columns mid-range)",
+                             lambda g, m=None: g.csr_powerlaw(**_m({"col_offset": 500_000}, m))),
 }
 
 
@@ -521,6 +524,10 @@ def run_fused(args, name, desc, p, rank, world, dist):
             return fx.dense(X, d["y"], d["v"], p.alpha, p.beta, d["z"], out=o, stream=stream)
         launches = 1 if p.n * p.itemsize <= 2048 else 2
     else:
+        analysis = None
+        if args.analyze:
+            analysis = fx.csr_analyze(d["row_ptr"], d["col_idx"], p.n, dtype_name(p), stream=stream)
+
         def call(o=out):
             return fx.csr(d["row_ptr"], d["col_idx"], d["vals"], d["y"], p.n, d["v"], p.alpha, p.beta, d["z"],
                           out=o, stream=stream)
@@ -632,6 +639,9 @@ def run_fused(args, name, desc, p, rank, world, dist):
         rec["roofline"]["bound"] = "alu" if alu_time > hbm_time else "hbm"
     if p.kind == "csr":
         rec["config"]["nnz"] = p.nnz
+        if analysis is not None:
+            rec["config"]["analysis"] = analysis
+            fx.csr_analysis_clear()
     return rec
 
 
@@ -836,6 +846,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rows", type=int, default=0, help="override the row count (same recipe), for profiling")
     ap.add_argument("--no-extras", action="store_true", help="skip the e2e and unfused-library legs")
+    ap.add_argument("--analyze", action="store_true",
+                    help="CSR: sample the matrix once (fxtx_csr_analyze) before timing, so the plan reads it")
     ap.add_argument("--solver", action="store_true", help="time ridge-regression CG on the tall X instead")
     ap.add_argument("--split", default=None, choices=["rows"],
                     help="rows: split one problem by rows across the ranks (all-reduce of n values) "

@@ -9,7 +9,8 @@ fallback: if the library cannot be loaded, importing the binding fails.
 Raw C-ABI calls (pointers as ints, stream as a cudaStream_t int) carry the C names:
 ``fxtx_dense_f32``, ``fxtx_dense_f64``, ``fxtx_dense_bf16``, ``fxtx_dense_f32_noalloc``,
 ``fxtx_dense_multi_f32``, ``fxtx_dense_multi_f64``, ``fxtx_csr_f32``, ``fxtx_csr_f64``,
-``fxtx_csr_validate``, ``fxtx_epilogue_f32``, ``fxtx_epilogue_f64``, ``fxtx_device_error``,
+``fxtx_csr_validate``, ``fxtx_csr_analyze``, ``fxtx_csr_analysis_clear``,
+``fxtx_csr_plan_describe_host``, ``fxtx_epilogue_f32``, ``fxtx_epilogue_f64``, ``fxtx_device_error``,
 ``fxtx_status_string``,
 ``fxtx_plan_describe``, ``fxtx_multi_plan_describe`` and the ``fxtx_autotune_*`` calls. ``dense``, ``dense_multi`` and
 ``csr`` take torch CUDA tensors; ``epilogue`` applies alpha * w + beta * z. The module
@@ -33,7 +34,11 @@ from ._lib import (  # noqa: F401
     autotune_mode,
     autotune_save,
     csr,
+    csr_analysis_clear,
+    csr_analyze,
+    csr_plan_describe_host,
     csr_validate,
+    CsrStats,
     dense,
     dense_multi,
     device_error,
@@ -45,8 +50,11 @@ from ._lib import (  # noqa: F401
     fxtx_autotune_load,
     fxtx_autotune_save,
     fxtx_autotune_set,
+    fxtx_csr_analysis_clear,
+    fxtx_csr_analyze,
     fxtx_csr_f32,
     fxtx_csr_f64,
+    fxtx_csr_plan_describe_host,
     fxtx_csr_validate,
     fxtx_dense_f32,
     fxtx_dense_f32_noalloc,

@@ -17,6 +17,22 @@ FXTX_ERR_TIMEOUT = 6
 FXTX_ERR_TOO_LARGE = 7
 
 
+class CsrStats(ctypes.Structure):
+    """fxtx_csr_stats_t: sampled characteristics of a CSR matrix and the plan figures they lead to."""
+
+    _fields_ = [("row_samples", ctypes.c_int64), ("col_samples", ctypes.c_int64),
+                ("mean_row_len", ctypes.c_double), ("cv_row_len", ctypes.c_double),
+                ("p50_row_len", ctypes.c_int64), ("p75_row_len", ctypes.c_int64), ("p90_row_len", ctypes.c_int64),
+                ("max_sampled_row_len", ctypes.c_int64), ("long_row_share", ctypes.c_double),
+                ("window_c0", ctypes.c_int64), ("window_len", ctypes.c_int64),
+                ("y_c0", ctypes.c_int64), ("y_len", ctypes.c_int64),
+                ("window_hit_share", ctypes.c_double), ("y_hit_share", ctypes.c_double),
+                ("group_lanes", ctypes.c_int32), ("group_entries", ctypes.c_int32)]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
 def _load() -> ctypes.CDLL:
     path = _build.LIB
     if not os.path.exists(path) or _build._stale():
@@ -35,6 +51,10 @@ def _load() -> ctypes.CDLL:
     lib.fxtx_csr_f32.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, f32, f32, vp, vp, vp]
     lib.fxtx_csr_f64.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, f64, f64, vp, vp, vp]
     lib.fxtx_csr_validate.argtypes = [i64, i64, i64, vp, vp, vp]
+    lib.fxtx_csr_analyze.argtypes = [i32, i64, i64, i64, vp, vp, vp, ctypes.POINTER(CsrStats)]
+    lib.fxtx_csr_analysis_clear.argtypes = []
+    lib.fxtx_csr_plan_describe_host.argtypes = [i32, i64, i64, i64, vp, vp, ctypes.POINTER(CsrStats),
+                                                ctypes.c_char_p, i64]
     lib.fxtx_epilogue_f32.argtypes = [i64, vp, f32, f32, vp, vp, vp]
     lib.fxtx_epilogue_f64.argtypes = [i64, vp, f64, f64, vp, vp, vp]
     lib.fxtx_device_error.argtypes = [vp]
@@ -52,7 +72,8 @@ def _load() -> ctypes.CDLL:
     lib.fxtx_autotune_candidates.argtypes = [i32, i32, i64, i64, i64, i64, ctypes.c_char_p, i64]
     for name in ("fxtx_dense_f32", "fxtx_dense_f64", "fxtx_dense_f32_noalloc", "fxtx_dense_bf16", "fxtx_dense_multi_f32",
                  "fxtx_dense_multi_f64", "fxtx_csr_f32", "fxtx_csr_f64", "fxtx_csr_validate", "fxtx_device_error",
-                 "fxtx_epilogue_f32", "fxtx_epilogue_f64",
+                 "fxtx_epilogue_f32", "fxtx_epilogue_f64", "fxtx_csr_analyze", "fxtx_csr_analysis_clear",
+                 "fxtx_csr_plan_describe_host",
                  "fxtx_plan_describe", "fxtx_multi_plan_describe", "fxtx_autotune_set", "fxtx_autotune_get",
                  "fxtx_autotune_clear", "fxtx_autotune_save", "fxtx_autotune_load", "fxtx_autotune_candidates"):
         getattr(lib, name).restype = i32
@@ -71,6 +92,9 @@ fxtx_dense_multi_f64 = _lib.fxtx_dense_multi_f64
 fxtx_csr_f32 = _lib.fxtx_csr_f32
 fxtx_csr_f64 = _lib.fxtx_csr_f64
 fxtx_csr_validate = _lib.fxtx_csr_validate
+fxtx_csr_analyze = _lib.fxtx_csr_analyze
+fxtx_csr_analysis_clear = _lib.fxtx_csr_analysis_clear
+fxtx_csr_plan_describe_host = _lib.fxtx_csr_plan_describe_host
 fxtx_epilogue_f32 = _lib.fxtx_epilogue_f32
 fxtx_epilogue_f64 = _lib.fxtx_epilogue_f64
 fxtx_device_error = _lib.fxtx_device_error
@@ -326,6 +350,44 @@ def epilogue(w, alpha: float = 1.0, beta: float = 0.0, z=None, out=None, stream=
         rc = fn(n, _ptr(w), alpha, beta, _ptr(z), _ptr(out), _stream(stream, w.device))
     _check(rc, "fxtx_epilogue")
     return out
+
+
+def csr_analyze(row_ptr, col_idx, n: int, dtype: str = "f32", stream=None) -> dict:
+    """Samples a CSR matrix on its GPU and records the statistics for later ``csr`` calls on
+    the same tensors (see fxtx_csr_analyze). Returns the statistics and plan figures for
+    values of `dtype` ("f32" or "f64"). Synchronous."""
+    torch = _torch()
+    if (row_ptr.dim() != 1 or row_ptr.shape[0] < 1 or col_idx.dim() != 1 or not row_ptr.is_cuda
+            or not col_idx.is_cuda):
+        raise ValueError("row_ptr (m + 1) and col_idx (nnz) must be 1-D CUDA tensors")
+    di = row_ptr.get_device()
+    _vec(row_ptr, torch.int64, row_ptr.shape[0], "row_ptr", di)
+    _vec(col_idx, torch.int32, col_idx.shape[0], "col_idx", di)
+    st = CsrStats()
+    with _on(di):
+        rc = fxtx_csr_analyze(1 if dtype in ("f64", "float64") else 0, row_ptr.shape[0] - 1, n, col_idx.shape[0],
+                              _ptr(row_ptr), _ptr(col_idx), _stream(stream, row_ptr.device), ctypes.byref(st))
+    _check(rc, "fxtx_csr_analyze")
+    return st.as_dict()
+
+
+def csr_analysis_clear() -> None:
+    _check(fxtx_csr_analysis_clear(), "fxtx_csr_analysis_clear")
+
+
+def csr_plan_describe_host(row_ptr, col_idx, n: int, dtype: str = "f32") -> tuple[str, dict]:
+    """The plan the model picks for a CSR matrix given as host (numpy) arrays, from its sampled
+    statistics; host only. Returns (description, statistics)."""
+    import numpy as np
+
+    rp = np.ascontiguousarray(row_ptr, dtype=np.int64)
+    ci = np.ascontiguousarray(col_idx, dtype=np.int32)
+    buf = ctypes.create_string_buffer(768)
+    st = CsrStats()
+    _check(fxtx_csr_plan_describe_host(1 if dtype in ("f64", "float64") else 0, rp.shape[0] - 1, n, ci.shape[0],
+                                       rp.ctypes.data if rp.size else None, ci.ctypes.data if ci.size else None,
+                                       ctypes.byref(st), buf, 768), "fxtx_csr_plan_describe_host")
+    return buf.value.decode(), st.as_dict()
 
 
 def csr_validate(row_ptr, col_idx, n: int, stream=None) -> bool:

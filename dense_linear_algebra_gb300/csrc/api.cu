@@ -70,6 +70,41 @@ fxtx_status_t alloc_ws(void** p, size_t bytes, cudaStream_t st) {
   return FXTX_OK;
 }
 
+// Sampled statistics of analysed CSR matrices (fxtx_csr_analyze), keyed by device,
+// structure pointers and sizes. They steer launch parameters only, never results.
+struct Analysis {
+  int dev;
+  const void* row_ptr;
+  const void* col_idx;
+  int64_t m, n, nnz;
+  CsrStats stats;
+};
+constexpr size_t kMaxAnalyses = 64;
+std::mutex g_an_mu;
+std::vector<Analysis> g_an;  // most recent last
+
+bool find_analysis(int dev, const void* rp, const void* ci, int64_t m, int64_t n, int64_t nnz, CsrStats* out) {
+  std::lock_guard<std::mutex> lock(g_an_mu);
+  for (auto it = g_an.rbegin(); it != g_an.rend(); ++it)
+    if (it->dev == dev && it->row_ptr == rp && it->col_idx == ci && it->m == m && it->n == n && it->nnz == nnz) {
+      *out = it->stats;
+      return true;
+    }
+  return false;
+}
+
+void store_analysis(const Analysis& a) {
+  std::lock_guard<std::mutex> lock(g_an_mu);
+  for (auto it = g_an.begin(); it != g_an.end(); ++it)
+    if (it->dev == a.dev && it->row_ptr == a.row_ptr && it->col_idx == a.col_idx && it->m == a.m && it->n == a.n &&
+        it->nnz == a.nnz) {
+      g_an.erase(it);
+      break;
+    }
+  if (g_an.size() >= kMaxAnalyses) g_an.erase(g_an.begin());
+  g_an.push_back(a);
+}
+
 template <typename T>
 bool aligned16(const T* p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
@@ -259,7 +294,10 @@ fxtx_status_t csr_impl(int64_t m, int64_t n, int64_t nnz, const int64_t* row_ptr
   if (s != FXTX_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
 
-  const CsrPlan model = plan_csr(*dev, m, n, nnz, (int)sizeof(T));
+  CsrStats stats;
+  const bool analysed = find_analysis(dev->device, row_ptr, col_idx, m, n, nnz, &stats);
+  const CsrStats* sp = analysed ? &stats : nullptr;
+  const CsrPlan model = plan_csr(*dev, m, n, nnz, (int)sizeof(T), sp);
   CsrArgs<T> a;
   a.m = m; a.n = n; a.nnz = nnz;
   a.row_ptr = row_ptr; a.col_idx = col_idx; a.vals = vals;
@@ -267,9 +305,10 @@ fxtx_status_t csr_impl(int64_t m, int64_t n, int64_t nnz, const int64_t* row_ptr
   a.alpha = (double)alpha; a.beta = (double)beta;
   a.use_z = (z != nullptr && beta != T(0));
 
-  const std::vector<CsrPlan> cands = csr_candidates(*dev, model, m, n, nnz, (int)sizeof(T));
+  const std::vector<CsrPlan> cands = csr_candidates(*dev, model, m, n, nnz, (int)sizeof(T), sp);
   TuneKey key;
   key.kind = 1; key.elem = (int)sizeof(T); key.m = m; key.n = n; key.nnz = nnz;
+  key.flags = analysed ? 1 : 0;
   key.sm_count = dev->sm_count;
   auto run = [&](const CsrPlan& p, void* o) {
     CsrArgs<T> b = a;
@@ -278,7 +317,7 @@ fxtx_status_t csr_impl(int64_t m, int64_t n, int64_t nnz, const int64_t* row_ptr
   };
   const CsrPlan& plan = cands[choose(key, cands, run, (size_t)n * sizeof(T), st)];
   if (log_enabled()) {
-    char buf[320];
+    char buf[512];
     describe(plan, buf, sizeof buf);
     fprintf(stderr, "[fxtx] m=%lld n=%lld nnz=%lld %s\n", (long long)m, (long long)n, (long long)nnz, buf);
   }
@@ -355,6 +394,38 @@ fxtx_status_t epilogue_impl(int64_t n, const T* w, T alpha, T beta, const T* z, 
     return FXTX_ERR_CUDA;
   }
   return FXTX_OK;
+}
+
+void fill_stats(const CsrStats& st, const CsrPlan& p, fxtx_csr_stats_t* out) {
+  out->row_samples = st.row_samples;
+  out->col_samples = st.col_samples;
+  out->mean_row_len = st.mean_len;
+  out->cv_row_len = st.cv_len;
+  out->p50_row_len = st.p50_len;
+  out->p75_row_len = st.p75_len;
+  out->p90_row_len = st.p90_len;
+  out->max_sampled_row_len = st.max_len;
+  out->long_row_share = st.long_share;
+  out->window_c0 = p.win_c0;
+  out->window_len = p.win_len;
+  out->y_c0 = p.y0;
+  out->y_len = p.ylen;
+  out->window_hit_share = p.win_hit;
+  out->y_hit_share = p.y_hit;
+  out->group_lanes = p.group_lpr;
+  out->group_entries = p.group_kg;
+}
+
+const DeviceInfo* device_or_fallback(DeviceInfo* fallback) {
+  const DeviceInfo* dev = nullptr;
+  if (current_device(&dev) == FXTX_OK) return dev;
+  // no GB300 current: a 152-SM device with 227 KB of shared memory per block
+  fallback->sm_count = 152;
+  fallback->cc_major = 10;
+  fallback->cc_minor = 3;
+  fallback->smem_optin = 232448;
+  fallback->smem_per_sm = 233472;
+  return fallback;
 }
 
 }  // namespace
@@ -437,6 +508,60 @@ fxtx_status_t fxtx_csr_validate(int64_t m, int64_t n, int64_t nnz, const int64_t
     return FXTX_ERR_CUDA;
   }
   return host ? FXTX_ERR_BAD_CSR : FXTX_OK;
+}
+
+fxtx_status_t fxtx_csr_analyze(int is_f64, int64_t m, int64_t n, int64_t nnz, const int64_t* row_ptr,
+                               const int32_t* col_idx, void* stream, fxtx_csr_stats_t* stats) {
+  if (m < 0 || n < 0 || nnz < 0 || n > INT32_MAX) return FXTX_ERR_INVALID_ARG;
+  if ((m > 0 && row_ptr == nullptr) || (nnz > 0 && col_idx == nullptr)) return FXTX_ERR_INVALID_ARG;
+  const DeviceInfo* dev = nullptr;
+  fxtx_status_t s = current_device(&dev);
+  if (s != FXTX_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  std::vector<int64_t> lens(kCsrSamples, 0);
+  std::vector<int32_t> cols(kCsrSamples, 0);
+  const int nl = (int)std::min<int64_t>(m, kCsrSamples), nc = (int)std::min<int64_t>(nnz, kCsrSamples);
+  if (nl > 0 || nc > 0) {
+    void* ws = nullptr;
+    const size_t lb = (size_t)kCsrSamples * 8, cb = (size_t)kCsrSamples * 4;
+    s = alloc_ws(&ws, lb + cb, st);
+    if (s != FXTX_OK) return s;
+    int64_t* dl = static_cast<int64_t*>(ws);
+    int32_t* dc = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + lb);
+    cudaError_t e = launch_csr_sample(m, nnz, row_ptr, col_idx, dl, dc, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(lens.data(), dl, lb, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(cols.data(), dc, cb, cudaMemcpyDeviceToHost, st);
+    cudaFreeAsync(ws, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return FXTX_ERR_CUDA;
+    }
+  }
+  Analysis an{dev->device, row_ptr, col_idx, m, n, nnz,
+              csr_stats_from_samples(n, lens.data(), nl, cols.data(), nc, csr_warp_long())};
+  store_analysis(an);
+  if (stats) fill_stats(an.stats, plan_csr(*dev, m, n, nnz, is_f64 ? 8 : 4, &an.stats), stats);
+  return FXTX_OK;
+}
+
+fxtx_status_t fxtx_csr_analysis_clear(void) {
+  std::lock_guard<std::mutex> lock(g_an_mu);
+  g_an.clear();
+  return FXTX_OK;
+}
+
+fxtx_status_t fxtx_csr_plan_describe_host(int is_f64, int64_t m, int64_t n, int64_t nnz, const int64_t* row_ptr,
+                                          const int32_t* col_idx, fxtx_csr_stats_t* stats, char* buf, int64_t cap) {
+  if (m < 0 || n < 0 || nnz < 0 || (m > 0 && row_ptr == nullptr) || (nnz > 0 && col_idx == nullptr))
+    return FXTX_ERR_INVALID_ARG;
+  DeviceInfo fallback;
+  const DeviceInfo* dev = device_or_fallback(&fallback);
+  const CsrStats st = csr_stats_from_host(m, n, nnz, row_ptr, col_idx);
+  const CsrPlan p = plan_csr(*dev, m, n, nnz, is_f64 ? 8 : 4, &st);
+  if (stats) fill_stats(st, p, stats);
+  if (buf != nullptr && cap > 0) describe(p, buf, (size_t)cap);
+  return FXTX_OK;
 }
 
 fxtx_status_t fxtx_device_error(void* stream) {
@@ -539,7 +664,7 @@ fxtx_status_t fxtx_autotune_candidates(int is_csr, int is_f64, int64_t m, int64_
     const int w = snprintf(buf + used, (size_t)cap - used, "%s%s", used ? "\n" : "", line);
     if (w > 0) used = std::min<size_t>((size_t)cap - 1, used + (size_t)w);
   };
-  char line[320];
+  char line[512];
   if (is_csr) {
     for (const CsrPlan& p : csr_candidates(*dev, plan_csr(*dev, m, n, nnz, elem), m, n, nnz, elem)) {
       describe(p, line, sizeof line);

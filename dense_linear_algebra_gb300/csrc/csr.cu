@@ -16,7 +16,8 @@
 //   long   (> WARP_LONG)  deferred to queues bucketed by length; in the long-row
 //                         kernel a group of 4 warps takes each row, longest
 //                         buckets first, two passes
-// The y gathers of hot columns hit a copy of y[0, ylen) in shared memory.
+// The y gathers of hot columns hit a copy of y[y0, y0 + ylen) in shared memory;
+// the two windows sit on the column ranges a sample of col_idx hits most.
 // Row dots of a packed batch are formed lane-locally per row segment, and each
 // segment's partial is added once into a per-warp fp64 buffer; t_i is then
 // computed once per row. Each CTA (one per SM; 1024 threads, 768 for the fp64
@@ -25,7 +26,8 @@
 // atomic per column; columns outside the window go straight to out with
 // atomics. fp64 window updates fold the product into the atomic itself (a CAS
 // loop around one fused multiply-add).
-// The prologue writes out = beta z and zeroes the counters. Warps of the packed
+// The prologue writes out = beta z, zeroes the counters and sets the window starts
+// (from the plan's sample, or from its own sample of col_idx). Warps of the packed
 // kernel take 32-row windows from one global counter; the fp64 lane-group kernel
 // splits rows among CTAs by equal shares of nnz + row_cost * rows.
 #include "common.cuh"
@@ -69,7 +71,7 @@ __device__ __forceinline__ void smem_fma_add(double* p, double a, double b) {
 }
 
 // Shared-memory windows of one CTA: scatters into columns [c0, c0 + len) are
-// accumulated in `acc`, and y[0, ylen) is held in `ys` for the gathers.
+// accumulated in `acc`, and y[y0, y0 + ylen) is held in `ys` for the gathers.
 template <typename T>
 struct Window {
   T* acc;
@@ -77,6 +79,7 @@ struct Window {
   int64_t len;
   T* out;
   const T* ys;
+  int64_t y0;
   int64_t ylen;
   const T* y;
   // out[col] += a * b, through the shared window when col falls inside it
@@ -87,15 +90,28 @@ struct Window {
     else
       atomicAdd(out + col, a * b);
   }
-  __device__ __forceinline__ T yat(int32_t col) const { return (int64_t)col < ylen ? ys[col] : ldg(y + col); }
+  __device__ __forceinline__ T yat(int32_t col) const {
+    const uint64_t off = (uint64_t)((int64_t)col - y0);
+    return off < (uint64_t)ylen ? ys[off] : ldg(y + col);
+  }
 };
 
-// Zeroes the accumulator window and copies y[0, ylen) into shared memory.
+// Workspace slots of the two window starts, written by the prologue.
+constexpr int SLOT_WIN_C0 = 8, SLOT_Y0 = 9;
+
+template <typename T>
+__device__ __forceinline__ Window<T> make_window(const CsrArgs<T>& a, T* acc, int64_t win_len, const T* ys,
+                                                 int64_t ylen) {
+  return Window<T>{acc, (int64_t)a.counters[SLOT_WIN_C0], win_len, a.out, ys, (int64_t)a.counters[SLOT_Y0], ylen,
+                   a.y};
+}
+
+// Zeroes the accumulator window and copies y[y0, y0 + ylen) into shared memory.
 template <typename T>
 __device__ __forceinline__ void window_init(const Window<T>& w) {
   for (int64_t j = threadIdx.x; j < w.len; j += blockDim.x) w.acc[j] = T(0);
   T* ys = const_cast<T*>(w.ys);
-  for (int64_t j = threadIdx.x; j < w.ylen; j += blockDim.x) ys[j] = ldg(w.y + j);
+  for (int64_t j = threadIdx.x; j < w.ylen; j += blockDim.x) ys[j] = ldg(w.y + w.y0 + j);
 }
 
 template <typename T>
@@ -131,9 +147,107 @@ int csr_warp_long() { return WARP_LONG; }
 int csr_group_threads() { return CSR_GROUP_THREADS; }
 int csr_long_buckets() { return LONG_BUCKETS; }
 
-// out = beta z (or 0); row partition; counters.
+constexpr int PROLOGUE_THREADS = 256;
+
+// Block-wide first maximum of (count, start) keys: the largest count, the lowest start on ties.
+__device__ __forceinline__ unsigned long long block_max_key(unsigned long long key, unsigned long long* red) {
+  for (int o = 16; o > 0; o >>= 1) key = tmax(key, __shfl_xor_sync(FULL_MASK, key, o));
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) red[warp] = key;
+  __syncthreads();
+  key = 0ull;
+  for (int w = 0; w < PROLOGUE_THREADS / 32; ++w) key = tmax(key, red[w]);
+  return key;
+}
+
+// The start of the len-column window holding the most sampled columns (pre: prefix sums of
+// the per-bin sample counts over nb bins of wb columns): the rule of csr_place_window on the
+// host, first maximum over bin-aligned starts, clamped to [0, n - len].
+__device__ int64_t place_on_device(const int* pre, int nb, int64_t wb, int64_t n, int64_t len,
+                                   unsigned long long* red) {
+  if (len >= n) return 0;
+  const int kb = (int)tmin<int64_t>(tmax<int64_t>(1, len / wb), nb);
+  unsigned long long key = 0ull;
+  for (int s0 = threadIdx.x; s0 + kb <= nb; s0 += PROLOGUE_THREADS) {
+    const unsigned long long w = (unsigned long long)(pre[s0 + kb] - pre[s0]);
+    key = tmax(key, (w << 32) | (unsigned long long)(0xffffffffu - (unsigned)s0));
+  }
+  key = block_max_key(key, red);
+  const int64_t s0 = (int64_t)(0xffffffffu - (unsigned)(key & 0xffffffffull));
+  return tmin<int64_t>(s0 * wb, n - len);
+}
+
+// Places the scatter window and the copy of y on the column ranges that a strided sample of
+// kCsrSamples column indices (the positions of csr_sample_index) hits most: a histogram over
+// bins of csr_bin_width(n) columns, its prefix sums, and the first maximum of each window's
+// sampled count. Run by one block of PROLOGUE_THREADS threads.
 template <typename T>
-__global__ void csr_prologue_kernel(const CsrArgs<T> a, const int nparts, const int row_cost) {
+__device__ void place_windows(const CsrArgs<T>& a, int64_t win_len, int64_t ylen) {
+  __shared__ int hist[kCsrBins + 1];
+  __shared__ int part[PROLOGUE_THREADS];
+  __shared__ unsigned long long red[PROLOGUE_THREADS / 32];
+  const int64_t wb = csr_bin_width(a.n);
+  const int nb = (int)((a.n + wb - 1) / wb);
+  for (int b = threadIdx.x; b <= kCsrBins; b += PROLOGUE_THREADS) hist[b] = 0;
+  __syncthreads();
+  const int ns = (int)tmin<int64_t>(a.nnz, kCsrSamples);
+  constexpr int U = 8;  // sampled loads in flight per thread
+  for (int s0 = threadIdx.x; s0 < ns; s0 += PROLOGUE_THREADS * U) {
+    int32_t c[U];
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const int s1 = s0 + k * PROLOGUE_THREADS;
+      c[k] = s1 < ns ? ldg(a.col_idx + csr_sample_index(s1, a.nnz)) : -1;
+    }
+#pragma unroll
+    for (int k = 0; k < U; ++k)
+      if (c[k] >= 0 && (int64_t)c[k] < a.n) atomicAdd(&hist[(int64_t)c[k] / wb], 1);
+  }
+  __syncthreads();
+  // exclusive prefix sums in place: each thread owns kCsrBins / PROLOGUE_THREADS consecutive bins
+  constexpr int PER = kCsrBins / PROLOGUE_THREADS;
+  static_assert(kCsrBins % PROLOGUE_THREADS == 0, "bins per thread");
+  int v[PER], sum = 0;
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    v[k] = hist[threadIdx.x * PER + k];
+    sum += v[k];
+  }
+  part[threadIdx.x] = sum;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int run = 0;
+    for (int t = 0; t < PROLOGUE_THREADS; ++t) {
+      const int x = part[t];
+      part[t] = run;
+      run += x;
+    }
+    hist[kCsrBins] = run;
+  }
+  __syncthreads();
+  int run = part[threadIdx.x];
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    hist[threadIdx.x * PER + k] = run;
+    run += v[k];
+  }
+  __syncthreads();
+  // bins past nb are empty, so the prefix at nb is the total as well
+  const int64_t c0 = place_on_device(hist, nb, wb, a.n, win_len, red);
+  const int64_t y0 = place_on_device(hist, nb, wb, a.n, ylen, red);
+  if (threadIdx.x == 0) {
+    a.counters[SLOT_WIN_C0] = (unsigned long long)c0;
+    a.counters[SLOT_Y0] = (unsigned long long)y0;
+  }
+}
+
+// out = beta z (or 0); row partition; counters; the starts of the shared-memory windows
+// (from the plan, or placed here from a column sample when the plan asks for it).
+template <typename T>
+__global__ void __launch_bounds__(PROLOGUE_THREADS)
+    csr_prologue_kernel(const CsrArgs<T> a, const int nparts, const int row_cost, const int64_t win_c0,
+                        const int64_t y0, const int64_t win_len, const int64_t ylen, const bool place) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   for (int64_t j = tid; j < a.n; j += stride) a.out[j] = a.use_z ? (T)(a.beta * (double)a.z[j]) : T(0);
@@ -157,6 +271,14 @@ __global__ void csr_prologue_kernel(const CsrArgs<T> a, const int nparts, const 
     a.part[p] = r;
   }
   if (tid < LONG_BUCKETS + 2) a.counters[tid] = 0ull;
+  if (blockIdx.x == 0) {
+    if (place) {
+      place_windows(a, win_len, ylen);
+    } else if (threadIdx.x == 0) {
+      a.counters[SLOT_WIN_C0] = (unsigned long long)win_c0;
+      a.counters[SLOT_Y0] = (unsigned long long)y0;
+    }
+  }
 }
 
 // One row of up to WARP_LONG entries (weight vi), taken by a whole warp: pass 1 forms the
@@ -202,7 +324,7 @@ __device__ __forceinline__ void warp_row(const CsrArgs<T>& a, const Window<T>& w
 
 template <typename T>
 __global__ void __launch_bounds__(CSR_THREADS, 1)
-    csr_rows_kernel(const CsrArgs<T> a, const int64_t win_c0, const int64_t win_len, const int64_t ylen) {
+    csr_rows_kernel(const CsrArgs<T> a, const int64_t win_len, const int64_t ylen) {
   constexpr int PACK_K = Pack<T>::K, PACK_CAP = Pack<T>::CAP;
   extern __shared__ __align__(128) unsigned char smem[];
   T* wacc = reinterpret_cast<T*>(smem);
@@ -213,7 +335,7 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
   double* dotb = reinterpret_cast<double*>(scratch);  // [32] row dots of the batch (fp32: [64] float-float words)
   T* tb = reinterpret_cast<T*>(scratch + 32 * 8);              // [32] row scales alpha * v_i * u_i
   int64_t* rsb = reinterpret_cast<int64_t*>(scratch + 64 * 8);  // [33] row starts of the window
-  const Window<T> win{wacc, win_c0, win_len, a.out, ys, ylen, a.y};
+  const Window<T> win = make_window(a, wacc, win_len, ys, ylen);
   const int64_t re = a.m;
   const T alpha = (T)a.alpha;
 
@@ -355,7 +477,7 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
     __syncwarp();  // rsb reuse
   }
   __syncthreads();
-  window_flush(wacc, win_c0, win_len, a.out);
+  window_flush(wacc, win.c0, win_len, a.out);
 }
 
 // Short rows in lane groups: LPR lanes per row, KG entries per lane held in
@@ -365,13 +487,13 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
 // to warp_row or to the long-row queue.
 template <typename T, int LPR, int KG>
 __global__ void __launch_bounds__(CSR_GROUP_THREADS, 1)
-    csr_group_kernel(const CsrArgs<T> a, const int64_t win_c0, const int64_t win_len, const int64_t ylen) {
+    csr_group_kernel(const CsrArgs<T> a, const int64_t win_len, const int64_t ylen) {
   constexpr int G = 32 / LPR;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ unsigned long long s_next;
   T* wacc = reinterpret_cast<T*>(smem);
   const T* ys = reinterpret_cast<const T*>(smem + window_bytes(win_len, sizeof(T)));
-  const Window<T> win{wacc, win_c0, win_len, a.out, ys, ylen, a.y};
+  const Window<T> win = make_window(a, wacc, win_len, ys, ylen);
   const int lane = threadIdx.x & 31;
   const int g = lane / LPR, q = lane % LPR;
   const int64_t rb = a.part[blockIdx.x], re = a.part[blockIdx.x + 1];
@@ -425,7 +547,7 @@ __global__ void __launch_bounds__(CSR_GROUP_THREADS, 1)
     }
   }
   __syncthreads();
-  window_flush(wacc, win_c0, win_len, a.out);
+  window_flush(wacc, win.c0, win_len, a.out);
 }
 
 // Rows longer than WARP_LONG: each group of LONG_GROUP threads takes queued rows
@@ -456,7 +578,7 @@ __device__ __forceinline__ void group_barrier(int id, int count) {
 
 template <typename T>
 __global__ void __launch_bounds__(CSR_THREADS, 1)
-    csr_long_kernel(const CsrArgs<T> a, const int64_t win_c0, const int64_t win_len, const int64_t ylen) {
+    csr_long_kernel(const CsrArgs<T> a, const int64_t win_len, const int64_t ylen) {
   constexpr int U = long_unroll<T>();
   constexpr int GW = LONG_GROUP / 32;           // warps per group
   constexpr int NG = CSR_THREADS / LONG_GROUP;  // groups per CTA (named barriers 1 .. NG)
@@ -467,7 +589,7 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
   __shared__ double s_red[NG][2][GW];
   T* wacc = reinterpret_cast<T*>(smem);
   const T* ys = reinterpret_cast<const T*>(smem + window_bytes(win_len, sizeof(T)));
-  const Window<T> win{wacc, win_c0, win_len, a.out, ys, ylen, a.y};
+  const Window<T> win = make_window(a, wacc, win_len, ys, ylen);
   const int lane = threadIdx.x & 31;
   const int grp = threadIdx.x / LONG_GROUP, gt = threadIdx.x % LONG_GROUP, gw = gt >> 5;
   const int bar = 1 + grp;
@@ -535,7 +657,7 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
     }
   }
   __syncthreads();
-  window_flush(wacc, win_c0, win_len, a.out);
+  window_flush(wacc, win.c0, win_len, a.out);
 }
 
 template <typename T, int LPR, int KG>
@@ -543,7 +665,7 @@ static cudaError_t launch_group(const CsrPlan& p, const CsrArgs<T>& a, cudaStrea
   if (p.threads != CSR_GROUP_THREADS) return cudaErrorInvalidConfiguration;
   const cudaError_t e = ensure_smem((const void*)csr_group_kernel<T, LPR, KG>, p.long_smem);
   if (e != cudaSuccess) return e;
-  csr_group_kernel<T, LPR, KG><<<p.ctas, p.threads, p.long_smem, st>>>(a, p.win_c0, p.win_len, p.ylen);
+  csr_group_kernel<T, LPR, KG><<<p.ctas, p.threads, p.long_smem, st>>>(a, p.win_len, p.ylen);
   return cudaGetLastError();
 }
 
@@ -551,8 +673,9 @@ template <typename T>
 cudaError_t launch_csr(const CsrPlan& p, const CsrArgs<T>& a, cudaStream_t st) {
   {
     const int64_t work = std::max<int64_t>(a.n, (int64_t)p.ctas + 1);
-    const int blocks = (int)std::min<int64_t>((work + 255) / 256, 4096);
-    csr_prologue_kernel<T><<<blocks, 256, 0, st>>>(a, p.ctas, p.row_cost);
+    const int blocks = (int)std::min<int64_t>((work + PROLOGUE_THREADS - 1) / PROLOGUE_THREADS, 4096);
+    csr_prologue_kernel<T><<<blocks, PROLOGUE_THREADS, 0, st>>>(a, p.ctas, p.row_cost, p.win_c0, p.y0, p.win_len,
+                                                                 p.ylen, p.place_on_device && a.nnz > 0);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -561,7 +684,7 @@ cudaError_t launch_csr(const CsrPlan& p, const CsrArgs<T>& a, cudaStream_t st) {
   if (p.group_lpr == 0) {
     e = ensure_smem((const void*)csr_rows_kernel<T>, p.smem);
     if (e != cudaSuccess) return e;
-    csr_rows_kernel<T><<<p.ctas, p.threads, p.smem, st>>>(a, p.win_c0, p.win_len, p.ylen);
+    csr_rows_kernel<T><<<p.ctas, p.threads, p.smem, st>>>(a, p.win_len, p.ylen);
   } else {
     switch (p.group_lpr * 100 + p.group_kg) {
       case 208: e = launch_group<T, 2, 8>(p, a, st); break;
@@ -580,12 +703,32 @@ cudaError_t launch_csr(const CsrPlan& p, const CsrArgs<T>& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   e = ensure_smem((const void*)csr_long_kernel<T>, p.long_smem);
   if (e != cudaSuccess) return e;
-  csr_long_kernel<T><<<p.long_ctas, p.long_threads, p.long_smem, st>>>(a, p.win_c0, p.win_len, p.ylen);
+  csr_long_kernel<T><<<p.long_ctas, p.long_threads, p.long_smem, st>>>(a, p.win_len, p.ylen);
   return cudaGetLastError();
 }
 
 template cudaError_t launch_csr<float>(const CsrPlan&, const CsrArgs<float>&, cudaStream_t);
 template cudaError_t launch_csr<double>(const CsrPlan&, const CsrArgs<double>&, cudaStream_t);
+
+// The strided sample the model reads: kCsrSamples row lengths and column indices at the
+// positions of csr_sample_index.
+__global__ void csr_sample_kernel(int64_t m, int64_t nnz, const int64_t* row_ptr, const int32_t* col_idx,
+                                  int64_t* lens, int32_t* cols) {
+  const int nl = (int)tmin<int64_t>(m, kCsrSamples), nc = (int)tmin<int64_t>(nnz, kCsrSamples);
+  for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < kCsrSamples; s += gridDim.x * blockDim.x) {
+    if (s < nl) {
+      const int64_t i = csr_sample_index(s, m);
+      lens[s] = row_ptr[i + 1] - row_ptr[i];
+    }
+    if (s < nc) cols[s] = col_idx[csr_sample_index(s, nnz)];
+  }
+}
+
+cudaError_t launch_csr_sample(int64_t m, int64_t nnz, const int64_t* row_ptr, const int32_t* col_idx, int64_t* lens,
+                              int32_t* cols, cudaStream_t st) {
+  csr_sample_kernel<<<kCsrSamples / 256, 256, 0, st>>>(m, nnz, row_ptr, col_idx, lens, cols);
+  return cudaGetLastError();
+}
 
 // Structure check: flag bit 1 set on any violation.
 __global__ void csr_validate_kernel(int64_t m, int64_t n, int64_t nnz, const int64_t* row_ptr, const int32_t* col_idx,

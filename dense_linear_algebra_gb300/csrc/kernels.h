@@ -59,6 +59,11 @@ cudaError_t launch_csr(const CsrPlan& p, const CsrArgs<T>& a, cudaStream_t st);
 cudaError_t launch_csr_validate(int64_t m, int64_t n, int64_t nnz, const int64_t* row_ptr,
                                 const int32_t* col_idx, int* flag, cudaStream_t st);
 
+// Gathers the model's strided sample: kCsrSamples row lengths into lens and column indices
+// into cols (the first min(m, kCsrSamples) and min(nnz, kCsrSamples) entries are written).
+cudaError_t launch_csr_sample(int64_t m, int64_t nnz, const int64_t* row_ptr, const int32_t* col_idx, int64_t* lens,
+                              int32_t* cols, cudaStream_t st);
+
 // out = alpha * w + beta * z (z read only when use_z): the epilogue of a row-sharded call,
 // applied once after the devices' partials are summed.
 template <typename T>

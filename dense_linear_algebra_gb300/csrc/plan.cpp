@@ -2,6 +2,7 @@
 #include "plan.h"
 
 #include <algorithm>
+#include <cmath>
 #include <cstdio>
 
 namespace fxtx {
@@ -30,6 +31,8 @@ constexpr double kFma32PerSmClk = 124.7;
 constexpr double kFma64PerSmClk = 2.0;
 constexpr double kL2SectorsPerS = 4.9e11;
 constexpr double kLaunchUs = 4.0;  // launch, grid reduction and epilogue of one call
+constexpr double kScatterMissWeight = 1.15;  // cost of a scatter outside the window / a gather outside y's copy
+constexpr double kSplitGain = 0.02;          // least sampled gain that moves the window/y split off ¾
 
 }  // namespace
 
@@ -55,12 +58,14 @@ double dense_est_us(const DeviceInfo& dev, const DensePlan& p, int64_t m, int64_
 }
 
 // CSR call: vals and col_idx once, row_ptr, v, y, z and out; two FMAs per entry; a
-// random L2 sector for each gather and scatter outside the shared-memory copies,
-// with columns taken as uniform over [0, n).
+// random L2 sector for each gather and scatter outside the shared-memory copies, at the
+// sampled hit rates of the two windows when the plan has them, else with columns taken
+// as uniform over [0, n).
 double csr_est_us(const DeviceInfo& dev, const CsrPlan& p, int64_t m, int64_t n, int64_t nnz, int elem) {
   const double bytes = (double)nnz * (elem + 4) + (double)(m + 1) * 8 + (double)m * elem + 3.0 * n * elem;
   const double nn = (double)std::max<int64_t>(n, 1);
-  const double miss = (1.0 - std::min(1.0, p.ylen / nn)) + (1.0 - std::min(1.0, p.win_len / nn));
+  const double miss = p.sampled ? (1.0 - p.y_hit) + (1.0 - p.win_hit)
+                                : (1.0 - std::min(1.0, p.ylen / nn)) + (1.0 - std::min(1.0, p.win_len / nn));
   // fp64 lane groups reach 45 % of the fp64 FMA rate (padding slots, reductions, the CAS
   // loop); fp32 packed rows are bound by memory and L2, not FMAs
   return roofline_us(dev, bytes, 0.8, 2.0 * nnz, elem, elem == 8 ? 0.45 : 0.6, miss * nnz, 0.6);
@@ -216,11 +221,102 @@ std::vector<DensePlan> dense_candidates(const DeviceInfo& dev, const DensePlan& 
   return c;
 }
 
-CsrPlan plan_csr(const DeviceInfo& dev, int64_t m, int64_t n, int64_t nnz, int elem) {
+CsrStats csr_stats_from_samples(int64_t n, const int64_t* lens, int nl, const int32_t* cols, int nc,
+                                int64_t warp_cap) {
+  CsrStats st;
+  st.valid = true;
+  st.row_samples = nl;
+  st.col_samples = nc;
+  if (nl > 0) {
+    std::vector<int64_t> v(lens, lens + nl);
+    std::sort(v.begin(), v.end());
+    double sum = 0.0, sq = 0.0, lng = 0.0;
+    for (int64_t x : v) {
+      sum += (double)x;
+      sq += (double)x * (double)x;
+      if (x > warp_cap) lng += (double)x;
+    }
+    st.mean_len = sum / nl;
+    const double var = std::max(0.0, sq / nl - st.mean_len * st.mean_len);
+    st.cv_len = st.mean_len > 0.0 ? std::sqrt(var) / st.mean_len : 0.0;
+    auto pct = [&](int q) { return v[std::min<int64_t>(nl - 1, (int64_t)nl * q / 100)]; };
+    st.p50_len = pct(50);
+    st.p75_len = pct(75);
+    st.p90_len = pct(90);
+    st.max_len = v.back();
+    st.long_share = sum > 0.0 ? lng / sum : 0.0;
+  }
+  st.bin_width = csr_bin_width(n);
+  st.bins = (int)((n + st.bin_width - 1) / st.bin_width);
+  st.col_hist.assign((size_t)std::max(st.bins, 1), 0);
+  for (int s = 0; s < nc; ++s) {
+    const int64_t c = cols[s];
+    if (c >= 0 && c < n) ++st.col_hist[(size_t)(c / st.bin_width)];
+  }
+  return st;
+}
+
+CsrStats csr_stats_from_host(int64_t m, int64_t n, int64_t nnz, const int64_t* row_ptr, const int32_t* col_idx) {
+  const int nl = (int)std::min<int64_t>(m, kCsrSamples), nc = (int)std::min<int64_t>(nnz, kCsrSamples);
+  std::vector<int64_t> lens((size_t)std::max(nl, 1));
+  std::vector<int32_t> cols((size_t)std::max(nc, 1));
+  for (int s = 0; s < nl; ++s) {
+    const int64_t i = csr_sample_index(s, m);
+    lens[(size_t)s] = row_ptr[i + 1] - row_ptr[i];
+  }
+  for (int s = 0; s < nc; ++s) cols[(size_t)s] = col_idx[csr_sample_index(s, nnz)];
+  return csr_stats_from_samples(n, lens.data(), nl, cols.data(), nc, csr_warp_long());
+}
+
+int64_t csr_place_window(const CsrStats& st, int64_t n, int64_t len, int* hits) {
+  int total = 0;
+  for (int c : st.col_hist) total += c;
+  if (len >= n || st.bins <= 0) {
+    if (hits) *hits = len >= n ? total : 0;
+    return 0;
+  }
+  const int64_t kb = std::max<int64_t>(1, len / st.bin_width);
+  std::vector<int64_t> pre((size_t)st.bins + 1, 0);
+  for (int b = 0; b < st.bins; ++b) pre[(size_t)b + 1] = pre[(size_t)b] + st.col_hist[(size_t)b];
+  int64_t best = -1, bs = 0;
+  for (int64_t s0 = 0; s0 + kb <= st.bins; ++s0) {
+    const int64_t w = pre[(size_t)(s0 + kb)] - pre[(size_t)s0];
+    if (w > best) {
+      best = w;
+      bs = s0;
+    }
+  }
+  if (best < 0) {  // fewer bins than the window spans
+    best = pre[(size_t)st.bins];
+    bs = 0;
+  }
+  if (hits) *hits = (int)best;
+  return std::min<int64_t>(bs * st.bin_width, n - len);
+}
+
+namespace {
+
+// Fills the window placement of p from the sample (win_len and ylen already set).
+void place_sampled(CsrPlan& p, const CsrStats& st, int64_t n) {
+  int hw = 0, hy = 0;
+  p.win_c0 = csr_place_window(st, n, p.win_len, &hw);
+  p.y0 = csr_place_window(st, n, p.ylen, &hy);
+  const double ns = (double)std::max(st.col_samples, 1);
+  p.win_hit = st.col_samples > 0 ? hw / ns : (p.win_len >= n ? 1.0 : 0.0);
+  p.y_hit = st.col_samples > 0 ? hy / ns : (p.ylen >= n ? 1.0 : 0.0);
+}
+
+}  // namespace
+
+CsrPlan plan_csr(const DeviceInfo& dev, int64_t m, int64_t n, int64_t nnz, int elem, const CsrStats* st) {
   CsrPlan p;
-  // fp64 short rows go to lane groups sized to the mean row (8 entries per lane); fp32 to packed batches
+  const bool sampled = st != nullptr && st->valid;
+  // fp64 short rows go to lane groups sized to the rows (16 entries per lane); fp32 to packed batches
   if (elem == 8) {
-    const double avg = m > 0 ? (double)nnz / (double)m : 0.0;
+    // the row length the groups are sized for: the sampled 75th percentile, which keeps a few
+    // long rows from widening every group; else the mean
+    const double avg = sampled && st->row_samples > 0 ? (double)st->p75_len
+                                                      : (m > 0 ? (double)nnz / (double)m : 0.0);
     // 16 entries a lane and just enough lanes to cover the mean row (rows of Poisson(50)
     // entries: 4 x 16; measured 1,441 us against 1,636 for 8 x 8, one shuffle level fewer
     // per row and two rows more per warp); rows averaging 16 entries or fewer: 2 x 8
@@ -244,36 +340,66 @@ CsrPlan plan_csr(const DeviceInfo& dev, int64_t m, int64_t n, int64_t nnz, int e
   const int64_t fixed = (int64_t)csr_rows_smem(0, 0, elem) + 32;  // per-warp scratch of the row kernel + padding
   p.ctas = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)dev.sm_count, cdiv(std::max<int64_t>(m, 1), 1024)));
   p.long_ctas = dev.sm_count;
-  // shared memory: the accumulator window takes up to three quarters, a copy of y's head the rest
+  // shared memory: the accumulator window takes three quarters (the unsampled default), a
+  // copy of y the rest; with a column sample, the split of ½, ¾ or ⅞ whose placed windows
+  // leave the fewest estimated misses, weighting a scatter miss (a global reduction, ~1.7 ns
+  // on the power-law workload) kScatterMissWeight times a gather miss (~1.5 ns), and leaving
+  // ¾ only for a gain of at least kSplitGain of the sampled entries (sampling noise)
   const int64_t room = std::max<int64_t>(0, budget - fixed) / elem;
-  p.win_c0 = 0;
-  p.win_len = std::min<int64_t>(n, room * 3 / 4);
-  p.ylen = std::min<int64_t>(n, room - p.win_len);
-  p.smem = csr_rows_smem(p.win_len, p.ylen, elem);
-  p.long_smem = csr_rows_smem(p.win_len, p.ylen, elem) - (size_t)csr_rows_smem(0, 0, elem);
   p.row_cost = 8;
   p.queue_cap = std::min<int64_t>(m, nnz / (p.warp_cap + 1) + 1);
   p.ws_bytes = align128((size_t)(p.ctas + 1) * 8) +
                align128((size_t)csr_long_buckets() * std::max<int64_t>(p.queue_cap, 1) * 8) + 128;
+  auto set_split = [&](CsrPlan& q, int eighths) {
+    q.win_len = std::min<int64_t>(n, room * eighths / 8);
+    q.ylen = std::min<int64_t>(n, room - q.win_len);
+    q.smem = csr_rows_smem(q.win_len, q.ylen, elem);
+    q.long_smem = q.smem - (size_t)csr_rows_smem(0, 0, elem);
+  };
+  set_split(p, 6);
+  if (sampled) {
+    p.sampled = true;
+    p.mean_len = st->mean_len;
+    p.cv_len = st->cv_len;
+    p.long_share = st->long_share;
+    p.p75_len = st->p75_len;
+    place_sampled(p, *st, n);
+    double best = kScatterMissWeight * (1.0 - p.win_hit) + (1.0 - p.y_hit) - kSplitGain;
+    for (int eighths : {4, 7}) {
+      CsrPlan q = p;
+      set_split(q, eighths);
+      place_sampled(q, *st, n);
+      const double cost = kScatterMissWeight * (1.0 - q.win_hit) + (1.0 - q.y_hit);
+      if (cost < best) {
+        best = cost;
+        p = q;
+      }
+    }
+  } else {
+    p.win_c0 = 0;
+    p.y0 = 0;
+    p.place_on_device = p.win_len < n || p.ylen < n;
+  }
   p.est_us = csr_est_us(dev, p, m, n, nnz, elem);
   return p;
 }
 
 std::vector<CsrPlan> csr_candidates(const DeviceInfo& dev, const CsrPlan& model, int64_t m, int64_t n, int64_t nnz,
-                                    int elem) {
+                                    int elem, const CsrStats* st) {
   std::vector<CsrPlan> c{model};
   const int64_t budget = std::min<int64_t>(kSmemBudget, dev.smem_optin > 0 ? dev.smem_optin : 48 * 1024);
   const int64_t fixed = (int64_t)csr_rows_smem(0, 0, elem) + 32;
   const int64_t room = std::max<int64_t>(0, budget - fixed) / elem;
   // the split of shared memory between the scatter window and the copy of y
   if (n > room / 2) {
-    for (int eighths : {4, 7}) {
+    for (int eighths : {4, 6, 7}) {
       CsrPlan q = model;
       q.win_len = std::min<int64_t>(n, room * eighths / 8);
       q.ylen = std::min<int64_t>(n, room - q.win_len);
       if (q.win_len == model.win_len) continue;
       q.smem = csr_rows_smem(q.win_len, q.ylen, elem);
       q.long_smem = q.smem - csr_rows_smem(0, 0, elem);
+      if (st != nullptr && st->valid) place_sampled(q, *st, n);
       q.est_us = csr_est_us(dev, q, m, n, nnz, elem);
       c.push_back(q);
     }
@@ -305,12 +431,19 @@ int describe(const DensePlan& p, char* buf, size_t cap) {
 }
 
 int describe(const CsrPlan& p, char* buf, size_t cap) {
-  return snprintf(buf, cap,
-                  "csr group_lanes=%d group_entries=%d pack_k=%d pack_cap=%d warp_cap=%d ctas=%d threads=%d long_ctas=%d "
-                  "window=[%lld,+%lld) y_window=%lld smem=%zu queue_cap=%lld ws=%zu est_us=%.1f",
-                  p.group_lpr, p.group_kg, p.pack_k, p.pack_cap, p.warp_cap, p.ctas, p.threads, p.long_ctas,
-                  (long long)p.win_c0,
-                  (long long)p.win_len, (long long)p.ylen, p.smem, (long long)p.queue_cap, p.ws_bytes, p.est_us);
+  int w = snprintf(buf, cap,
+                   "csr group_lanes=%d group_entries=%d pack_k=%d pack_cap=%d warp_cap=%d ctas=%d threads=%d "
+                   "long_ctas=%d window=[%lld,+%lld) y_window=[%lld,+%lld) placement=%s smem=%zu queue_cap=%lld ws=%zu "
+                   "est_us=%.1f",
+                   p.group_lpr, p.group_kg, p.pack_k, p.pack_cap, p.warp_cap, p.ctas, p.threads, p.long_ctas,
+                   (long long)p.win_c0, (long long)p.win_len, (long long)p.y0, (long long)p.ylen,
+                   p.sampled ? "sampled" : (p.place_on_device ? "device" : "whole"), p.smem, (long long)p.queue_cap,
+                   p.ws_bytes, p.est_us);
+  if (p.sampled && w > 0 && (size_t)w < cap)
+    w += snprintf(buf + w, cap - (size_t)w,
+                  " mean_len=%.1f cv_len=%.2f p75_len=%lld long_share=%.3f win_hit=%.3f y_hit=%.3f", p.mean_len,
+                  p.cv_len, (long long)p.p75_len, p.long_share, p.win_hit, p.y_hit);
+  return w;
 }
 
 }  // namespace fxtx

@@ -198,6 +198,56 @@ fxtx_status_t fxtx_epilogue_f64(int64_t n, const double* w, double alpha, double
                                 void* stream);
 
 /*
+ * Input-data characteristics of a CSR matrix, read by the launch model ("On
+ * optimizing machine learning workloads via kernel fusion", abstract: the
+ * analytical model considers input data characteristics and the GPU's resources).
+ * All figures come from a strided sample of 8,192 row lengths and 8,192 column
+ * indices (positions spread evenly over the rows and over the entries).
+ */
+typedef struct {
+  int64_t row_samples, col_samples;  /* sampled rows and entries (min(m or nnz, 8192)) */
+  double mean_row_len, cv_row_len;   /* sampled row lengths: mean and coefficient of variation */
+  int64_t p50_row_len, p75_row_len, p90_row_len, max_sampled_row_len;
+  double long_row_share;             /* length-weighted share of sampled rows over 2,048 entries */
+  int64_t window_c0, window_len;     /* the columns the plan accumulates in shared memory */
+  int64_t y_c0, y_len;               /* the entries of y the plan copies to shared memory */
+  double window_hit_share, y_hit_share; /* sampled column indices falling in each */
+  int32_t group_lanes, group_entries;   /* fp64 lane groups (0 for fp32: packed batches) */
+} fxtx_csr_stats_t;
+
+/*
+ * Samples a CSR matrix on the device (row_ptr, col_idx: device pointers, as for
+ * fxtx_csr_f32/_f64) and records the statistics for later calls on the same
+ * matrix: a fxtx_csr_f32/_f64 call whose (current device, row_ptr, col_idx, m, n,
+ * nnz) match an analysed matrix plans from them (the fp64 lane groups are sized to
+ * the sampled 75th-percentile row, the shared-memory split between the scatter
+ * window and the copy of y is chosen, and both are placed, from the sampled
+ * columns). Without an analysis every call places the two windows itself, on the
+ * device, from its own sample of col_idx, so the call stays asynchronous. The
+ * statistics steer launch parameters only, never results; analyse again after
+ * changing a matrix in place, or clear. Synchronous on `stream` (one small kernel
+ * and two copies of 64 KB and 32 KB). is_f64 selects the element size the returned
+ * plan figures are for; `stats` may be NULL. Up to 64 analyses are kept (the oldest
+ * is dropped). Errors: FXTX_ERR_INVALID_ARG (sizes, NULL structure), FXTX_ERR_ALLOC,
+ * FXTX_ERR_CUDA, FXTX_ERR_UNSUPPORTED.
+ */
+fxtx_status_t fxtx_csr_analyze(int is_f64, int64_t m, int64_t n, int64_t nnz, const int64_t* row_ptr,
+                               const int32_t* col_idx, void* stream, fxtx_csr_stats_t* stats);
+/* Forgets every analysis. */
+fxtx_status_t fxtx_csr_analysis_clear(void);
+
+/*
+ * The plan the model picks for a CSR matrix given as HOST arrays (row_ptr: m + 1
+ * entries, col_idx: nnz entries), from the same sample positions as
+ * fxtx_csr_analyze. Host only, no device needed (without a GB300 current it plans
+ * for 152 SMs and 227 KB of shared memory). Writes the statistics to `stats` (may
+ * be NULL) and a NUL-terminated description of at most `cap` bytes to `buf` (may
+ * be NULL).
+ */
+fxtx_status_t fxtx_csr_plan_describe_host(int is_f64, int64_t m, int64_t n, int64_t nnz, const int64_t* row_ptr,
+                                          const int32_t* col_idx, fxtx_csr_stats_t* stats, char* buf, int64_t cap);
+
+/*
  * Checks a CSR structure on the device (row_ptr[0] == 0, non-decreasing,
  * row_ptr[m] == nnz, 0 <= col_idx < n). Synchronous: it waits for `stream`.
  * Returns FXTX_OK or FXTX_ERR_BAD_CSR (or an argument/CUDA error).
@@ -217,9 +267,11 @@ const char* fxtx_status_string(fxtx_status_t status);
 
 /*
  * The launch plan the analytical model picks for a dense or CSR call, for
- * logging and tests. Host only; nothing is launched. For CSR, row_ptr is not
- * read (the plan uses m, n and nnz only). Writes a NUL-terminated description
- * of at most `cap` bytes into `buf` and returns FXTX_OK.
+ * logging and tests. Host only; nothing is launched. For CSR this is the plan
+ * from the shape alone (m, n, nnz): the window placement is then left to each
+ * call's device-side sample ("placement=device"); fxtx_csr_plan_describe_host
+ * gives the plan that sampled statistics lead to. Writes a NUL-terminated
+ * description of at most `cap` bytes into `buf` and returns FXTX_OK.
  */
 fxtx_status_t fxtx_plan_describe(int is_csr, int is_f64, int64_t m, int64_t n, int64_t nnz,
                                   int64_t ld, char* buf, int64_t cap);

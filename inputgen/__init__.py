@@ -260,15 +260,21 @@ def csr_uniform(seed: int = 0, m: int = 4_000_000, n: int = 10_000, lam: float =
 
 
 def csr_powerlaw(seed: int = 0, m: int = 2_000_000, n: int = 1_000_000, mean_len: float = 100.0,
-                 cap: int = 50_000, len_s: float = 1.5, col_s: float = 1.1) -> Problem:
+                 cap: int = 50_000, len_s: float = 1.5, col_s: float = 1.1, col_offset: int = 0) -> Problem:
+    """Zipf row lengths and Zipf-skewed columns (rank r at column r - 1). ``col_offset``
+    rotates every column index by that many places (mod n), so the hottest columns sit
+    at [col_offset, ...) instead of [0, ...); the rows stay sorted up to the wrap."""
     d = np.float32
     cap = min(cap, n)
     lens, c = zipf_lengths(seed, m, len_s, cap, int(round(mean_len * m)), cap)
     rp = row_ptr_from_lengths(lens)
     col = csr_columns(seed, n, rp, col_s)
+    if col_offset:
+        col = ((col.astype(np.int64) + col_offset) % n).astype(np.int32)
     nnz = int(rp[-1])
     mu = lens.mean() if m else 0.0
-    return Problem("csr_f32_%dx%d_powerlaw" % (m, n), "csr", d, m, n, 1.0, 0.0,
+    name = "csr_f32_%dx%d_powerlaw" % (m, n) + ("_rot%d" % col_offset if col_offset else "")
+    return Problem(name, "csr", d, m, n, 1.0, 0.0,
                    row_ptr=rp, col_idx=col, vals=normal(seed, XSTREAM, nnz, d),
                    y=normal(seed, YSTREAM, n, d),
                    v=uniform(seed, VSTREAM, m, 0.0, 1.0, d), z=None,
