@@ -66,8 +66,11 @@ def test_csr_plans(dtype, elem):
         f = fields(fx.plan_describe("csr", dtype, m, n, nnz))
         where = (dtype, m, n, nnz, f)
         c0, wlen = f["window"].strip("[)").split(",+")
-        wlen, ylen = int(wlen), int(f["y_window"])
-        assert int(c0) == 0 and 0 <= wlen <= n and 0 <= ylen <= n, where
+        y0, ylen = f["y_window"].strip("[)").split(",+")
+        wlen, ylen = int(wlen), int(ylen)
+        assert int(c0) == 0 and int(y0) == 0 and 0 <= wlen <= n and 0 <= ylen <= n, where
+        # without a sample the windows are placed per call on the device, unless they cover every column
+        assert f["placement"] == ("whole" if wlen >= n and ylen >= n else "device"), where
         # window and copy of y share the dynamic shared memory
         assert int(f["smem"]) <= SMEM_LIMIT and (wlen + ylen) * elem <= int(f["smem"]), where
         assert 1 <= int(f["ctas"]) <= SMS and int(f["long_ctas"]) == SMS, where
