@@ -102,6 +102,8 @@ def dominant_kernel(p) -> str:
         return "csr_group_kernel" if int(f["group_lanes"]) > 0 else "csr_rows_kernel"
     desc = fx.plan_describe("dense", dtype_name(p), p.m, p.n, 0, p.ld)
     kind = dict(kv.split("=") for kv in desc.split()[1:] if "=" in kv)["kind"]
+    if kind == "wide" and dtype_name(p) == "f64":
+        return "dense_wide_f64_kernel"
     return {"tile_tma": "dense_tile_kernel", "narrow_tma": "dense_narrow_kernel", "narrow_direct": "dense_narrow_kernel",
             "wide": "dense_wide_kernel"}.get(kind, kind)
 

@@ -131,7 +131,8 @@ fxtx_status_t run_dense(const DensePlan& plan, DenseArgs<typename DenseT<TX>::T,
   if (ws) {
     a.ws = static_cast<double*>(ws);
     a.ticket = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + plan.ws_bytes - 128);
-    if (cudaMemsetAsync(a.ticket, 0, sizeof(unsigned), st) != cudaSuccess) {
+    const cudaError_t e = cudaMemsetAsync(a.ticket, 0, sizeof(unsigned), st);
+    if (e != cudaSuccess) {
       cudaGetLastError();
       cudaFreeAsync(ws, st);
       return FXTX_ERR_CUDA;
@@ -158,9 +159,13 @@ fxtx_status_t run_csr(const CsrPlan& plan, CsrArgs<T> a, cudaStream_t st) {
   if (s != FXTX_OK) return s;
   char* w = static_cast<char*>(ws);
   const size_t part_bytes = ((size_t)(plan.ctas + 1) * 8 + 127) / 128 * 128;
+  const size_t queue_bytes =
+      ((size_t)csr_long_buckets() * (size_t)std::max<int64_t>(plan.queue_cap, 1) * 8 + 127) / 128 * 128;
   a.part = reinterpret_cast<int64_t*>(w);
   a.queue = reinterpret_cast<int64_t*>(w + part_bytes);
   a.queue_cap = plan.queue_cap;
+  a.med_queue = reinterpret_cast<int64_t*>(w + part_bytes + queue_bytes);
+  a.med_cap = plan.med_cap;
   a.counters = reinterpret_cast<unsigned long long*>(w + plan.ws_bytes - 128);
   cudaError_t e = launch_csr<T>(plan, a, st);
   cudaFreeAsync(ws, st);

@@ -12,10 +12,12 @@
 //                         left idle by rows shorter than the warp); fp64: lane
 //                         groups of LPR lanes x 8 entries per row, which spend
 //                         fewer fp64 operations per entry
-//   medium (<= WARP_LONG) one warp per row, two passes (the second from L1/L2)
+//   medium (<= WARP_LONG) one warp per row, two passes (the second from L1/L2):
+//                         fp32 defers them to a queue that the long-row kernel
+//                         drains after its long rows; fp64 takes them in place
 //   long   (> WARP_LONG)  deferred to queues bucketed by length; in the long-row
-//                         kernel a group of 4 warps takes each row, longest
-//                         buckets first, two passes
+//                         kernel a group of threads (128 by default) takes each
+//                         row, longest buckets first, two passes
 // The y gathers of hot columns hit a copy of y[y0, y0 + ylen) in shared memory;
 // the two windows sit on the column ranges a sample of col_idx hits most.
 // Row dots of a packed batch are formed lane-locally per row segment, and each
@@ -54,12 +56,17 @@ template <typename T>
 __host__ __device__ constexpr int long_unroll() {
   return sizeof(T) == 4 ? 8 : 4;
 }
-constexpr int LONG_GROUP = 128;            // threads that share one long row
+// threads that share one long row, chosen by the plan (128, 256 or 512): 128 by default, the
+// fastest on the power-law workload (1,091 us per call against 1,113 at 256, 1,289 at 512 and
+// 2,491 at 1,024): more rows in flight hide the latency of the gathers, which outweighs the
+// pass-2 re-reads that fewer rows in flight would keep in L2
+constexpr int LONG_GROUP_DEFAULT = 128;
 constexpr int LONG_BUCKETS = 6;            // long-row queues: (2K, 4K], (4K, 8K], ... (32K, 64K], > 64K entries
 // per-warp scratch after the window: 32 row dots (double), 32 row scales (T), 33 row starts
 constexpr size_t WARP_SCRATCH = 32 * 8 + 32 * 8 + 33 * 8;
 
-// *p += a * b in shared memory (fp64: CAS loop around one FMA; fp32: native atomic).
+// *p += a * b in shared memory (fp64: CAS loop around one FMA, so the product folds into
+// the atomic and costs one fp64 instruction per attempt; fp32: native atomic).
 __device__ __forceinline__ void smem_fma_add(float* p, float a, float b) { atomicAdd(p, a * b); }
 __device__ __forceinline__ void smem_fma_add(double* p, double a, double b) {
   unsigned long long* q = reinterpret_cast<unsigned long long*>(p);
@@ -96,8 +103,8 @@ struct Window {
   }
 };
 
-// Workspace slots of the two window starts, written by the prologue.
-constexpr int SLOT_WIN_C0 = 8, SLOT_Y0 = 9;
+// Workspace slots of the two window starts, written by the prologue, and of the medium-row queue.
+constexpr int SLOT_WIN_C0 = 8, SLOT_Y0 = 9, SLOT_MED_COUNT = 10, SLOT_MED_CLAIM = 11;
 
 template <typename T>
 __device__ __forceinline__ Window<T> make_window(const CsrArgs<T>& a, T* acc, int64_t win_len, const T* ys,
@@ -126,13 +133,20 @@ __host__ __device__ constexpr size_t window_bytes(int64_t len, size_t elem) {
   return ((size_t)len * elem + 15) / 16 * 16;
 }
 
-// Defers row r (len > WARP_LONG entries) to the long-row queue of its length bucket.
+// Defers row r, too long for the row kernel's batches, to the long-row kernel: rows of more
+// than WARP_LONG entries to the queue of their length bucket (a group of threads each), the
+// others to the medium queue (a warp each, once the long rows are done).
 template <typename T>
-__device__ __forceinline__ void push_long(const CsrArgs<T>& a, int64_t r, int64_t len) {
-  const unsigned long long q = (unsigned long long)(len - 1) / WARP_LONG;  // >= 1
-  const int b = (int)tmin<unsigned long long>(LONG_BUCKETS - 1, 63 - __clzll((long long)q));
-  const unsigned long long k = atomicAdd(&a.counters[1 + b], 1ull);
-  a.queue[(int64_t)b * a.queue_cap + (int64_t)k] = r;
+__device__ __forceinline__ void defer_row(const CsrArgs<T>& a, int64_t r, int64_t len) {
+  if (len > WARP_LONG) {
+    const unsigned long long q = (unsigned long long)(len - 1) / WARP_LONG;  // >= 1
+    const int b = (int)tmin<unsigned long long>(LONG_BUCKETS - 1, 63 - __clzll((long long)q));
+    const unsigned long long k = atomicAdd(&a.counters[1 + b], 1ull);
+    a.queue[(int64_t)b * a.queue_cap + (int64_t)k] = r;
+  } else {
+    const unsigned long long k = atomicAdd(&a.counters[SLOT_MED_COUNT], 1ull);
+    a.med_queue[k] = r;
+  }
 }
 
 }  // namespace
@@ -146,6 +160,7 @@ int csr_pack_cap(int elem) { return elem == 4 ? Pack<float>::CAP : Pack<double>:
 int csr_warp_long() { return WARP_LONG; }
 int csr_group_threads() { return CSR_GROUP_THREADS; }
 int csr_long_buckets() { return LONG_BUCKETS; }
+int csr_long_group_default() { return LONG_GROUP_DEFAULT; }
 
 constexpr int PROLOGUE_THREADS = 256;
 
@@ -271,6 +286,10 @@ __global__ void __launch_bounds__(PROLOGUE_THREADS)
     a.part[p] = r;
   }
   if (tid < LONG_BUCKETS + 2) a.counters[tid] = 0ull;
+  if (tid == 0) {
+    a.counters[SLOT_MED_COUNT] = 0ull;
+    a.counters[SLOT_MED_CLAIM] = 0ull;
+  }
   if (blockIdx.x == 0) {
     if (place) {
       place_windows(a, win_len, ylen);
@@ -461,18 +480,17 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
       b0 = b1;
     }
 
-    // rows longer than a packed batch: one warp each, or the long-row queue
-    unsigned lm = __ballot_sync(FULL_MASK, hasrow && !isshort);
-    while (lm) {
-      const int j = __ffs(lm) - 1;
-      lm &= lm - 1;
-      const int64_t s2 = __shfl_sync(FULL_MASK, rs, j), e2 = __shfl_sync(FULL_MASK, rend, j);
-      const T vj = __shfl_sync(FULL_MASK, vrow, j);
-      if (e2 - s2 > WARP_LONG) {
-        if (lane == 0) push_long(a, r0 + j, e2 - s2);
-      } else {
-        warp_row(a, win, vj, s2, e2, alpha, lane);
-      }
+    // rows longer than a packed batch go to the long-row kernel's queues: the medium ones of the
+    // window with one atomic for the warp (the counter is shared by every warp of the grid)
+    if (hasrow && len > WARP_LONG) defer_row(a, r0 + lane, len);
+    const bool med = hasrow && !isshort && len <= WARP_LONG;
+    const unsigned mm = __ballot_sync(FULL_MASK, med);
+    if (mm) {
+      const int leader = __ffs(mm) - 1;
+      unsigned long long base = 0;
+      if (lane == leader) base = atomicAdd(&a.counters[SLOT_MED_COUNT], (unsigned long long)__popc(mm));
+      base = __shfl_sync(FULL_MASK, base, leader);
+      if (med) a.med_queue[base + (unsigned long long)__popc(mm & ((1u << lane) - 1u))] = r0 + lane;
     }
     __syncwarp();  // rsb reuse
   }
@@ -532,7 +550,8 @@ __global__ void __launch_bounds__(CSR_GROUP_THREADS, 1)
     for (int k = 0; k < KG; ++k)
       if (col[k] >= 0) win.add(col[k], ts, val[k]);
 
-    // longer rows: one warp each, or the long-row queue
+    // longer rows: one warp each, here (rows of similar length rarely outgrow a group, and each
+    // deferral would cost an atomic on one shared counter), or the long-row queue
     unsigned lm = __ballot_sync(FULL_MASK, has && !small && q == 0);
     while (lm) {
       const int src = __ffs(lm) - 1;
@@ -540,7 +559,7 @@ __global__ void __launch_bounds__(CSR_GROUP_THREADS, 1)
       const int64_t rr = __shfl_sync(FULL_MASK, r, src);
       const int64_t s2 = __shfl_sync(FULL_MASK, st, src), e2 = __shfl_sync(FULL_MASK, en, src);
       if (e2 - s2 > WARP_LONG) {
-        if (lane == 0) push_long(a, rr, e2 - s2);
+        if (lane == 0) defer_row(a, rr, e2 - s2);
       } else {
         warp_row(a, win, a.v ? ldg(a.v + rr) : T(1), s2, e2, alpha, lane);
       }
@@ -550,7 +569,7 @@ __global__ void __launch_bounds__(CSR_GROUP_THREADS, 1)
   window_flush(wacc, win.c0, win_len, a.out);
 }
 
-// Rows longer than WARP_LONG: each group of LONG_GROUP threads takes queued rows
+// Rows longer than WARP_LONG: each group of G threads takes queued rows
 // one at a time, with one group barrier per row. Rows are claimed from one global
 // counter that walks the length buckets from the longest down, so the longest
 // rows start first and short ones fill in at the end. A group rather than a warp
@@ -559,12 +578,12 @@ __global__ void __launch_bounds__(CSR_GROUP_THREADS, 1)
 // while the current batch is used. The next row's index is claimed while the
 // current one is processed, and the per-warp partial dots are double-buffered by
 // row parity, so the single barrier orders both.
-template <typename T>
+template <typename T, int G>
 __device__ __forceinline__ void long_batch(const CsrArgs<T>& a, int64_t b, int64_t en, T* xv, int32_t* xc) {
   constexpr int U = long_unroll<T>();
 #pragma unroll
   for (int k = 0; k < U; ++k) {
-    const int64_t idx = b + (int64_t)k * LONG_GROUP;
+    const int64_t idx = b + (int64_t)k * G;
     const bool ok = idx < en;
     xv[k] = ok ? ldg(a.vals + idx) : T(0);
     xc[k] = ok ? ldg(a.col_idx + idx) : -1;
@@ -576,14 +595,14 @@ __device__ __forceinline__ void group_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
-template <typename T>
+template <typename T, int G>
 __global__ void __launch_bounds__(CSR_THREADS, 1)
     csr_long_kernel(const CsrArgs<T> a, const int64_t win_len, const int64_t ylen) {
   constexpr int U = long_unroll<T>();
-  constexpr int GW = LONG_GROUP / 32;           // warps per group
-  constexpr int NG = CSR_THREADS / LONG_GROUP;  // groups per CTA (named barriers 1 .. NG)
-  static_assert(NG <= 15, "named barrier ids");
-  constexpr int64_t STEP = (int64_t)LONG_GROUP * U;
+  constexpr int GW = G / 32;           // warps per group
+  constexpr int NG = CSR_THREADS / G;  // groups per CTA (named barriers 1 .. NG)
+  static_assert(NG >= 1 && NG <= 15 && CSR_THREADS % G == 0, "named barrier ids");
+  constexpr int64_t STEP = (int64_t)G * U;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ long long s_row[NG][2];
   __shared__ double s_red[NG][2][GW];
@@ -591,7 +610,7 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
   const T* ys = reinterpret_cast<const T*>(smem + window_bytes(win_len, sizeof(T)));
   const Window<T> win = make_window(a, wacc, win_len, ys, ylen);
   const int lane = threadIdx.x & 31;
-  const int grp = threadIdx.x / LONG_GROUP, gt = threadIdx.x % LONG_GROUP, gw = gt >> 5;
+  const int grp = threadIdx.x / G, gt = threadIdx.x % G, gw = gt >> 5;
   const int bar = 1 + grp;
   const T alpha = (T)a.alpha;
   auto claim = [&]() -> long long {
@@ -618,11 +637,11 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
     DotAcc<T, sizeof(T) == 4> d;
     T xv[U];
     int32_t xc[U];
-    long_batch(a, st + gt, en, xv, xc);
+    long_batch<T, G>(a, st + gt, en, xv, xc);
     for (int64_t b = st + gt; b < en; b += STEP) {
       T nv[U];
       int32_t nc[U];
-      long_batch(a, b + STEP, en, nv, nc);
+      long_batch<T, G>(a, b + STEP, en, nv, nc);
       T yv[U];
 #pragma unroll
       for (int k = 0; k < U; ++k) yv[k] = xc[k] >= 0 ? win.yat(xc[k]) : T(0);
@@ -635,7 +654,7 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
     }
     d.template group_reduce<32>();
     if (lane == 0) s_red[grp][cur][gw] = d.value_f64();
-    group_barrier(bar, LONG_GROUP);
+    group_barrier(bar, G);
     double u = 0.0;
 #pragma unroll
     for (int w = 0; w < GW; ++w) u += s_red[grp][cur][w];
@@ -643,17 +662,33 @@ __global__ void __launch_bounds__(CSR_THREADS, 1)
     const T ts = alpha * (vi * (T)u);
 
     // pass 2: the scatter, re-reading the row (served by L2)
-    long_batch(a, st + gt, en, xv, xc);
+    long_batch<T, G>(a, st + gt, en, xv, xc);
     for (int64_t b = st + gt; b < en; b += STEP) {
       T nv[U];
       int32_t nc[U];
-      long_batch(a, b + STEP, en, nv, nc);
+      long_batch<T, G>(a, b + STEP, en, nv, nc);
 #pragma unroll
       for (int k = 0; k < U; ++k) {
         if (xc[k] >= 0) win.add(xc[k], ts, xv[k]);
         xv[k] = nv[k];
         xc[k] = nc[k];
       }
+    }
+  }
+  // then the medium rows (longer than the row kernel's batches, at most WARP_LONG entries):
+  // one warp each, claimed one at a time, so the last rows of the call spread over every warp
+  // (claims of 4 rows were measured 2 % slower on the power-law workload)
+  constexpr unsigned long long MED_CLAIM = 1;
+  const unsigned long long nmed = a.counters[SLOT_MED_COUNT];
+  for (;;) {
+    unsigned long long k0 = 0;
+    if (lane == 0) k0 = atomicAdd(&a.counters[SLOT_MED_CLAIM], MED_CLAIM);
+    k0 = __shfl_sync(FULL_MASK, k0, 0);
+    if (k0 >= nmed) break;
+    const unsigned long long k1 = tmin(nmed, k0 + MED_CLAIM);
+    for (unsigned long long k = k0; k < k1; ++k) {
+      const int64_t r = a.med_queue[k];
+      warp_row(a, win, a.v ? ldg(a.v + r) : T(1), a.row_ptr[r], a.row_ptr[r + 1], alpha, lane);
     }
   }
   __syncthreads();
@@ -666,6 +701,14 @@ static cudaError_t launch_group(const CsrPlan& p, const CsrArgs<T>& a, cudaStrea
   const cudaError_t e = ensure_smem((const void*)csr_group_kernel<T, LPR, KG>, p.long_smem);
   if (e != cudaSuccess) return e;
   csr_group_kernel<T, LPR, KG><<<p.ctas, p.threads, p.long_smem, st>>>(a, p.win_len, p.ylen);
+  return cudaGetLastError();
+}
+
+template <typename T, int G>
+static cudaError_t launch_long(const CsrPlan& p, const CsrArgs<T>& a, cudaStream_t st) {
+  const cudaError_t e = ensure_smem((const void*)csr_long_kernel<T, G>, p.long_smem);
+  if (e != cudaSuccess) return e;
+  csr_long_kernel<T, G><<<p.long_ctas, p.long_threads, p.long_smem, st>>>(a, p.win_len, p.ylen);
   return cudaGetLastError();
 }
 
@@ -701,10 +744,13 @@ cudaError_t launch_csr(const CsrPlan& p, const CsrArgs<T>& a, cudaStream_t st) {
   }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = ensure_smem((const void*)csr_long_kernel<T>, p.long_smem);
-  if (e != cudaSuccess) return e;
-  csr_long_kernel<T><<<p.long_ctas, p.long_threads, p.long_smem, st>>>(a, p.win_len, p.ylen);
-  return cudaGetLastError();
+  switch (p.long_group) {
+    case 128: return launch_long<T, 128>(p, a, st);
+    case 256: return launch_long<T, 256>(p, a, st);
+    case 512: return launch_long<T, 512>(p, a, st);
+    case 1024: return launch_long<T, 1024>(p, a, st);
+    default: return cudaErrorInvalidConfiguration;
+  }
 }
 
 template cudaError_t launch_csr<float>(const CsrPlan&, const CsrArgs<float>&, cudaStream_t);

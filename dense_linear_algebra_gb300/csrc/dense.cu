@@ -593,6 +593,132 @@ __global__ void __launch_bounds__(WIDE_THREADS) dense_wide_kernel(const DenseArg
     for (int64_t j = threadIdx.x; j < n; j += blockDim.x) a.ws[(int64_t)blockIdx.x * n + j] = acc[j];
 }
 
+// fp64 wide rows, software-pipelined. The fp64 units (2 FMAs per clock per SM on GB300)
+// bind this kernel: every element costs two fp64 FMAs, one in the row dot and one in the
+// scatter. One sweep over the columns forms the dots of step k + 1 (rows from HBM) and
+// scatters step k (the same rows re-read, from L2, into the CTA's fp64 column sums in
+// shared memory), so the FMAs of both passes interleave in one instruction stream and
+// the memory latency of each hides behind the other's arithmetic; one CTA barrier per
+// step turns the dots into the next t_i. Rows stay live for two steps: at the plan's R = 8
+// (152 CTAs x 16 rows x 160 KB for n = 20,000) the re-reads exceed L2 and partly return to
+// HBM, which has the bandwidth to spare while the fp64 units bind; R = 2 keeps them in L2
+// but leaves too few independent FMA chains per thread.
+template <int R, bool VEC>
+__global__ void __launch_bounds__(WIDE_THREADS) dense_wide_f64_kernel(const DenseArgs<double> a, const bool smem_acc) {
+  constexpr int NWARP = WIDE_THREADS / 32;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ double s_dot[R][NWARP];
+  __shared__ double s_t[2][R];
+
+  const int64_t n = a.n, ld = a.ld;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  double* acc = smem_acc ? reinterpret_cast<double*>(smem) : a.ws + (int64_t)blockIdx.x * n;
+  for (int64_t j = threadIdx.x; j < n; j += blockDim.x) acc[j] = 0.0;
+
+  const int64_t r_begin = a.m * blockIdx.x / gridDim.x, r_end = a.m * (blockIdx.x + 1) / gridDim.x;
+  const int64_t nvec = VEC ? n / 2 : 0;  // whole 16-byte chunks per row (VEC: rows start 16-byte aligned)
+
+  // the dots of the R rows from i0 (rows of them real) reduced over the CTA into t = v_i u_i,
+  // written to buffer b; ends with a barrier
+  auto finish_dots = [&](double* d, int64_t i0, int rows, int b) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const double v = group_sum<32>(d[r]);
+      if (lane == 0) s_dot[r][warp] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x < R) {
+      const int r = threadIdx.x;
+      double u = 0.0;
+      for (int w = 0; w < NWARP; ++w) u += s_dot[r][w];
+      const double vi = (r < rows && a.v) ? a.v[i0 + r] : 1.0;
+      s_t[b][r] = r < rows ? vi * u : 0.0;
+    }
+    __syncthreads();
+  };
+
+  // step 0: its dots alone
+  {
+    const int rows = (int)tmax<int64_t>(0, tmin<int64_t>(R, r_end - r_begin));
+    double d[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) d[r] = 0.0;
+    for (int64_t c = threadIdx.x; c < nvec; c += blockDim.x) {
+      const double2 yv = *reinterpret_cast<const double2*>(a.y + 2 * c);
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+        if (r < rows) {
+          const double2 xv = *reinterpret_cast<const double2*>(a.X + (r_begin + r) * ld + 2 * c);
+          d[r] = fma(xv.y, yv.y, fma(xv.x, yv.x, d[r]));
+        }
+    }
+    for (int64_t j = nvec * 2 + threadIdx.x; j < n; j += blockDim.x) {
+      const double yj = a.y[j];
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+        if (r < rows) d[r] = fma(a.X[(r_begin + r) * ld + j], yj, d[r]);
+    }
+    finish_dots(d, r_begin, rows, 0);  // its first barrier also orders the zeroing of acc
+  }
+
+  for (int k = 0;; ++k) {
+    const int b = k & 1;
+    const int64_t i0 = r_begin + (int64_t)k * R;
+    if (i0 >= r_end) break;
+    const int rows = (int)tmin<int64_t>(R, r_end - i0);
+    const int64_t i1 = i0 + R;  // the next step, whose dots this sweep forms
+    const int rows1 = (int)tmax<int64_t>(0, tmin<int64_t>(R, r_end - i1));
+    double t[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) t[r] = s_t[b][r];
+    double d[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) d[r] = 0.0;
+    for (int64_t c = threadIdx.x; c < nvec; c += blockDim.x) {
+      // the next step's dots (rows from HBM) ...
+      if (rows1 > 0) {
+        const double2 yv = *reinterpret_cast<const double2*>(a.y + 2 * c);
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+          if (r < rows1) {
+            const double2 xv = *reinterpret_cast<const double2*>(a.X + (i1 + r) * ld + 2 * c);
+            d[r] = fma(xv.y, yv.y, fma(xv.x, yv.x, d[r]));
+          }
+      }
+      // ... and this step's scatter (rows from L2): the FMA chain starts from the column sum
+      // (read as two doubles: in global memory a CTA's sums start 8-byte aligned for odd n)
+      double s0 = acc[2 * c], s1 = acc[2 * c + 1];
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+        if (r < rows) {
+          const double2 xv = *reinterpret_cast<const double2*>(a.X + (i0 + r) * ld + 2 * c);
+          s0 = fma(t[r], xv.x, s0);
+          s1 = fma(t[r], xv.y, s1);
+        }
+      acc[2 * c] = s0;
+      acc[2 * c + 1] = s1;
+    }
+    for (int64_t j = nvec * 2 + threadIdx.x; j < n; j += blockDim.x) {
+      if (rows1 > 0) {
+        const double yj = a.y[j];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+          if (r < rows1) d[r] = fma(a.X[(i1 + r) * ld + j], yj, d[r]);
+      }
+      double s = acc[j];
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+        if (r < rows) s = fma(t[r], a.X[(i0 + r) * ld + j], s);
+      acc[j] = s;
+    }
+    if (rows1 > 0) finish_dots(d, i1, rows1, b ^ 1);  // uniform across the CTA
+  }
+  if (smem_acc) {
+    __syncthreads();
+    for (int64_t j = threadIdx.x; j < n; j += blockDim.x) a.ws[(int64_t)blockIdx.x * n + j] = acc[j];
+  }
+}
+
 // Fixed-order sum of per-CTA column partials [nc][n], then out = alpha * w + beta * z.
 template <typename T>
 __global__ void __launch_bounds__(256) reduce_partials_kernel(const DenseArgs<T> a, const int nc) {
@@ -722,6 +848,31 @@ static cudaError_t launch_tile(const DensePlan& p, const DenseArgs<typename Stor
   }
 }
 
+template <int R>
+static cudaError_t launch_wide_f64_r(const DensePlan& p, const DenseArgs<double>& a, bool vec, cudaStream_t st) {
+  const void* k = vec ? (const void*)dense_wide_f64_kernel<R, true> : (const void*)dense_wide_f64_kernel<R, false>;
+  cudaError_t e = ensure_smem(k, p.smem);
+  if (e != cudaSuccess) return e;
+  if (vec)
+    dense_wide_f64_kernel<R, true><<<p.ctas, WIDE_THREADS, p.smem, st>>>(a, p.smem_acc);
+  else
+    dense_wide_f64_kernel<R, false><<<p.ctas, WIDE_THREADS, p.smem, st>>>(a, p.smem_acc);
+  return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t launch_wide_f64(const DensePlan& p, const DenseArgs<T>& a, bool vec, cudaStream_t st) {
+  if constexpr (sizeof(T) == 8) {
+    switch (p.rows_per_tile) {
+      case 2: return launch_wide_f64_r<2>(p, a, vec, st);
+      case 4: return launch_wide_f64_r<4>(p, a, vec, st);
+      case 8: return launch_wide_f64_r<8>(p, a, vec, st);
+      default: return cudaErrorInvalidConfiguration;
+    }
+  }
+  return cudaErrorInvalidConfiguration;
+}
+
 template <typename T>
 cudaError_t launch_dense(const DensePlan& p, const DenseArgs<T>& a, cudaStream_t st) {
   switch (p.kind) {
@@ -752,6 +903,12 @@ cudaError_t launch_dense(const DensePlan& p, const DenseArgs<T>& a, cudaStream_t
     case DENSE_WIDE: {
       const bool vec = (reinterpret_cast<uintptr_t>(a.X) % 16 == 0) && (reinterpret_cast<uintptr_t>(a.y) % 16 == 0) &&
                        ((a.ld * (int64_t)sizeof(T)) % 16 == 0);
+      if constexpr (sizeof(T) == 8) {
+        cudaError_t e = launch_wide_f64(p, a, vec, st);
+        if (e != cudaSuccess) return e;
+        reduce_partials_kernel<T><<<(unsigned)((a.n + 31) / 32), 256, 0, st>>>(a, p.ctas);
+        return cudaGetLastError();
+      }
       const void* k = vec ? (const void*)dense_wide_kernel<T, true> : (const void*)dense_wide_kernel<T, false>;
       cudaError_t e = ensure_smem(k, p.smem);
       if (e != cudaSuccess) return e;

@@ -49,7 +49,10 @@ struct CsrArgs {
   int64_t* part = nullptr;       // [ctas + 1] row partition of the row-group kernel
   int64_t* queue = nullptr;      // [buckets][queue_cap] rows deferred to the long-row kernel, by length
   int64_t queue_cap = 0;
-  // [0] long-row claims, [1 .. buckets] bucket lengths, [buckets + 1] row windows handed out
+  int64_t* med_queue = nullptr;  // [med_cap] rows too long for the row kernel's batches, taken one warp each
+  int64_t med_cap = 0;
+  // [0] long-row claims, [1 .. buckets] bucket lengths, [buckets + 1] row windows handed out,
+  // [8], [9] the window starts, [10] medium rows queued, [11] medium rows claimed
   unsigned long long* counters = nullptr;
 };
 

@@ -54,7 +54,8 @@ double dense_est_us(const DeviceInfo& dev, const DensePlan& p, int64_t m, int64_
   const int ce = elem == 2 ? 4 : elem;  // compute-type bytes of the vectors
   const double bytes = (double)m * n * elem + (double)m * ce + 3.0 * n * ce;
   static const double hbm_eff[] = {1.0, 1.0, 0.85, 0.5, 0.9, 0.99};  // by DenseKind
-  return roofline_us(dev, bytes, hbm_eff[p.kind], 2.0 * m * n, elem == 2 ? 4 : elem, 0.7, 0.0, 1.0);
+  const double fmas = 2.0 * m * n;
+  return roofline_us(dev, bytes, hbm_eff[p.kind], fmas, elem == 2 ? 4 : elem, 0.7, 0.0, 1.0);
 }
 
 // CSR call: vals and col_idx once, row_ptr, v, y, z and out; two FMAs per entry; a
@@ -90,6 +91,19 @@ bool narrow_shape(int64_t chunks, int* lpr, int* vpl) {
     return false;
   }
   return true;
+}
+
+// Workspace of the wide kernels: [ctas][n] fp64 column partials (which are also the column
+// sums when these do not fit shared memory); the ticket word last.
+static size_t wide_ws_bytes(const DensePlan& p, int64_t n, int elem) {
+  (void)elem;
+  return align128((size_t)p.ctas * n * sizeof(double)) + 128;
+}
+
+static void set_wide_grid(const DeviceInfo& dev, DensePlan& p, int64_t m, int64_t n, int elem) {
+  (void)n;
+  (void)elem;
+  p.ctas = (int)std::max<int64_t>(1, std::min<int64_t>(dev.sm_count, cdiv(m, p.rows_per_tile)));
 }
 
 static DensePlan plan_dense_model(const DeviceInfo& dev, int64_t m, int64_t n, int64_t ld, int elem, bool tma_ok,
@@ -172,14 +186,16 @@ static DensePlan plan_dense_model(const DeviceInfo& dev, int64_t m, int64_t n, i
     p.ws_bytes = align128((size_t)p.ctas * n * sizeof(double)) + 128;
     return p;
   }
-  // wide rows
+  // wide rows: 8 rows coarsened per step (fp64 on 20,000 x 20,000: 1,603 us per call against
+  // 2,331 at 4 and 2,034 at 2 rows; the dots' independent FMA chains matter more than keeping
+  // the re-read rows in L2, since the fp64 units, not HBM, bind)
   p.kind = DENSE_WIDE;
   p.warps = 16;
-  p.rows_per_tile = 8;  // rows the wide kernel coarsens per step (WIDE_R)
-  p.ctas = (int)std::max<int64_t>(1, std::min<int64_t>(dev.sm_count, cdiv(m, 8)));
+  p.rows_per_tile = 8;
+  set_wide_grid(dev, p, m, n, elem);
   p.smem_acc = (int64_t)(n * sizeof(double)) <= budget;
   p.smem = p.smem_acc ? (size_t)n * sizeof(double) : 0;
-  p.ws_bytes = align128((size_t)p.ctas * n * sizeof(double)) + 128;
+  p.ws_bytes = wide_ws_bytes(p, n, elem);
   return p;
 }
 
@@ -211,12 +227,25 @@ std::vector<DensePlan> dense_candidates(const DeviceInfo& dev, const DensePlan& 
         q.est_us = dense_est_us(dev, q, m, n, elem);
         c.push_back(q);
       }
-  } else if (model.kind == DENSE_WIDE && model.smem_acc) {
+  } else if (model.kind == DENSE_WIDE) {
+    // fp64: rows per step (fewer keeps more of the re-read in L2, more amortises the dot reduction)
+    if (elem == 8)
+      for (int r : {2, 4}) {
+        DensePlan q = model;
+        q.rows_per_tile = r;
+        set_wide_grid(dev, q, m, n, elem);
+        q.ws_bytes = wide_ws_bytes(q, n, elem);
+        q.est_us = dense_est_us(dev, q, m, n, elem);
+        c.push_back(q);
+      }
     // the column accumulator in global memory instead of shared memory
-    DensePlan q = model;
-    q.smem_acc = false;
-    q.smem = 0;
-    c.push_back(q);
+    if (model.smem_acc) {
+      DensePlan q = model;
+      q.smem_acc = false;
+      q.smem = 0;
+      q.ws_bytes = wide_ws_bytes(q, n, elem);
+      c.push_back(q);
+    }
   }
   return c;
 }
@@ -296,6 +325,18 @@ int64_t csr_place_window(const CsrStats& st, int64_t n, int64_t len, int* hits) 
 
 namespace {
 
+// Workspace of a CSR call: the row partition, the long-row queues, the medium-row queue
+// (rows longer than a short-row batch or lane group, at most the one-warp limit) and the
+// counters.
+void csr_set_ws(CsrPlan& p, int64_t m, int64_t nnz) {
+  const int64_t batch = p.group_lpr > 0 ? (int64_t)p.group_lpr * p.group_kg : (int64_t)p.pack_cap;
+  p.queue_cap = std::min<int64_t>(m, nnz / (p.warp_cap + 1) + 1);
+  p.med_cap = std::min<int64_t>(m, nnz / (batch + 1) + 1);
+  p.ws_bytes = align128((size_t)(p.ctas + 1) * 8) +
+               align128((size_t)csr_long_buckets() * std::max<int64_t>(p.queue_cap, 1) * 8) +
+               align128((size_t)std::max<int64_t>(p.med_cap, 1) * 8) + 128;
+}
+
 // Fills the window placement of p from the sample (win_len and ylen already set).
 void place_sampled(CsrPlan& p, const CsrStats& st, int64_t n) {
   int hw = 0, hy = 0;
@@ -336,6 +377,7 @@ CsrPlan plan_csr(const DeviceInfo& dev, int64_t m, int64_t n, int64_t nnz, int e
   // buffers from spilling; 1,399 against 1,441 us on rows of Poisson(50) entries)
   p.threads = p.group_lpr > 0 ? csr_group_threads() : kCsrThreads;
   p.long_threads = kCsrThreads;
+  p.long_group = csr_long_group_default();
   const int64_t budget = std::min<int64_t>(kSmemBudget, dev.smem_optin > 0 ? dev.smem_optin : 48 * 1024);
   const int64_t fixed = (int64_t)csr_rows_smem(0, 0, elem) + 32;  // per-warp scratch of the row kernel + padding
   p.ctas = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)dev.sm_count, cdiv(std::max<int64_t>(m, 1), 1024)));
@@ -347,9 +389,7 @@ CsrPlan plan_csr(const DeviceInfo& dev, int64_t m, int64_t n, int64_t nnz, int e
   // ¾ only for a gain of at least kSplitGain of the sampled entries (sampling noise)
   const int64_t room = std::max<int64_t>(0, budget - fixed) / elem;
   p.row_cost = 8;
-  p.queue_cap = std::min<int64_t>(m, nnz / (p.warp_cap + 1) + 1);
-  p.ws_bytes = align128((size_t)(p.ctas + 1) * 8) +
-               align128((size_t)csr_long_buckets() * std::max<int64_t>(p.queue_cap, 1) * 8) + 128;
+  csr_set_ws(p, m, nnz);
   auto set_split = [&](CsrPlan& q, int eighths) {
     q.win_len = std::min<int64_t>(n, room * eighths / 8);
     q.ylen = std::min<int64_t>(n, room - q.win_len);
@@ -404,6 +444,13 @@ std::vector<CsrPlan> csr_candidates(const DeviceInfo& dev, const CsrPlan& model,
       c.push_back(q);
     }
   }
+  // threads sharing one long row (only when the matrix can have rows past the one-warp limit)
+  if (nnz > model.warp_cap)
+    for (int g : {256, 512}) {
+      CsrPlan q = model;
+      q.long_group = g;
+      c.push_back(q);
+    }
   // fp64 lane groups: the same capacity with 8 entries a lane, and one size wider
   if (model.group_lpr > 0) {
     const int cap = model.group_lpr * model.group_kg;
@@ -414,6 +461,7 @@ std::vector<CsrPlan> csr_candidates(const DeviceInfo& dev, const CsrPlan& model,
         CsrPlan q = model;
         q.group_lpr = lpr;
         q.group_kg = kg;
+        csr_set_ws(q, m, nnz);
         c.push_back(q);
       }
     }
@@ -433,9 +481,10 @@ int describe(const DensePlan& p, char* buf, size_t cap) {
 int describe(const CsrPlan& p, char* buf, size_t cap) {
   int w = snprintf(buf, cap,
                    "csr group_lanes=%d group_entries=%d pack_k=%d pack_cap=%d warp_cap=%d ctas=%d threads=%d "
-                   "long_ctas=%d window=[%lld,+%lld) y_window=[%lld,+%lld) placement=%s smem=%zu queue_cap=%lld ws=%zu "
-                   "est_us=%.1f",
+                   "long_ctas=%d long_group=%d window=[%lld,+%lld) y_window=[%lld,+%lld) placement=%s smem=%zu "
+                   "queue_cap=%lld ws=%zu est_us=%.1f",
                    p.group_lpr, p.group_kg, p.pack_k, p.pack_cap, p.warp_cap, p.ctas, p.threads, p.long_ctas,
+                   p.long_group,
                    (long long)p.win_c0, (long long)p.win_len, (long long)p.y0, (long long)p.ylen,
                    p.sampled ? "sampled" : (p.place_on_device ? "device" : "whole"), p.smem, (long long)p.queue_cap,
                    p.ws_bytes, p.est_us);

@@ -111,6 +111,7 @@ struct CsrPlan {
   int warp_cap = 0;         // longest row one warp takes; longer rows go to the long-row kernel
   int ctas = 0, threads = 0;            // row kernel
   int long_ctas = 0, long_threads = 0;  // long-row kernel
+  int long_group = 0;                   // threads sharing one long row (128, 256, 512 or 1024)
   int64_t win_c0 = 0, win_len = 0;      // columns accumulated in shared memory
   int64_t y0 = 0, ylen = 0;             // y[y0, y0 + ylen) held in shared memory for the gathers
   bool place_on_device = false;         // the prologue places both windows from its own column sample
@@ -120,7 +121,8 @@ struct CsrPlan {
   size_t smem = 0, long_smem = 0;
   int row_cost = 0;         // nnz-equivalent cost of one row, for the partition
   size_t ws_bytes = 0;
-  int64_t queue_cap = 0;    // capacity of the long-row queue
+  int64_t queue_cap = 0;    // capacity of each long-row queue
+  int64_t med_cap = 0;      // capacity of the medium-row queue (rows past the short-row batches)
   double est_us = 0.0;      // the model's estimate of the call's duration
 };
 
@@ -132,6 +134,7 @@ int csr_pack_cap(int elem);
 int csr_warp_long();
 int csr_group_threads();  // block size of the lane-group kernel
 int csr_long_buckets();  // length buckets of the long-row queue
+int csr_long_group_default();  // threads sharing one long row unless a candidate says otherwise
 
 // The CSR plan from the shape alone (st == nullptr: both windows are then placed on the
 // device, per call, from a column sample), or from sampled statistics of the matrix.

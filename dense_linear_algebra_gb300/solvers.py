@@ -17,7 +17,8 @@ textbook consumers of ``alpha * X^T (v * (X p)) + beta * z``:
 X may be dense (a 2-D CUDA tensor) or CSR (a tuple ``(row_ptr, col_idx, vals, n)``).
 The few operations outside the pattern (``X^T b`` once, and per Newton step the
 margins ``X w`` and the gradient ``X^T (mu - b)``) are plain matrix-vector products
-done by torch; vector updates on n-vectors are torch operations as well.
+done by torch (for CSR X on torch CSR copies built once per solve); vector updates on
+n-vectors are torch operations as well.
 """
 from __future__ import annotations
 
@@ -52,18 +53,32 @@ def _torch_csr(X):
     return torch.sparse_csr_tensor(row_ptr, col_idx.to(torch.int64), vals, size=(row_ptr.shape[0] - 1, n))
 
 
+class TorchOps:
+    """X w and X^T r outside the pattern (torch). For CSR X the torch CSR tensor and its
+    transposed copy are built once, when the operator is made, not per product."""
+
+    def __init__(self, X):
+        if _is_csr(X):
+            self.A = _torch_csr(X)
+            self.AT = self.A.t().to_sparse_csr()
+        else:
+            self.A, self.AT = X, X.t()
+
+    def matvec(self, w):
+        return torch.mv(self.A, w)
+
+    def rmatvec(self, r):
+        return torch.mv(self.AT, r)
+
+
 def matvec(X, w):
     """X w (outside the pattern; torch)."""
-    if _is_csr(X):
-        return torch.mv(_torch_csr(X), w)
-    return torch.mv(X, w)
+    return TorchOps(X).matvec(w) if _is_csr(X) else torch.mv(X, w)
 
 
 def rmatvec(X, r):
     """X^T r (outside the pattern; torch)."""
-    if _is_csr(X):
-        return torch.mv(_torch_csr(X).t().to_sparse_csr(), r)
-    return torch.mv(X.t(), r)
+    return TorchOps(X).rmatvec(r) if _is_csr(X) else torch.mv(X.t(), r)
 
 
 @dataclass
@@ -185,12 +200,13 @@ def logistic_newton_cg(X, labels, lam: float, newton_steps: int = 20, tol: float
     product X^T (D * (X p)) + lam p, D = mu (1 - mu), is one fused call with v = D.
     """
     m, n, dt, dev = _shape(X)
+    ops = TorchOps(X)  # the margins' and the gradient's products; CSR copies built once per solve
     w = torch.zeros(n, dtype=dt, device=dev)
     info = NewtonInfo()
     g0 = None
     for step in range(newton_steps):
-        mu = torch.sigmoid(matvec(X, w))
-        g = rmatvec(X, mu - labels) + lam * w
+        mu = torch.sigmoid(ops.matvec(w))
+        g = ops.rmatvec(mu - labels) + lam * w
         gn = float(torch.linalg.vector_norm(g))
         if g0 is None:
             g0 = max(gn, 1e-300)
