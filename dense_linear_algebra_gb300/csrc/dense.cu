@@ -685,9 +685,18 @@ __global__ void __launch_bounds__(WIDE_THREADS) dense_wide_f64_kernel(const Dens
             d[r] = fma(xv.y, yv.y, fma(xv.x, yv.x, d[r]));
           }
       }
-      // ... and this step's scatter (rows from L2): the FMA chain starts from the column sum
-      // (read as two doubles: in global memory a CTA's sums start 8-byte aligned for odd n)
-      double s0 = acc[2 * c], s1 = acc[2 * c + 1];
+      // ... and this step's scatter (rows from L2): the FMA chain starts from the column sum,
+      // read as one 16-byte access in shared memory (half the wavefronts of two 8-byte ones)
+      // and as two doubles in global memory (a CTA's sums start 8-byte aligned for odd n)
+      double s0, s1;
+      if (smem_acc) {
+        const double2 sv = *reinterpret_cast<const double2*>(acc + 2 * c);
+        s0 = sv.x;
+        s1 = sv.y;
+      } else {
+        s0 = acc[2 * c];
+        s1 = acc[2 * c + 1];
+      }
 #pragma unroll
       for (int r = 0; r < R; ++r)
         if (r < rows) {
@@ -695,8 +704,12 @@ __global__ void __launch_bounds__(WIDE_THREADS) dense_wide_f64_kernel(const Dens
           s0 = fma(t[r], xv.x, s0);
           s1 = fma(t[r], xv.y, s1);
         }
-      acc[2 * c] = s0;
-      acc[2 * c + 1] = s1;
+      if (smem_acc) {
+        *reinterpret_cast<double2*>(acc + 2 * c) = make_double2(s0, s1);
+      } else {
+        acc[2 * c] = s0;
+        acc[2 * c + 1] = s1;
+      }
     }
     for (int64_t j = nvec * 2 + threadIdx.x; j < n; j += blockDim.x) {
       if (rows1 > 0) {
