@@ -17,8 +17,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfusedxtx.so")
-SOURCES = ["api.cu", "dense.cu", "csr.cu", "multi.cu", "split.cu", "plan.cpp", "tmap.cpp", "tune.cpp",
-           "noalloc.cu"]
+SOURCES = ["api.cu", "dense.cu", "csr.cu", "multi.cu", "multi_tc.cu", "split.cu", "plan.cpp", "tmap.cpp",
+           "tune.cpp", "noalloc.cu"]
 HEADERS = ["common.cuh", "kernels.h", "multi.h", "plan.h", "tmap.h", "tune.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -20,6 +20,7 @@
 
 #include <algorithm>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 
 #include "common.cuh"
@@ -455,12 +456,36 @@ MultiPlan plan_multi(const DeviceInfo& dev, int64_t m, int64_t n, int64_t k, int
   const int64_t tiles = (m + p.rows_per_tile - 1) / p.rows_per_tile;
   p.ctas = (int)std::max<int64_t>(1, std::min<int64_t>(dev.sm_count, (tiles + p.warps - 1) / p.warps));
   p.ws_bytes = (size_t)p.ctas * n * p.kb_max * sizeof(double) + 128;
+  // fp32 rows of at most 32 columns with 8 or more right-hand sides: both products on the
+  // tensor cores, 128-row tiles, one CTA per SM (the environment variable
+  // FXTX_MULTI_TC=0 keeps such calls on the CUDA-core kernel)
+  static const bool tc_on = [] {
+    const char* e = getenv("FXTX_MULTI_TC");
+    return !(e && e[0] == '0');
+  }();
+  if (tc_on && elem == 4 && n <= 32 && k >= 8 && p.tma) {
+    MultiPlan q = p;
+    q.tc = true;
+    q.nb = 1;
+    q.kb_max = k <= 8 ? 8 : (k <= 16 ? 16 : 32);
+    q.passes = (int)((k + q.kb_max - 1) / q.kb_max);
+    q.rows_per_tile = 128;
+    q.warps = multi_tc_warps(q.kb_max);
+    q.stages = multi_tc_stages(q.kb_max);
+    q.smem = multi_tc_smem(q.kb_max);
+    const int64_t tc_tiles = (m + 127) / 128;
+    q.ctas = (int)std::max<int64_t>(1, std::min<int64_t>(dev.sm_count, tc_tiles));
+    q.ws_bytes = (size_t)q.ctas * n * q.kb_max * sizeof(double) + 128;
+    if (q.smem <= budget) p = q;
+  }
   // the model's estimate: every pass reads X; weights, Y, Z and OUT once; two FMAs per element
   // of X and right-hand side, at the ~35 % of the FMA rate this kernel's issue rate allows
   const double vbytes = full_v ? (double)m * k * elem : (has_v ? (double)m * elem * p.passes : 0.0);
   const double bytes = (double)m * n * elem * p.passes + vbytes + 3.0 * n * k * elem;
-  p.est_us = roofline_us(dev, bytes, 0.9, 2.0 * m * n * k, elem, elem == 4 ? 0.35 : 0.8, 0.0, 1.0) +
-             4.0 * (p.passes - 1);
+  // the tensor-core form leaves the CUDA cores the bfloat16 split of X (about three FMA issue
+  // slots per element and pass), independent of the right-hand sides
+  const double fmas = p.tc ? 3.0 * m * n * p.passes : 2.0 * m * n * k;
+  p.est_us = roofline_us(dev, bytes, 0.9, fmas, elem, elem == 4 ? 0.35 : 0.8, 0.0, 1.0) + 4.0 * (p.passes - 1);
   return p;
 }
 
@@ -470,10 +495,10 @@ int multi_pass_kb(const MultiPlan& p, int64_t k, int64_t c0) {
 
 int describe_multi(const MultiPlan& p, char* buf, size_t cap) {
   return snprintf(buf, cap,
-                  "multi ok=%d tma=%d blocks=%d kb=%d passes=%d rows_per_tile=%d stages=%d warps=%d ctas=%d smem=%zu "
-                  "ws=%zu est_us=%.1f",
-                  (int)p.ok, (int)p.tma, p.nb, p.kb_max, p.passes, p.rows_per_tile, p.stages, p.warps, p.ctas, p.smem,
-                  p.ws_bytes, p.est_us);
+                  "multi ok=%d tma=%d tc=%d blocks=%d kb=%d passes=%d rows_per_tile=%d stages=%d warps=%d ctas=%d "
+                  "smem=%zu ws=%zu est_us=%.1f",
+                  (int)p.ok, (int)p.tma, (int)p.tc, p.nb, p.kb_max, p.passes, p.rows_per_tile, p.stages, p.warps,
+                  p.ctas, p.smem, p.ws_bytes, p.est_us);
 }
 
 int take_multi_device_error() { return take_device_error(); }
@@ -516,6 +541,9 @@ static cudaError_t launch_nb(const MultiPlan& p, const MultiArgs<T>& a, int vmod
 template <typename T>
 cudaError_t launch_multi(const MultiPlan& p, const MultiArgs<T>& a, cudaStream_t st) {
   if (!p.ok || a.kb < 1 || a.kb > p.kb_max) return cudaErrorInvalidConfiguration;
+  if constexpr (sizeof(T) == 4) {
+    if (p.tc) return launch_multi_tc(p, a, st);
+  }
   const int vmode = a.V == nullptr ? 0 : (a.ldv == 0 ? 1 : 2);
   switch (p.nb) {
     case 1: return launch_nb<T, 1>(p, a, vmode, st);

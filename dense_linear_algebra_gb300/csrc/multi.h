@@ -53,6 +53,7 @@ struct MultiPlan {
   size_t smem = 0;
   size_t ws_bytes = 0;  // per-CTA partials of the widest pass, plus the ticket
   double est_us = 0.0;  // the model's estimate of the call (all passes)
+  bool tc = false;      // fp32, n <= 32, k >= 8: X^T T on the tensor cores (multi_tc.cu)
 };
 
 MultiPlan plan_multi(const DeviceInfo& dev, int64_t m, int64_t n, int64_t k, int elem, bool tma_ok, bool full_v,
@@ -63,6 +64,13 @@ int multi_pass_kb(const MultiPlan& p, int64_t k, int64_t c0);
 
 template <typename T>
 cudaError_t launch_multi(const MultiPlan& p, const MultiArgs<T>& a, cudaStream_t st);
+
+// The tensor-core form (fp32 X of at most 32 columns, kb_max = 8, 16 or 32 right-hand sides
+// a pass): its dynamic shared memory, its X pipeline depth, and its launcher.
+size_t multi_tc_smem(int kb);
+int multi_tc_stages(int kb);
+int multi_tc_warps(int kb);
+cudaError_t launch_multi_tc(const MultiPlan& p, const MultiArgs<float>& a, cudaStream_t st);
 
 int describe_multi(const MultiPlan& p, char* buf, size_t cap);
 

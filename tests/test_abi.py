@@ -116,7 +116,11 @@ def test_launch_model_grid_and_smem_limits():
 @pytest.mark.parametrize(
     "args,expect",
     [
-        (("f32", 16_000_000, 32, 8), "tma=1 blocks=1 kb=8 passes=1 rows_per_tile=64 stages=2 warps=8 ctas=152"),
+        (("f32", 16_000_000, 32, 8), "tma=1 tc=1 blocks=1 kb=8 passes=1 rows_per_tile=128 stages=6 warps=15 ctas=152"),
+        (("f32", 16_000_000, 32, 4), "tma=1 tc=0 blocks=1 kb=4 passes=1 rows_per_tile=64"),
+        (("f32", 16_000_000, 32, 16), "tc=1 blocks=1 kb=16 passes=1"),
+        (("f64", 16_000_000, 32, 8), "tc=0"),
+        (("f32", 1000, 33, 8), "tc=0"),
         (("f32", 16_000_000, 32, 1), "kb=1 passes=1 rows_per_tile=32 stages=6"),
         (("f32", 16_000_000, 32, 40), "kb=32 passes=2"),
         (("f32", 1000, 32, 3), "kb=4 passes=1"),
@@ -124,7 +128,7 @@ def test_launch_model_grid_and_smem_limits():
         (("f32", 1000, 512, 8, "none"), "blocks=16 kb=2 passes=4 rows_per_tile=8 stages=3 warps=4"),
         (("f32", 1000, 513, 8), "ok=0"),
         (("f64", 0, 17, 8), "tma=0"),
-        (("f32", 1000, 32, 8, "full", 33), "tma=0 blocks=1 kb=8"),
+        (("f32", 1000, 32, 8, "full", 33), "tma=0 tc=0 blocks=1 kb=8"),
     ],
 )
 def test_multi_launch_model(args, expect):
