@@ -70,6 +70,12 @@ WORKLOADS = {
     "dense_multi": ("dense f32 16,000,000 x 32 with k=8 right-hand sides: Y, Z (32 x 8) N(0,1), V (16,000,000 x 8) "
                     "U[0.1,2], alpha=2, beta=-1",
                     lambda g, m=None: g.dense_multi(**_m({}, m))),
+    "dense_multi_k16": ("dense f32 16,000,000 x 32 with k=16 right-hand sides: Y, Z (32 x 16) N(0,1), V "
+                        "(16,000,000 x 16) U[0.1,2], alpha=2, beta=-1",
+                        lambda g, m=None: g.dense_multi(**_m({"k": 16}, m))),
+    "dense_multi_k32": ("dense f32 16,000,000 x 32 with k=32 right-hand sides: Y, Z (32 x 32) N(0,1), V "
+                        "(16,000,000 x 32) U[0.1,2], alpha=2, beta=-1",
+                        lambda g, m=None: g.dense_multi(**_m({"k": 32}, m))),
     "dense_multi_shared": ("dense f32 16,000,000 x 32 with k=8 right-hand sides and one shared v: Y, Z (32 x 8) "
                            "N(0,1), v U[0.1,2], alpha=2, beta=-1",
                            lambda g, m=None: g.dense_multi(**_m({"v_mode": "shared"}, m))),
@@ -89,7 +95,9 @@ def dominant_kernel(p) -> str:
     if p.x_store == "bf16":
         return "dense_tile_kernel"
     if is_multi(p):
-        return "dense_multi_kernel"
+        vm = "none" if p.v is None else ("full" if p.v.ndim == 2 else "shared")
+        plan = fx.multi_plan_describe(dtype_name(p), p.m, p.n, p.y.shape[1], vm, p.ld)
+        return "dense_multi_tc_kernel" if " tc=1 " in plan else "dense_multi_kernel"
     if p.kind == "csr":
         # rows longer than the plan's one-warp limit go to the long-row kernel, which dominates
         # when they hold most entries; otherwise the row kernel of the plan (lane groups for
@@ -230,14 +238,16 @@ class ClockSampler:
 
 
 KERNEL_SOURCES = {"dense": ["dense.cu", "common.cuh", "kernels.h"], "csr": ["csr.cu", "common.cuh", "kernels.h"],
-                  "multi": ["multi.cu", "multi.h", "common.cuh", "kernels.h"]}
+                  "multi": ["multi.cu", "multi.h", "common.cuh", "kernels.h"],
+                  "multi_tc": ["multi_tc.cu", "multi.h", "common.cuh", "kernels.h"]}
 
 
 def source_sha(kernel: str) -> str:
     """Hash of the source files that define a kernel (its .cu file and the device headers it includes)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_linear_algebra_gb300", "csrc")
-    group = "csr" if kernel.startswith("csr") else ("multi" if kernel.startswith("dense_multi") else "dense")
+    group = ("csr" if kernel.startswith("csr") else "multi_tc" if kernel.startswith("dense_multi_tc")
+             else "multi" if kernel.startswith("dense_multi") else "dense")
     for fn in KERNEL_SOURCES[group]:
         h.update(open(os.path.join(csrc, fn), "rb").read())
     return h.hexdigest()[:16]
@@ -613,7 +623,25 @@ def run_fused(args, name, desc, p, rank, world, dist):
         "unfused_library": unfused,
         "model": model_estimate(p),
     }
-    if is_multi(p):
+    if is_multi(p) and kernel == "dense_multi_tc_kernel":
+        # both products on the tensor cores (bfloat16 terms, fp32 accumulation): per 128-row tile
+        # 6 + 8 MMAs of M = 128, K = 16 and N = 3 kb rounded up to 16; the kernel is bound by the
+        # number of MMAs and shared-memory traffic long before the tensor pipe's flop rate
+        k = p.y.shape[1]
+        kb = 8 if k <= 8 else (16 if k <= 16 else 32)
+        nw = (3 * kb + 15) // 16 * 16
+        passes = -(-k // kb)
+        tiles = -(-p.m // 128)
+        mma_flops = 2.0 * 128 * nw * 16 * 14 * tiles * passes
+        bf16_peak = _num(peaks.get("bf16_tflops")) if isinstance(peaks, dict) else None
+        rec["roofline_tensor"] = {"bound": "tensor", "algorithmic_flops_per_step": 4.0 * p.m * p.n * k,
+                                  "executed_mma_flops_per_step": mma_flops,
+                                  "achieved": round(mma_flops / (kernel_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                                  "peak": bf16_peak, "peak_source": "measured cuBLAS bf16 (burst)",
+                                  "frac": None if not bf16_peak else round(mma_flops / (kernel_ms * 1e-3) / 1e12 /
+                                                                          bf16_peak, 4)}
+        rec["config"]["right_hand_sides"] = int(k)
+    elif is_multi(p):
         # k right-hand sides: two FMAs (4 flops) per stored element per right-hand side, on the fp32 or fp64 pipe
         flops = 4.0 * p.m * p.n * p.y.shape[1]
         alu_peak = FP32_PEAK_TFLOPS if dtype_name(p) == "f32" else fp64_peak_tflops(peaks)
@@ -815,8 +843,9 @@ def config_summary(label, target, rec):
          "hbm_pct_of_nominal_7900": round(100 * rec["roofline"]["achieved"] / 7900.0, 2),
          "algorithmic_bytes_per_call": rec["config"]["algorithmic_bytes_per_step"],
          "roofline": rec["roofline"], "e2e": rec["e2e"], "clocks": rec["clocks"], "model": rec["model"]}
-    if "roofline_alu" in rec:
-        d["roofline_alu"] = rec["roofline_alu"]
+    for key in ("roofline_alu", "roofline_tensor"):
+        if key in rec:
+            d[key] = rec[key]
     if "nnz" in rec["config"]:
         d["nnz"] = rec["config"]["nnz"]
     u = rec.get("unfused_library") or {}

@@ -361,8 +361,8 @@ __global__ void __launch_bounds__(TcCfg<KB>::THREADS, 1)
           const float4 f = *reinterpret_cast<const float4*>(xrow + ((c ^ (r & 7)) * 16));
           x[4 * c] = f.x; x[4 * c + 1] = f.y; x[4 * c + 2] = f.z; x[4 * c + 3] = f.w;
         }
-        // the row's loads are complete before the stage goes back to the tensor copies (a
-        // generic-proxy read, then an async-proxy write of the same bytes)
+        // the stage goes back to the tensor copies at once; the proxy fence completes the row's
+        // loads first (generic-proxy reads, then an async-proxy write of the same bytes)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&xfree[s]);
@@ -444,9 +444,6 @@ __global__ void __launch_bounds__(TcCfg<KB>::THREADS, 1)
 #pragma unroll
             for (int c = 0; c < KB; ++c) v[c] = w;
           }
-          fence_proxy_async_smem();  // as for the X stages: reads done before the copy refills
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&vfree[s]);
         }
         tc_fence_after();
         float t[KB];
@@ -461,10 +458,15 @@ __global__ void __launch_bounds__(TcCfg<KB>::THREADS, 1)
           *reinterpret_cast<uint4*>(tb + (size_t)((KB + c8) >> 3) * 128) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
           *reinterpret_cast<uint4*>(tb + (size_t)((2 * KB + c8) >> 3) * 128) = make_uint4(w3[0], w3[1], w3[2], w3[3]);
         }
+        // one proxy fence covers the T stores (read next by the products) and the V stage's
+        // loads (its bytes are rewritten next by a tensor copy)
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tready[i % NT]);
+        if (lane == 0) {
+          if (v_staged) mbar_arrive(&vfree[i % SV]);
+          mbar_arrive(&tready[i % NT]);
+        }
         // the previous tile group's sums, once this tile group's first tile is formed (its
         // first tiles fall to row group 0, so W is read before the next products overwrite it)
         if (h == 0 && i % C::G == 0 && i >= C::G && !(ok = drain(i / C::G - 1))) break;

@@ -45,7 +45,8 @@ def test_reference_arm_prints_on_rank_zero_only():
     (lambda: inputgen.dense_tall(m=1000, variant="b"), "dense_tile_kernel"),
     (lambda: inputgen.dense_tall(m=1000, variant="b", x_store="bf16"), "dense_tile_kernel"),
     (lambda: inputgen.dense_wide(m=64, n=20_000), "dense_wide_f64_kernel"),
-    (lambda: inputgen.dense_multi(m=1000, k=8), "dense_multi_kernel"),
+    (lambda: inputgen.dense_multi(m=1000, k=8), "dense_multi_tc_kernel"),
+    (lambda: inputgen.dense_multi(m=1000, k=4), "dense_multi_kernel"),
     (lambda: inputgen.csr_uniform(m=20_000), "csr_group_kernel"),
     (lambda: inputgen.csr_powerlaw(m=20_000), "csr_long_kernel"),
 ])
