@@ -29,10 +29,10 @@
 //   warp 0       one thread: tensor copies of X tiles (128 x 32 fp32, 128-byte swizzle);
 //   warp 1       one thread: issues the products and commits them to mbarriers;
 //   warps 2..5   split warps: one row each, X into its three terms in an operand buffer;
-//   warps 6..    row warps, one or two groups of four (tensor-memory lanes 32 (warp % 4) ..)
-//                taking alternate tiles: each row's U from tensor memory, t = v u and its
-//                terms into the T buffer; group 0 also folds W, every four tiles, into the
-//                column sums;
+//   warps 6..13  row warps, two groups of four (tensor-memory lanes 32 (warp % 4) ..),
+//                taking alternate tiles (kb = 32: every tile, half of the right-hand sides
+//                each): each row's U from tensor memory, t = v u and its terms into the T
+//                buffer; every four tiles, W folded into the column sums;
 //   last warp    one thread: tensor copies of the tiles' rows of V.
 //
 // Shared-memory operand layouts (no swizzle; core matrices of 8 rows x 16 bytes):
@@ -163,7 +163,10 @@ struct TcCfg {
   static constexpr int NA = 3;                        // X-terms buffers
   static constexpr int NT = KB <= 16 ? 2 : 1;         // T-terms buffers
   static constexpr int G = 4;                         // tiles summed in tensor memory per W drain
-  static constexpr int RG = KB <= 16 ? 2 : 1;         // row-warp groups (alternate tiles)
+  static constexpr int RG = 2;                        // row-warp groups
+  static constexpr bool CS = KB == 32;                // groups split the columns (else alternate tiles)
+  static constexpr int KC = CS ? KB / 2 : KB;         // right-hand sides a row group takes
+  static constexpr int TARRIVE = CS ? 8 : 4;          // row warps that form each tile's T
   static constexpr int WARPS = 7 + 4 * RG;            // producers, products, split warps, row warps
   static constexpr int THREADS = 32 * WARPS;
   static constexpr int LBO_T = (NW / 8) * 128;        // core stride along K (rows) of the T terms
@@ -226,9 +229,9 @@ __global__ void __launch_bounds__(TcCfg<KB>::THREADS, 1)
   }
   if (tid == 0) {
     for (int s = 0; s < SX; ++s) { mbar_init(&xfull[s], 1); mbar_init(&xfree[s], 4); }
-    for (int s = 0; s < SV; ++s) { mbar_init(&vfull[s], 1); mbar_init(&vfree[s], 4); }
+    for (int s = 0; s < SV; ++s) { mbar_init(&vfull[s], 1); mbar_init(&vfree[s], C::TARRIVE); }
     for (int s = 0; s < NA; ++s) { mbar_init(&aready[s], 4); mbar_init(&opfree[s], 1); }
-    for (int s = 0; s < NT; ++s) { mbar_init(&tready[s], 4); mbar_init(&tfree[s], 1); }
+    for (int s = 0; s < NT; ++s) { mbar_init(&tready[s], C::TARRIVE); mbar_init(&tfree[s], 1); }
     for (int s = 0; s < 2; ++s) { mbar_init(&uready[s], 1); mbar_init(&wready[s], 1); }
     mbar_init(&fin_bar, 1);
     fence_mbar_init();
@@ -247,8 +250,8 @@ __global__ void __launch_bounds__(TcCfg<KB>::THREADS, 1)
   bool ok = true;
 
   // compensated column sums: a row-warp thread of quarter q < 3 holds term q of X column
-  // `lane` (tensor-memory lane 32 q + lane of W), for every right-hand side
-  CompF32 acc[KB];
+  // `lane` (tensor-memory lane 32 q + lane of W), for its group's right-hand sides
+  CompF32 acc[C::KC];
 
   if (warp == 0 || warp == C::WARPS - 1) {
     // ---- tensor copies: X tiles (warp 0), rows of V (the last warp) ----
@@ -381,13 +384,17 @@ __global__ void __launch_bounds__(TcCfg<KB>::THREADS, 1)
         if (lane == 0) mbar_arrive(&aready[ob]);
       }
     } else {
-      // ---- row warps: group h takes tiles h, h + RG, ...; group 0 also drains W ----
+      // ---- row warps: two groups, taking alternate tiles (group 0 also drains W) or, at
+      // kb = 32, every tile with half of the right-hand sides each (columns cofs .. + KC) ----
+      constexpr int KC = C::KC;
       const int h = (warp - 6) >> 2;
+      const int cofs = C::CS ? KC * h : 0;
+      const bool drains = C::CS || h == 0;
       const int q = warp & 3;      // quarter of the tile: tensor-memory lanes 32 q ..
       const int r = 32 * q + lane;
       const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
-      // 3 x KB fp32 columns (three groups of KB) from tensor memory at column `col`, summed
-      // by group into s[KB]; `f` folds each sum
+      // the group's KC right-hand sides of the three column groups (of KB each) from tensor
+      // memory at column `col`, summed by group; `f(c, sum)` folds each, c < KC
       auto sum_groups = [&](uint32_t col, auto&& f) {
         if constexpr (KB == 8) {  // groups in columns 0..7, 8..15, 16..23
           uint32_t d0[16], d1[16];
@@ -398,11 +405,11 @@ __global__ void __launch_bounds__(TcCfg<KB>::THREADS, 1)
           for (int c = 0; c < 8; ++c) f(c, (__uint_as_float(d0[c]) + __uint_as_float(d0[8 + c])) + __uint_as_float(d1[c]));
         } else {
 #pragma unroll
-          for (int c0 = 0; c0 < KB; c0 += 16) {
+          for (int c0 = 0; c0 < KC; c0 += 16) {
             uint32_t d0[16], d1[16], d2[16];
-            tc_load16(lane_base + col + (uint32_t)c0, d0);
-            tc_load16(lane_base + col + (uint32_t)(KB + c0), d1);
-            tc_load16(lane_base + col + (uint32_t)(2 * KB + c0), d2);
+            tc_load16(lane_base + col + (uint32_t)(cofs + c0), d0);
+            tc_load16(lane_base + col + (uint32_t)(KB + cofs + c0), d1);
+            tc_load16(lane_base + col + (uint32_t)(2 * KB + cofs + c0), d2);
             tc_wait_ld();
 #pragma unroll
             for (int c = 0; c < 16; ++c)
@@ -417,15 +424,16 @@ __global__ void __launch_bounds__(TcCfg<KB>::THREADS, 1)
         if (q < 3) sum_groups(wcol + (uint32_t)((gidx & 1) * NW), [&](int c, float w) { acc[c].add(w); });
         return true;
       };
-      for (int i = h; i < nt; i += C::RG) {
+      for (int i = C::CS ? 0 : h; i < nt; i += C::CS ? 1 : C::RG) {
         const int64_t row = (t0 + i) * TC_ROWS + r;
-        float v[KB];
+        float v[KC];
 #pragma unroll
-        for (int c = 0; c < KB; ++c) v[c] = 1.f;
+        for (int c = 0; c < KC; ++c) v[c] = 1.f;
         if (vmode != 0 && !v_tma) {  // rows of V by plain loads, issued before the waits
 #pragma unroll
-          for (int c = 0; c < KB; ++c)
-            v[c] = row < a.m && (vmode == 1 || c < kb) ? ldg(a.V + (vmode == 1 ? row : row * a.ldv + c)) : 0.f;
+          for (int c = 0; c < KC; ++c)
+            v[c] = row < a.m && (vmode == 1 || cofs + c < kb)
+                       ? ldg(a.V + (vmode == 1 ? row : row * a.ldv + cofs + c)) : 0.f;
         }
         if (i >= NT && !(ok = wait_warp(&tfree[i % NT], (uint32_t)(((i - NT) / NT) & 1)))) break;
         if (!(ok = wait_warp(&uready[i & 1], (uint32_t)((i >> 1) & 1)))) break;
@@ -433,30 +441,36 @@ __global__ void __launch_bounds__(TcCfg<KB>::THREADS, 1)
           const int s = i % SV;
           if (!(ok = wait_warp(&vfull[s], (uint32_t)((i / SV) & 1)))) break;
           if (vmode == 2) {
-            const float4* vp = reinterpret_cast<const float4*>(vs + (size_t)s * C::VTILE + (size_t)r * KB * 4);
+            // the stage holds 128 rows of KB fp32 in the swizzle of their width (32, 64 or
+            // 128 bytes): 16-byte chunk bits 4.. of a byte offset are XORed with its bits 7..,
+            // so the eight rows a quarter-warp reads land in eight distinct chunks
+            constexpr uint32_t SWZ = KB == 8 ? 1u : (KB == 16 ? 3u : 7u);
+            const unsigned char* vst = vs + (size_t)s * C::VTILE;
 #pragma unroll
-            for (int c = 0; c < KB / 4; ++c) {
-              const float4 w = vp[c];
+            for (int c = 0; c < KC / 4; ++c) {
+              const uint32_t o = (uint32_t)(r * KB + cofs + 4 * c) * 4u;
+              const float4 w = *reinterpret_cast<const float4*>(vst + (o ^ (((o >> 7) & SWZ) << 4)));
               v[4 * c] = w.x; v[4 * c + 1] = w.y; v[4 * c + 2] = w.z; v[4 * c + 3] = w.w;
             }
           } else {
             const float w = reinterpret_cast<const float*>(vs + (size_t)s * C::VTILE)[r];
 #pragma unroll
-            for (int c = 0; c < KB; ++c) v[c] = w;
+            for (int c = 0; c < KC; ++c) v[c] = w;
           }
         }
         tc_fence_after();
-        float t[KB];
+        float t[KC];
         sum_groups(ucol + (uint32_t)((i & 1) * NW), [&](int c, float u) { t[c] = v[c] * u; });
         unsigned char* tb = ts + (size_t)(i % NT) * C::TBUF + (size_t)(r >> 3) * C::LBO_T + (size_t)(r & 7) * 16;
 #pragma unroll
-        for (int c8 = 0; c8 < KB; c8 += 8) {
+        for (int c8 = 0; c8 < KC; c8 += 8) {
           uint32_t w1[4], w2[4], w3[4];
 #pragma unroll
           for (int p = 0; p < 4; ++p) split3(t[c8 + 2 * p], t[c8 + 2 * p + 1], w1[p], w2[p], w3[p]);
-          *reinterpret_cast<uint4*>(tb + (size_t)(c8 >> 3) * 128) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-          *reinterpret_cast<uint4*>(tb + (size_t)((KB + c8) >> 3) * 128) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
-          *reinterpret_cast<uint4*>(tb + (size_t)((2 * KB + c8) >> 3) * 128) = make_uint4(w3[0], w3[1], w3[2], w3[3]);
+          const int cc = cofs + c8;  // T column of term 0
+          *reinterpret_cast<uint4*>(tb + (size_t)(cc >> 3) * 128) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+          *reinterpret_cast<uint4*>(tb + (size_t)((KB + cc) >> 3) * 128) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+          *reinterpret_cast<uint4*>(tb + (size_t)((2 * KB + cc) >> 3) * 128) = make_uint4(w3[0], w3[1], w3[2], w3[3]);
         }
         // one proxy fence covers the T stores (read next by the products) and the V stage's
         // loads (its bytes are rewritten next by a tensor copy)
@@ -467,11 +481,12 @@ __global__ void __launch_bounds__(TcCfg<KB>::THREADS, 1)
           if (v_staged) mbar_arrive(&vfree[i % SV]);
           mbar_arrive(&tready[i % NT]);
         }
-        // the previous tile group's sums, once this tile group's first tile is formed (its
-        // first tiles fall to row group 0, so W is read before the next products overwrite it)
-        if (h == 0 && i % C::G == 0 && i >= C::G && !(ok = drain(i / C::G - 1))) break;
+        // the previous tile group's sums, once this tile group's first tile is formed (a
+        // group that drains forms every tile group's first tile, so W is read before the next
+        // products overwrite it)
+        if (drains && i % C::G == 0 && i >= C::G && !(ok = drain(i / C::G - 1))) break;
       }
-      if (ok && h == 0 && nt > 0) ok = drain((nt - 1) / C::G);
+      if (ok && drains && nt > 0) ok = drain((nt - 1) / C::G);
     }
   }
 
@@ -483,10 +498,10 @@ __global__ void __launch_bounds__(TcCfg<KB>::THREADS, 1)
 
   // the column sums of the three X terms through shared memory into per-CTA partials
   double* red = reinterpret_cast<double*>(smem);  // [3][32][KB], over the X stages
-  if (warp >= 6 && warp < 10 && (warp & 3) < 3) {
-    const int q = warp & 3;
+  if (warp >= 6 && warp < 6 + 4 * C::RG && (warp & 3) < 3 && (C::CS || warp < 10)) {
+    const int q = warp & 3, cofs = C::CS ? C::KC * ((warp - 6) >> 2) : 0;
 #pragma unroll
-    for (int c = 0; c < KB; ++c) red[(q * 32 + lane) * KB + c] = acc[c].value();
+    for (int c = 0; c < C::KC; ++c) red[(q * 32 + lane) * KB + cofs + c] = acc[c].value();
   }
   __syncthreads();
   const int64_t N = n * KB;
@@ -520,12 +535,13 @@ cudaError_t launch_tc_kb(const MultiPlan& p, const MultiArgs<float>& a, int vmod
   if (!encode_rows_map(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.X, a.m, a.n, a.ld * 4, 4, TC_ROWS, 128, 128))
     return cudaErrorInvalidValue;
   // rows of V by tensor copies where V (and its pitch) allow: an m x kb block in boxes of
-  // 128 rows x KB columns (columns past kb read as zero), or the m-vector as one row in
-  // boxes of 128 elements
+  // 128 rows x KB columns (columns past kb read as zero), swizzled at the rows' width, or
+  // the m-vector as one row in boxes of 128 elements
   int v_tma = 0;
   const bool v_aligned = (reinterpret_cast<uintptr_t>(a.V) & 15u) == 0;
   if (vmode == 2 && v_aligned && (a.ldv * 4) % 16 == 0)
-    v_tma = encode_rows_map(&vmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.V, a.m, a.kb, a.ldv * 4, 4, TC_ROWS, KB * 4, 0);
+    v_tma = encode_rows_map(&vmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.V, a.m, a.kb, a.ldv * 4, 4, TC_ROWS, KB * 4,
+                            KB * 4);
   else if (vmode == 1 && v_aligned)
     v_tma = encode_rows_map(&vmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.V, 1, a.m, (a.m * 4 + 15) / 16 * 16, 4, 1,
                             TC_ROWS * 4, 0);

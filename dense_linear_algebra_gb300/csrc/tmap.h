@@ -10,7 +10,7 @@ namespace fxtx {
 
 // Map of a matrix of `rows` rows and `cols` elements of `elem` bytes, rows `pitch_bytes`
 // apart (a multiple of 16), read in boxes of box_rows x box_bytes (a multiple of 16,
-// at most 128 when swizzled). swizzle: 0 (rows land unpermuted), 64 or 128 (the
+// at most 128 when swizzled). swizzle: 0 (rows land unpermuted), 32, 64 or 128 (the
 // swizzle of that width; box_bytes must equal it). Out-of-range elements read as zero.
 // False if the driver entry point is missing or refuses the arguments.
 bool encode_rows_map(CUtensorMap* map, CUtensorMapDataType type, const void* base, int64_t rows, int64_t cols,
