@@ -28,8 +28,9 @@
 // only:
 //   warp 0       one thread: tensor copies of X tiles (128 x 32 fp32, 128-byte swizzle);
 //   warp 1       one thread: issues the products and commits them to mbarriers;
-//   warps 2..5   split warps: one row each, X into its three terms in an operand buffer;
-//   warps 6..13  row warps, two groups of four (tensor-memory lanes 32 (warp % 4) ..),
+//   warps 2..    split warps, one group of four (two at kb = 8, taking alternate tiles): one
+//                row each, X into its three terms in an operand buffer;
+//   next 8 warps row warps, two groups of four (tensor-memory lanes 32 (warp % 4) ..),
 //                taking alternate tiles (kb = 32: every tile, half of the right-hand sides
 //                each): each row's U from tensor memory, t = v u and its terms into the T
 //                buffer; every four tiles, W folded into the column sums;
@@ -167,7 +168,9 @@ struct TcCfg {
   static constexpr bool CS = KB == 32;                // groups split the columns (else alternate tiles)
   static constexpr int KC = CS ? KB / 2 : KB;         // right-hand sides a row group takes
   static constexpr int TARRIVE = CS ? 8 : 4;          // row warps that form each tile's T
-  static constexpr int WARPS = 7 + 4 * RG;            // producers, products, split warps, row warps
+  static constexpr int SG = KB == 8 ? 2 : 1;          // split-warp groups (alternate tiles; registers allow 2 at kb = 8)
+  static constexpr int ROW0 = 2 + 4 * SG;             // first row warp
+  static constexpr int WARPS = ROW0 + 4 * RG + 1;     // producers, products, split warps, row warps
   static constexpr int THREADS = 32 * WARPS;
   static constexpr int LBO_T = (NW / 8) * 128;        // core stride along K (rows) of the T terms
   static constexpr int TBUF = TC_ROWS * NW * 2;       // bytes of one tile's T terms
@@ -349,10 +352,10 @@ __global__ void __launch_bounds__(TcCfg<KB>::THREADS, 1)
   } else {
     // every lane of these warps takes the same branch after a wait
     auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool { return warp_wait(bar, parity, abort_word); };
-    if (warp < 6) {
+    if (warp < C::ROW0) {
       // ---- split warps ----
-      const int r = 32 * (warp - 2) + lane;
-      for (int i = 0; i < nt; ++i) {
+      const int r = 32 * ((warp - 2) & 3) + lane;
+      for (int i = (warp - 2) >> 2; i < nt; i += C::SG) {
         const int s = i % SX, ob = i % NA;
         if (!(ok = wait_warp(&xfull[s], (uint32_t)((i / SX) & 1)))) break;
         if (i >= NA && !(ok = wait_warp(&opfree[ob], (uint32_t)(((i - NA) / NA) & 1)))) break;
@@ -387,7 +390,7 @@ __global__ void __launch_bounds__(TcCfg<KB>::THREADS, 1)
       // ---- row warps: two groups, taking alternate tiles (group 0 also drains W) or, at
       // kb = 32, every tile with half of the right-hand sides each (columns cofs .. + KC) ----
       constexpr int KC = C::KC;
-      const int h = (warp - 6) >> 2;
+      const int h = (warp - C::ROW0) >> 2;
       const int cofs = C::CS ? KC * h : 0;
       const bool drains = C::CS || h == 0;
       const int q = warp & 3;      // quarter of the tile: tensor-memory lanes 32 q ..
@@ -498,8 +501,8 @@ __global__ void __launch_bounds__(TcCfg<KB>::THREADS, 1)
 
   // the column sums of the three X terms through shared memory into per-CTA partials
   double* red = reinterpret_cast<double*>(smem);  // [3][32][KB], over the X stages
-  if (warp >= 6 && warp < 6 + 4 * C::RG && (warp & 3) < 3 && (C::CS || warp < 10)) {
-    const int q = warp & 3, cofs = C::CS ? C::KC * ((warp - 6) >> 2) : 0;
+  if (warp >= C::ROW0 && warp < C::ROW0 + 4 * C::RG && (warp & 3) < 3 && (C::CS || warp < C::ROW0 + 4)) {
+    const int q = warp & 3, cofs = C::CS ? C::KC * ((warp - C::ROW0) >> 2) : 0;
 #pragma unroll
     for (int c = 0; c < C::KC; ++c) red[(q * 32 + lane) * KB + cofs + c] = acc[c].value();
   }
