@@ -864,6 +864,26 @@ def config_summary(label, target, rec):
     return d
 
 
+# rows beyond BASELINE's configurations measured in the default run: the multi-vector form
+NEXT_WORKLOADS = [("multi_k8", "dense_multi"), ("multi_k16", "dense_multi_k16"), ("multi_k32", "dense_multi_k32")]
+
+
+def next_summary(rec):
+    """The figures of one multi-vector measurement, for the headline line's `next` object."""
+    d = {"workload": rec["config"]["workload"], "name": rec["config"]["name"], "dtype": rec["dtype"],
+         "right_hand_sides": rec["config"].get("right_hand_sides"), "us_per_call": rec["us_per_call"],
+         "isolated_call_us": rec["isolated_call_us"], "value": rec["roofline"]["achieved"], "unit": "GB/s",
+         "hbm_frac_of_measured": rec["roofline"]["frac"], "roofline": rec["roofline"]}
+    for key in ("roofline_alu", "roofline_tensor"):
+        if key in rec:
+            d[key] = rec[key]
+    u = rec.get("unfused_library") or {}
+    if "ms_per_step" in u:
+        d["unfused_library"] = {"what": u["what"], "us_per_call": round(u["ms_per_step"] * 1e3, 2),
+                                "fused_speedup": u["fused_speedup"]}
+    return d
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -960,7 +980,16 @@ def main():
                 torch.cuda.empty_cache()
             rec["config"]["configs_note"] = ("headline: BASELINE configuration 2 (dense f32 16,000,000 x 32, "
                                              "alpha=2, beta=-1); every configuration, the headline included, "
-                                             "under `configs`, each measured in this run")
+                                             "under `configs`, each measured in this run; the multi-vector form "
+                                             "(k = 8, 16, 32 on the same X) under `next`")
+            rec["next"] = {}
+            for label, wl in NEXT_WORKLOADS:
+                wdesc, wmk = WORKLOADS[wl]
+                q = wmk(inputgen, None)
+                r = run_fused(args, wl, wdesc, q, rank, world, dist)
+                rec["next"][label] = next_summary(r)
+                del q, r
+                torch.cuda.empty_cache()
         if rank == 0:
             print(json.dumps(rec), flush=True)
     if dist:
