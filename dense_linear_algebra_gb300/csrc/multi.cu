@@ -20,6 +20,7 @@
 
 #include <algorithm>
 #include <cstdio>
+#include <cmath>
 #include <cstdlib>
 #include <cstring>
 
@@ -482,9 +483,18 @@ MultiPlan plan_multi(const DeviceInfo& dev, int64_t m, int64_t n, int64_t k, int
   // of X and right-hand side, at the ~35 % of the FMA rate this kernel's issue rate allows
   const double vbytes = full_v ? (double)m * k * elem : (has_v ? (double)m * elem * p.passes : 0.0);
   const double bytes = (double)m * n * elem * p.passes + vbytes + 3.0 * n * k * elem;
-  // the tensor-core form leaves the CUDA cores the bfloat16 split of X (about three FMA issue
-  // slots per element and pass), independent of the right-hand sides
-  const double fmas = p.tc ? 3.0 * m * n * p.passes : 2.0 * m * n * k;
+  if (p.tc) {
+    // the tensor-core form: its pipeline of roles takes a measured number of SM cycles per
+    // 128-row tile (16,000,000 x 32 on GB300 at 2,070 MHz: 610, 784 and 1,243 us per call at
+    // kb = 8, 16 and 32, i.e. ~1,540, ~1,970 and ~3,130 cycles a tile; the product warp's
+    // issue and waits, not HBM, set it), or the HBM time if that is longer
+    const double cyc = p.kb_max == 8 ? 1540.0 : (p.kb_max == 16 ? 1970.0 : 3130.0);
+    const double tiles_per_cta = std::ceil((double)((m + 127) / 128) / std::max(p.ctas, 1));
+    const double hbm_us = roofline_us(dev, bytes, 0.9, 0.0, elem, 1.0, 0.0, 1.0);  // includes the launch
+    p.est_us = std::max(sm_cycles_us(tiles_per_cta * cyc * p.passes), hbm_us) + 4.0 * (p.passes - 1);
+    return p;
+  }
+  const double fmas = 2.0 * m * n * k;
   p.est_us = roofline_us(dev, bytes, 0.9, fmas, elem, elem == 4 ? 0.35 : 0.8, 0.0, 1.0) + 4.0 * (p.passes - 1);
   return p;
 }

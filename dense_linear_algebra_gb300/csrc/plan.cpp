@@ -47,6 +47,8 @@ double roofline_us(const DeviceInfo& dev, double bytes, double hbm_eff, double f
   return t * 1e6 + kLaunchUs;
 }
 
+double sm_cycles_us(double cycles) { return cycles / kClockHz * 1e6; }
+
 namespace {
 
 // Dense call: X once, v, y, z and out; two FMAs per element of X.

@@ -147,6 +147,9 @@ CsrPlan plan_csr(const DeviceInfo& dev, int64_t m, int64_t n, int64_t nnz, int e
 double roofline_us(const DeviceInfo& dev, double bytes, double hbm_eff, double fmas, int elem, double fma_eff,
                    double l2_sectors, double l2_eff);
 
+// Microseconds of `cycles` SM cycles at the clock the estimates assume.
+double sm_cycles_us(double cycles);
+
 int describe(const DensePlan& p, char* buf, size_t cap);
 int describe(const CsrPlan& p, char* buf, size_t cap);
 

@@ -164,3 +164,16 @@ def test_multi_invalid_arguments_rejected_on_host():
     assert fx.fxtx_dense_multi_f64(4, 8, 2, None, 8, 16, 2, None, 0, 1.0, 0.0, None, 0, 16, 2, None) == fx.FXTX_ERR_INVALID_ARG
     assert m32(4, 0, 2, None, 1, None, 2, None, 0, 1.0, 0.0, None, 0, None, 2, None) == fx.FXTX_OK  # n == 0
     assert m32(4, 4, 0, None, 4, None, 0, None, 0, 1.0, 0.0, None, 0, None, 0, None) == fx.FXTX_OK  # k == 0
+
+
+def test_multi_tensor_core_estimate():
+    """The tensor-core form's estimate: never below the HBM time of its bytes (X and an m x k
+    V once, at 6.8 TB/s), and rising with the right-hand sides a pass takes."""
+    est = {}
+    for k in (8, 16, 32):
+        f = dict(kv.split("=") for kv in fx.multi_plan_describe("f32", 16_000_000, 32, k, "full").split()[1:])
+        assert f["tc"] == "1"
+        est[k] = float(f["est_us"])
+        hbm_us = (16_000_000 * 32 * 4 + 16_000_000 * k * 4) / 6.8e12 * 1e6
+        assert est[k] >= hbm_us, (k, est[k], hbm_us)
+    assert est[8] < est[16] < est[32]
