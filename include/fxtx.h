@@ -115,8 +115,9 @@ fxtx_status_t fxtx_dense_bf16(int64_t m, int64_t n, const uint16_t* X, int64_t l
  * fp32 with n <= 32, k >= 8 and tensor-copied X runs both products on the tensor
  * cores (8, 16 or 32 right-hand sides a pass): X, Y and each row's v * (x_i . Y)
  * are split into three bfloat16 terms whose products are summed in fp32, which
- * keeps the same bound. The environment variable FXTX_MULTI_TC set to "0" when
- * the library first plans such a call keeps those shapes on the CUDA cores.
+ * keeps the same bound for inputs of magnitude below 3.39e38 (larger ones round
+ * to infinity as bfloat16). The environment variable FXTX_MULTI_TC set to "0"
+ * when the library first plans such a call keeps those shapes on the CUDA cores.
  *
  * Each column c meets the bound of fxtx_dense_f32 / _f64 with its own
  * S_jc = |alpha| sum_i |t_ic| |X_ij| + |beta Z_jc|, t_ic = V_ic (x_i . Y[:, c]).
