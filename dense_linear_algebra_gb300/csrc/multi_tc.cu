@@ -12,9 +12,10 @@
 // Precision. The tensor cores take bfloat16 operands; fp32 values are split into three
 // bfloat16 terms, x = x1 + x2 + x3 exactly (each rounded to nearest, every residual exact in
 // fp32), and all nine products of the terms are formed, accumulated in fp32 in tensor
-// memory: U per tile; W per tile, drained after every tile into compensated two-float
-// column sums (so the fp32 rounding of a tile's sums, ~2^-24 S, does not grow with the
-// number of tiles). The error bound is the fp32 entry points' 2e-5 S.
+// memory: U per tile; W over four tiles (512 rows, 32 accumulation steps of K = 16), then
+// folded into compensated two-float column sums (so the fp32 rounding of W, at most
+// 32 * 2^-24 S, does not grow with the number of tiles). The error bound is the fp32 entry
+// points' 2e-5 S.
 //
 // Throughput. An M = 128, K = 16 tensor-core product holds the tensor pipe for about 64
 // cycles for any N up to 128 (measured on GB300), so the number of products per tile, not
@@ -27,14 +28,15 @@
 // Roles (one CTA per SM, persistent over a contiguous range of tiles), linked by mbarriers
 // only:
 //   warp 0       one thread: tensor copies of X tiles (128 x 32 fp32, 128-byte swizzle);
-//   warp 1       one thread: issues the products and commits them to mbarriers;
+//   warp 1       the product loop, run by the whole warp (converged), one elected lane
+//                issuing the products and committing them to mbarriers;
 //   warps 2..    split warps, one group of four (two at kb = 8, taking alternate tiles): one
 //                row each, X into its three terms in an operand buffer;
 //   next 8 warps row warps, two groups of four (tensor-memory lanes 32 (warp % 4) ..),
 //                taking alternate tiles (kb = 32: every tile, half of the right-hand sides
 //                each): each row's U from tensor memory, t = v u and its terms into the T
 //                buffer; every four tiles, W folded into the column sums;
-//   last warp    one thread: tensor copies of the tiles' rows of V.
+//   last warp    one thread: tensor copies of the tiles' rows of V (swizzled at their width).
 //
 // Shared-memory operand layouts (no swizzle; core matrices of 8 rows x 16 bytes):
 //   X terms   128 tile rows x 96 columns (term a's column j at 32 a + j): the 16 bytes of
