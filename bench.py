@@ -814,8 +814,8 @@ def run_solver(args):
     print(json.dumps(rec), flush=True)
 
 
-# BASELINE's configurations in order: (label, workload, HBM-fraction target or None)
-BASELINE_CONFIGS = [("1", "dense_small", None), ("2a", "dense_tall_a", 0.75), ("2b", "dense_tall_b", 0.75),
+# the benchmark configurations in order: (label, workload, HBM-fraction target or None)
+BENCH_CONFIGS = [("1", "dense_small", None), ("2a", "dense_tall_a", 0.75), ("2b", "dense_tall_b", 0.75),
                     ("2c", "dense_tall_c", 0.75), ("3", "dense_wide", 0.75), ("4", "csr_uniform", 0.5),
                     ("5", "csr_powerlaw", 0.5)]
 HEADLINE = "dense_tall_b"
@@ -864,7 +864,7 @@ def config_summary(label, target, rec):
     return d
 
 
-# rows beyond BASELINE's configurations measured in the default run: the multi-vector form
+# rows beyond the benchmark configurations measured in the default run: the multi-vector form
 NEXT_WORKLOADS = [("multi_k8", "dense_multi"), ("multi_k16", "dense_multi_k16"), ("multi_k32", "dense_multi_k32")]
 
 
@@ -891,7 +891,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="fused", choices=["fused", "reference"])
     ap.add_argument("--workload", default=None, choices=sorted(WORKLOADS),
-                    help="one workload only (default: the headline, with every BASELINE configuration nested)")
+                    help="one workload only (default: the headline, with every benchmark configuration nested)")
     ap.add_argument("--headline-only", action="store_true", help="skip the nested configurations")
     ap.add_argument("--all", action="store_true", help="one line per workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -909,7 +909,7 @@ def main():
 
     rank, world, local = dist_env()
     names = sorted(WORKLOADS) if args.all else [args.workload or HEADLINE]
-    # the default run nests every BASELINE configuration in the headline's line
+    # the default run nests every benchmark configuration in the headline's line
     nest = not args.all and args.workload is None and not args.headline_only and args.impl == "fused"
     if args.solver:
         if rank == 0:
@@ -966,7 +966,7 @@ def main():
         del p
         if nest:
             rec["configs"] = {}
-            for label, wl, target in BASELINE_CONFIGS:
+            for label, wl, target in BENCH_CONFIGS:
                 if wl == name:
                     rec["configs"][label] = config_summary(label, target, rec)
                     continue
@@ -978,7 +978,7 @@ def main():
                 rec["configs"][label] = config_summary(label, target, r)
                 del q, r
                 torch.cuda.empty_cache()
-            rec["config"]["configs_note"] = ("headline: BASELINE configuration 2 (dense f32 16,000,000 x 32, "
+            rec["config"]["configs_note"] = ("headline: configuration 2 (dense f32 16,000,000 x 32, "
                                              "alpha=2, beta=-1); every configuration, the headline included, "
                                              "under `configs`, each measured in this run; the multi-vector form "
                                              "(k = 8, 16, 32 on the same X) under `next`")
