@@ -28,15 +28,15 @@
 // Roles (one CTA per SM, persistent over a contiguous range of tiles), linked by mbarriers
 // only:
 //   warp 0       one thread: tensor copies of X tiles (128 x 32 fp32, 128-byte swizzle);
-//   warp 1       the product loop, run by the whole warp (converged), one elected lane
-//                issuing the products and committing them to mbarriers;
+//   warp 1       the products (at kb = 8 U's only, the last warp issuing W's): each loop run
+//                by a whole (converged) warp, one elected lane issuing and committing;
 //   warps 2..    split warps, one group of four (two at kb = 8, taking alternate tiles): one
 //                row each, X into its three terms in an operand buffer;
 //   next 8 warps row warps, two groups of four (tensor-memory lanes 32 (warp % 4) ..),
 //                taking alternate tiles (kb = 32: every tile, half of the right-hand sides
 //                each): each row's U from tensor memory, t = v u and its terms into the T
 //                buffer; every four tiles, W folded into the column sums;
-//   last warp    one thread: tensor copies of the tiles' rows of V (swizzled at their width).
+//   next warp    one thread: tensor copies of the tiles' rows of V (swizzled at their width).
 //
 // Shared-memory operand layouts (no swizzle; core matrices of 8 rows x 16 bytes):
 //   X terms   128 tile rows x 96 columns (term a's column j at 32 a + j): the 16 bytes of
@@ -172,7 +172,11 @@ struct TcCfg {
   static constexpr int TARRIVE = CS ? 8 : 4;          // row warps that form each tile's T
   static constexpr int SG = KB == 8 ? 2 : 1;          // split-warp groups (alternate tiles; registers allow 2 at kb = 8)
   static constexpr int ROW0 = 2 + 4 * SG;             // first row warp
-  static constexpr int WARPS = ROW0 + 4 * RG + 1;     // producers, products, split warps, row warps
+  // at kb = 8 U's and W's products are issued by two warps (each then carries half of the
+  // product loop's waits); at 16 and 32 one warp issues both, in an order (U of tile i, W of
+  // tile i - 1) that keeps W, and so the release of the T and X-term buffers, early
+  static constexpr bool TWO_MMA = KB == 8;
+  static constexpr int WARPS = ROW0 + 4 * RG + (TWO_MMA ? 2 : 1);  // ... split, row, V copies[, W products]
   static constexpr int THREADS = 32 * WARPS;
   static constexpr int LBO_T = (NW / 8) * 128;        // core stride along K (rows) of the T terms
   static constexpr int TBUF = TC_ROWS * NW * 2;       // bytes of one tile's T terms
@@ -200,7 +204,8 @@ __global__ void __launch_bounds__(TcCfg<KB>::THREADS, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t xfull[SX], xfree[SX], vfull[SV], vfree[SV];
-  __shared__ __align__(8) uint64_t aready[NA], opfree[NA], tready[NT], tfree[NT], uready[2], wready[2], fin_bar;
+  __shared__ __align__(8) uint64_t aready[NA], opfree[NA], tready[NT], tfree[NT], uready[2], ufree[2], wready[2];
+  __shared__ __align__(8) uint64_t fin_bar, fin_w_bar;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   volatile int* abort_word = &s_abort;
@@ -237,8 +242,13 @@ __global__ void __launch_bounds__(TcCfg<KB>::THREADS, 1)
     for (int s = 0; s < SV; ++s) { mbar_init(&vfull[s], 1); mbar_init(&vfree[s], C::TARRIVE); }
     for (int s = 0; s < NA; ++s) { mbar_init(&aready[s], 4); mbar_init(&opfree[s], 1); }
     for (int s = 0; s < NT; ++s) { mbar_init(&tready[s], C::TARRIVE); mbar_init(&tfree[s], 1); }
-    for (int s = 0; s < 2; ++s) { mbar_init(&uready[s], 1); mbar_init(&wready[s], 1); }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&uready[s], 1);
+      mbar_init(&ufree[s], C::TARRIVE);
+      mbar_init(&wready[s], 1);
+    }
     mbar_init(&fin_bar, 1);
+    mbar_init(&fin_w_bar, 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -258,8 +268,8 @@ __global__ void __launch_bounds__(TcCfg<KB>::THREADS, 1)
   // `lane` (tensor-memory lane 32 q + lane of W), for its group's right-hand sides
   CompF32 acc[C::KC];
 
-  if (warp == 0 || warp == C::WARPS - 1) {
-    // ---- tensor copies: X tiles (warp 0), rows of V (the last warp) ----
+  if (warp == 0 || warp == C::ROW0 + 4 * C::RG) {
+    // ---- tensor copies: X tiles (warp 0), rows of V (the warp after the row warps) ----
     const bool is_x = warp == 0;
     if (lane == 0 && (is_x || v_staged)) {
       const uint64_t policy = policy_evict_first();
@@ -295,9 +305,10 @@ __global__ void __launch_bounds__(TcCfg<KB>::THREADS, 1)
       for (int j = issued > S ? issued - S : 0; j < issued; ++j)
         mbar_wait_bounded(&full[j % S], (uint32_t)((j / S) & 1));
     }
-  } else if (warp == 1) {
-    // ---- the products: the whole warp runs the loop (converged control flow keeps the
-    // descriptors in uniform registers) and one elected lane issues ----
+  } else if (warp == 1 || (C::TWO_MMA && warp == C::WARPS - 1)) {
+    // ---- the products: warp 1 (and at kb = 8 the last warp, for W's) runs its loop as a
+    // converged warp (the descriptors stay warp-uniform) and one elected lane issues ----
+    const bool is_u = warp == 1;
     constexpr uint32_t idesc_u = tc_idesc(128, NW, 0), idesc_w = tc_idesc(128, NW, 1);
     const uint64_t a_u0 = smem_desc(smem_addr(as), 2048, 128);      // X terms, K-major (M = rows)
     const uint64_t a_w0 = smem_desc(smem_addr(as), 128, 2048);      // X terms, MN-major (M = columns)
@@ -332,25 +343,48 @@ __global__ void __launch_bounds__(TcCfg<KB>::THREADS, 1)
       }
       __syncwarp();
     };
-    int i = 0;
-    for (; i < nt; ++i) {
-      if (!wait_all(&aready[i % NA], (uint32_t)((i / NA) & 1))) break;
-      tc_fence_after();
-      issue_u(i);
-      if (i >= 1) {
-        if (!wait_all(&tready[(i - 1) % NT], (uint32_t)(((i - 1) / NT) & 1))) break;
+    if constexpr (C::TWO_MMA) {
+      if (is_u) {
+        // U of tile i once its X terms are in place and U's accumulator i % 2 has been read
+        // (by the row warps, for tile i - 2)
+        for (int i = 0; i < nt; ++i) {
+          if (!wait_all(&aready[i % NA], (uint32_t)((i / NA) & 1))) break;
+          if (i >= 2 && !wait_all(&ufree[i & 1], (uint32_t)(((i - 2) >> 1) & 1))) break;
+          tc_fence_after();
+          issue_u(i);
+        }
+      } else {
+        // W of tile j once its T terms are in place
+        for (int j = 0; j < nt; ++j) {
+          if (!wait_all(&tready[j % NT], (uint32_t)((j / NT) & 1))) break;
+          tc_fence_after();
+          issue_w(j);
+        }
+      }
+    } else {
+      // U of tile i, then W of tile i - 1: U's accumulator i % 2 is free again, since this
+      // loop waited for tile i - 2's T (formed from that U) one step before
+      int i = 0;
+      for (; i < nt; ++i) {
+        if (!wait_all(&aready[i % NA], (uint32_t)((i / NA) & 1))) break;
         tc_fence_after();
-        issue_w(i - 1);
+        issue_u(i);
+        if (i >= 1) {
+          if (!wait_all(&tready[(i - 1) % NT], (uint32_t)(((i - 1) / NT) & 1))) break;
+          tc_fence_after();
+          issue_w(i - 1);
+        }
+      }
+      if (i == nt && nt > 0 && wait_all(&tready[(nt - 1) % NT], (uint32_t)(((nt - 1) / NT) & 1))) {
+        tc_fence_after();
+        issue_w(nt - 1);
       }
     }
-    if (i == nt && nt > 0 && wait_all(&tready[(nt - 1) % NT], (uint32_t)(((nt - 1) / NT) & 1))) {
-      tc_fence_after();
-      issue_w(nt - 1);
-    }
-    // every product issued has completed before tensor memory is released
-    if (leader) tc_commit(&fin_bar);
+    // every product this warp issued has completed before tensor memory is released
+    uint64_t* fin = is_u ? &fin_bar : &fin_w_bar;
+    if (leader) tc_commit(fin);
     __syncwarp();
-    mbar_wait_bounded(&fin_bar, 0);
+    mbar_wait_bounded(fin, 0);
   } else {
     // every lane of these warps takes the same branch after a wait
     auto wait_warp = [&](uint64_t* bar, uint32_t parity) -> bool { return warp_wait(bar, parity, abort_word); };
@@ -484,6 +518,7 @@ __global__ void __launch_bounds__(TcCfg<KB>::THREADS, 1)
         __syncwarp();
         if (lane == 0) {
           if (v_staged) mbar_arrive(&vfree[i % SV]);
+          if (C::TWO_MMA) mbar_arrive(&ufree[i & 1]);
           mbar_arrive(&tready[i % NT]);
         }
         // the previous tile group's sums, once this tile group's first tile is formed (a

@@ -116,7 +116,7 @@ def test_launch_model_grid_and_smem_limits():
 @pytest.mark.parametrize(
     "args,expect",
     [
-        (("f32", 16_000_000, 32, 8), "tma=1 tc=1 blocks=1 kb=8 passes=1 rows_per_tile=128 stages=6 warps=19 ctas=152"),
+        (("f32", 16_000_000, 32, 8), "tma=1 tc=1 blocks=1 kb=8 passes=1 rows_per_tile=128 stages=6 warps=20 ctas=152"),
         (("f32", 16_000_000, 32, 4), "tma=1 tc=0 blocks=1 kb=4 passes=1 rows_per_tile=64"),
         (("f32", 16_000_000, 32, 16), "tc=1 blocks=1 kb=16 passes=1"),
         (("f64", 16_000_000, 32, 8), "tc=0"),
