@@ -28,7 +28,7 @@
 // Roles (one CTA per SM, persistent over a contiguous range of tiles), linked by mbarriers
 // only:
 //   warp 0       one thread: tensor copies of X tiles (128 x 32 fp32, 128-byte swizzle);
-//   warp 1       the products (at kb = 8 U's only, the last warp issuing W's): each loop run
+//   warp 1       the products (at kb = 8, 16 U's only, the last warp issuing W's): each loop run
 //                by a whole (converged) warp, one elected lane issuing and committing;
 //   warps 2..    split warps, one group of four (two at kb = 8, taking alternate tiles): one
 //                row each, X into its three terms in an operand buffer;
@@ -161,10 +161,10 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 template <int KB>
 struct TcCfg {
   static constexpr int NW = (3 * KB + 15) / 16 * 16;  // N of both products (three terms of kb)
-  static constexpr int SX = KB == 8 ? 6 : (KB == 16 ? 5 : 3);  // X stages
+  static constexpr int SX = KB == 8 ? 6 : (KB == 16 ? 4 : 3);  // X stages
   static constexpr int SV = KB == 8 ? 6 : (KB == 16 ? 4 : 3);  // V stages
   static constexpr int NA = 3;                        // X-terms buffers
-  static constexpr int NT = KB <= 16 ? 2 : 1;         // T-terms buffers
+  static constexpr int NT = KB == 8 ? 2 : (KB == 16 ? 3 : 1);  // T-terms buffers
   static constexpr int G = 4;                         // tiles summed in tensor memory per W drain
   static constexpr int RG = 2;                        // row-warp groups
   static constexpr bool CS = KB == 32;                // groups split the columns (else alternate tiles)
@@ -172,10 +172,11 @@ struct TcCfg {
   static constexpr int TARRIVE = CS ? 8 : 4;          // row warps that form each tile's T
   static constexpr int SG = KB == 8 ? 2 : 1;          // split-warp groups (alternate tiles; registers allow 2 at kb = 8)
   static constexpr int ROW0 = 2 + 4 * SG;             // first row warp
-  // at kb = 8 U's and W's products are issued by two warps (each then carries half of the
-  // product loop's waits); at 16 and 32 one warp issues both, in an order (U of tile i, W of
-  // tile i - 1) that keeps W, and so the release of the T and X-term buffers, early
-  static constexpr bool TWO_MMA = KB == 8;
+  // at kb = 8 and 16 U's and W's products are issued by two warps (each then carries half of
+  // the product loop's waits; kb = 16 takes a third T buffer for it, so that U running ahead
+  // does not hold up the T buffers' release); at 32 (one T buffer) one warp issues both, in
+  // an order (U of tile i, W of tile i - 1) that keeps W, and so that release, early
+  static constexpr bool TWO_MMA = KB <= 16;
   static constexpr int WARPS = ROW0 + 4 * RG + (TWO_MMA ? 2 : 1);  // ... split, row, V copies[, W products]
   static constexpr int THREADS = 32 * WARPS;
   static constexpr int LBO_T = (NW / 8) * 128;        // core stride along K (rows) of the T terms
@@ -306,7 +307,7 @@ __global__ void __launch_bounds__(TcCfg<KB>::THREADS, 1)
         mbar_wait_bounded(&full[j % S], (uint32_t)((j / S) & 1));
     }
   } else if (warp == 1 || (C::TWO_MMA && warp == C::WARPS - 1)) {
-    // ---- the products: warp 1 (and at kb = 8 the last warp, for W's) runs its loop as a
+    // ---- the products: warp 1 (and at kb = 8, 16 the last warp, for W's) runs its loop as a
     // converged warp (the descriptors stay warp-uniform) and one elected lane issues ----
     const bool is_u = warp == 1;
     constexpr uint32_t idesc_u = tc_idesc(128, NW, 0), idesc_w = tc_idesc(128, NW, 1);
