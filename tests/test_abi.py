@@ -177,3 +177,29 @@ def test_multi_tensor_core_estimate():
         hbm_us = (16_000_000 * 32 * 4 + 16_000_000 * k * 4) / 6.8e12 * 1e6
         assert est[k] >= hbm_us, (k, est[k], hbm_us)
     assert est[8] < est[16] < est[32]
+
+
+@pytest.mark.parametrize("args,tc", [
+    (("f32", 1_000_000, 32, 7), "0"), (("f32", 1_000_000, 32, 8), "1"),
+    (("f32", 1_000_000, 33, 8), "0"), (("f32", 1_000_000, 1, 8), "1"),
+    (("f64", 1_000_000, 16, 8), "0"), (("f32", 1_000_000, 32, 100), "1"),
+    (("f32", 1_000_000, 32, 8, "full", 33), "0"),  # a pitch tensor copies cannot take
+])
+def test_multi_tensor_core_choice(args, tc):
+    f = dict(kv.split("=") for kv in fx.multi_plan_describe(*args).split()[1:])
+    assert f["tc"] == tc, (args, f)
+
+
+def test_multi_tensor_core_switch():
+    """FXTX_MULTI_TC=0, read when the library first plans such a call, keeps the shapes the
+    tensor cores would take on the CUDA-core kernel."""
+    import subprocess
+    import sys
+
+    code = ("import dense_linear_algebra_gb300 as fx; "
+            "print(fx.multi_plan_describe('f32', 1000000, 32, 8, 'full'))")
+    env = dict(os.environ, FXTX_MULTI_TC="0")
+    out = subprocess.run([sys.executable, "-c", code], env=env, cwd=ROOT, capture_output=True, text=True,
+                         timeout=300)
+    assert out.returncode == 0, out.stderr
+    assert " tc=0 " in out.stdout, out.stdout
