@@ -181,7 +181,7 @@ def test_multi_tensor_core_estimate():
 
 @pytest.mark.parametrize("args,tc", [
     (("f32", 1_000_000, 32, 7), "0"), (("f32", 1_000_000, 32, 8), "1"),
-    (("f32", 1_000_000, 33, 8), "0"), (("f32", 1_000_000, 1, 8), "1"),
+    (("f32", 1_000_000, 33, 8), "0"), (("f32", 1_000_000, 4, 8), "1"), (("f32", 1_000_000, 1, 8), "0"),
     (("f64", 1_000_000, 16, 8), "0"), (("f32", 1_000_000, 32, 100), "1"),
     (("f32", 1_000_000, 32, 8, "full", 33), "0"),  # a pitch tensor copies cannot take
 ])
