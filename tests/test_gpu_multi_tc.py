@@ -64,8 +64,21 @@ def test_ragged_rows(m, k):
 @pytest.mark.parametrize("k", [8, 9, 16, 17, 32])
 def test_columns_and_partial_passes(n, k):
     """X narrower than the 32-column tile (the copy fills the rest with zeros) and passes
-    with fewer right-hand sides than the kernel's width."""
-    check(*make(20_000, n, k, seed=n * 100 + k), what=f"n={n} k={k}")
+    with fewer right-hand sides than the kernel's width. X is a column slice of a matrix
+    whose pitch is a multiple of 16 bytes, so the tensor copies (and the tensor cores) take
+    it; with the pitch n itself, rows of 1, 7 or 31 values go to the CUDA-core kernel."""
+    X, Y, V, Z, alpha, beta = make(20_000, n, k, seed=n * 100 + k)
+    ld = (n + 3) // 4 * 4
+    assert "tc=1" in fx.multi_plan_describe("f32", X.shape[0], n, k, "full", ld)
+    Xp = torch.zeros(X.shape[0], ld, device="cuda")
+    Xp[:, :n] = dev(X)
+    got = fx.dense_multi(Xp[:, :n], dev(Y), dev(V), alpha, beta, dev(Z))
+    torch.cuda.synchronize()
+    assert fx.device_error() == fx.FXTX_OK
+    check(X, Y, V, Z, alpha, beta, got=got.cpu().numpy(), what=f"n={n} ld={ld} k={k}")
+    if n % 4:
+        assert "tc=0" in fx.multi_plan_describe("f32", X.shape[0], n, k, "full", n)
+        check(X, Y, V, Z, alpha, beta, what=f"n={n} ld={n} k={k} (CUDA cores)")
 
 
 @pytest.mark.parametrize("v_mode", ["full", "shared", "none"])
