@@ -485,10 +485,10 @@ MultiPlan plan_multi(const DeviceInfo& dev, int64_t m, int64_t n, int64_t k, int
   const double bytes = (double)m * n * elem * p.passes + vbytes + 3.0 * n * k * elem;
   if (p.tc) {
     // the tensor-core form: its pipeline of roles takes a measured number of SM cycles per
-    // 128-row tile (16,000,000 x 32 on GB300 at 2,070 MHz: 592, 757 and 1,243 us per call at
-    // kb = 8, 16 and 32, i.e. ~1,490, ~1,910 and ~3,130 cycles a tile; the product warps'
+    // 128-row tile (16,000,000 x 32 on GB300 at 2,070 MHz: 592, 757 and 1,144 us per call at
+    // kb = 8, 16 and 32, i.e. ~1,490, ~1,910 and ~2,880 cycles a tile; the product warps'
     // issue and waits, not HBM, set it), or the HBM time if that is longer
-    const double cyc = p.kb_max == 8 ? 1490.0 : (p.kb_max == 16 ? 1910.0 : 3130.0);
+    const double cyc = p.kb_max == 8 ? 1490.0 : (p.kb_max == 16 ? 1910.0 : 2880.0);
     const double tiles_per_cta = std::ceil((double)((m + 127) / 128) / std::max(p.ctas, 1));
     const double hbm_us = roofline_us(dev, bytes, 0.9, 0.0, elem, 1.0, 0.0, 1.0);  // includes the launch
     p.est_us = std::max(sm_cycles_us(tiles_per_cta * cyc * p.passes), hbm_us) + 4.0 * (p.passes - 1);

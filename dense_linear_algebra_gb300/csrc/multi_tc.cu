@@ -28,8 +28,8 @@
 // Roles (one CTA per SM, persistent over a contiguous range of tiles), linked by mbarriers
 // only:
 //   warp 0       one thread: tensor copies of X tiles (128 x 32 fp32, 128-byte swizzle);
-//   warp 1       the products (at kb = 8, 16 U's only, the last warp issuing W's): each loop run
-//                by a whole (converged) warp, one elected lane issuing and committing;
+//   warp 1       U's products, and the last warp W's: each loop run by a whole (converged)
+//                warp, one elected lane issuing and committing to mbarriers;
 //   warps 2..    split warps, one group of four (two at kb = 8, taking alternate tiles): one
 //                row each, X into its three terms in an operand buffer;
 //   next 8 warps row warps, two groups of four (tensor-memory lanes 32 (warp % 4) ..),
@@ -162,9 +162,9 @@ template <int KB>
 struct TcCfg {
   static constexpr int NW = (3 * KB + 15) / 16 * 16;  // N of both products (three terms of kb)
   static constexpr int SX = KB == 8 ? 6 : (KB == 16 ? 4 : 3);  // X stages
-  static constexpr int SV = KB == 8 ? 6 : (KB == 16 ? 4 : 3);  // V stages
+  static constexpr int SV = KB == 8 ? 6 : (KB == 16 ? 4 : 2);  // V stages
   static constexpr int NA = 3;                        // X-terms buffers
-  static constexpr int NT = KB == 8 ? 2 : (KB == 16 ? 3 : 1);  // T-terms buffers
+  static constexpr int NT = KB == 8 ? 2 : (KB == 16 ? 3 : 2);  // T-terms buffers
   static constexpr int G = 4;                         // tiles summed in tensor memory per W drain
   static constexpr int RG = 2;                        // row-warp groups
   static constexpr bool CS = KB == 32;                // groups split the columns (else alternate tiles)
@@ -172,12 +172,10 @@ struct TcCfg {
   static constexpr int TARRIVE = CS ? 8 : 4;          // row warps that form each tile's T
   static constexpr int SG = KB == 8 ? 2 : 1;          // split-warp groups (alternate tiles; registers allow 2 at kb = 8)
   static constexpr int ROW0 = 2 + 4 * SG;             // first row warp
-  // at kb = 8 and 16 U's and W's products are issued by two warps (each then carries half of
-  // the product loop's waits; kb = 16 takes a third T buffer for it, so that U running ahead
-  // does not hold up the T buffers' release); at 32 (one T buffer) one warp issues both, in
-  // an order (U of tile i, W of tile i - 1) that keeps W, and so that release, early
-  static constexpr bool TWO_MMA = KB <= 16;
-  static constexpr int WARPS = ROW0 + 4 * RG + (TWO_MMA ? 2 : 1);  // ... split, row, V copies[, W products]
+  // U's and W's products are issued by two warps, each carrying half of the product loop's
+  // waits; U may then run ahead of W, so the T buffers (released by W's products) are at
+  // least two, and three at kb = 16
+  static constexpr int WARPS = ROW0 + 4 * RG + 2;     // producers, U products, split, row, V copies, W products
   static constexpr int THREADS = 32 * WARPS;
   static constexpr int LBO_T = (NW / 8) * 128;        // core stride along K (rows) of the T terms
   static constexpr int TBUF = TC_ROWS * NW * 2;       // bytes of one tile's T terms
@@ -306,8 +304,8 @@ __global__ void __launch_bounds__(TcCfg<KB>::THREADS, 1)
       for (int j = issued > S ? issued - S : 0; j < issued; ++j)
         mbar_wait_bounded(&full[j % S], (uint32_t)((j / S) & 1));
     }
-  } else if (warp == 1 || (C::TWO_MMA && warp == C::WARPS - 1)) {
-    // ---- the products: warp 1 (and at kb = 8, 16 the last warp, for W's) runs its loop as a
+  } else if (warp == 1 || warp == C::WARPS - 1) {
+    // ---- the products: warp 1 issues U's, the last warp W's; each runs its loop as a
     // converged warp (the descriptors stay warp-uniform) and one elected lane issues ----
     const bool is_u = warp == 1;
     constexpr uint32_t idesc_u = tc_idesc(128, NW, 0), idesc_w = tc_idesc(128, NW, 1);
@@ -344,41 +342,21 @@ __global__ void __launch_bounds__(TcCfg<KB>::THREADS, 1)
       }
       __syncwarp();
     };
-    if constexpr (C::TWO_MMA) {
-      if (is_u) {
-        // U of tile i once its X terms are in place and U's accumulator i % 2 has been read
-        // (by the row warps, for tile i - 2)
-        for (int i = 0; i < nt; ++i) {
-          if (!wait_all(&aready[i % NA], (uint32_t)((i / NA) & 1))) break;
-          if (i >= 2 && !wait_all(&ufree[i & 1], (uint32_t)(((i - 2) >> 1) & 1))) break;
-          tc_fence_after();
-          issue_u(i);
-        }
-      } else {
-        // W of tile j once its T terms are in place
-        for (int j = 0; j < nt; ++j) {
-          if (!wait_all(&tready[j % NT], (uint32_t)((j / NT) & 1))) break;
-          tc_fence_after();
-          issue_w(j);
-        }
-      }
-    } else {
-      // U of tile i, then W of tile i - 1: U's accumulator i % 2 is free again, since this
-      // loop waited for tile i - 2's T (formed from that U) one step before
-      int i = 0;
-      for (; i < nt; ++i) {
+    if (is_u) {
+      // U of tile i once its X terms are in place and U's accumulator i % 2 has been read
+      // (by the row warps, for tile i - 2)
+      for (int i = 0; i < nt; ++i) {
         if (!wait_all(&aready[i % NA], (uint32_t)((i / NA) & 1))) break;
+        if (i >= 2 && !wait_all(&ufree[i & 1], (uint32_t)(((i - 2) >> 1) & 1))) break;
         tc_fence_after();
         issue_u(i);
-        if (i >= 1) {
-          if (!wait_all(&tready[(i - 1) % NT], (uint32_t)(((i - 1) / NT) & 1))) break;
-          tc_fence_after();
-          issue_w(i - 1);
-        }
       }
-      if (i == nt && nt > 0 && wait_all(&tready[(nt - 1) % NT], (uint32_t)(((nt - 1) / NT) & 1))) {
+    } else {
+      // W of tile j once its T terms are in place
+      for (int j = 0; j < nt; ++j) {
+        if (!wait_all(&tready[j % NT], (uint32_t)((j / NT) & 1))) break;
         tc_fence_after();
-        issue_w(nt - 1);
+        issue_w(j);
       }
     }
     // every product this warp issued has completed before tensor memory is released
@@ -519,7 +497,7 @@ __global__ void __launch_bounds__(TcCfg<KB>::THREADS, 1)
         __syncwarp();
         if (lane == 0) {
           if (v_staged) mbar_arrive(&vfree[i % SV]);
-          if (C::TWO_MMA) mbar_arrive(&ufree[i & 1]);
+          mbar_arrive(&ufree[i & 1]);
           mbar_arrive(&tready[i % NT]);
         }
         // the previous tile group's sums, once this tile group's first tile is formed (a
